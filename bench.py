@@ -1,0 +1,500 @@
+#!/usr/bin/env python3
+"""Benchmark of the F16-weight products on one GB300 (or N replicas).
+
+Default workload: a SmolLM2-135M-shaped decode step -- 30 layers of
+[round -> fused Q/K/V GEMV (576+192+192 rows x 576), round -> O (576 x 576),
+ round -> fused gate/up GEMV (2 x 1536 x 576), round -> down (576 x 1536)]
+then round -> tied logits (49152 x 576): 1 column, 242 C-ABI calls, 269 MB of
+f16 weights (more than the 129 MB L2), seeded synthetic weights N(0, 0.02)
+and activations N(0, 1).  The step is captured once as a CUDA graph of those
+calls and replayed; `value` is algorithmic bytes per step / time per step.
+
+Extra lines in the same JSON object:
+  roofline     -- the one-column GEMV kernel alone (graph of the step's GEMV
+                  launches, no rounding kernels), achieved GB/s vs measured HBM peak
+  products     -- single products of the Llama-3-8B / Qwen3-0.6B shapes:
+                  decode GB/s and 512-column tensor-core TFLOP/s
+  e2e          -- the same step through the Python binding, eagerly, with the
+                  step's activations copied from pinned host memory and the logits
+                  copied back every step
+  cpu_baseline -- the CPU oracle on this host, full decode steps
+
+`--impl reference` times the CPU oracle (the only reference that exists for
+this method) on the same workload and prints the same JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+HIDDEN, FFN, VOCAB, LAYERS = 576, 1536, 49152, 30
+Q_ROWS, KV_ROWS = 9 * 64, 3 * 64
+SEED = 0
+W_SIGMA, A_SIGMA = 0.02, 1.0
+
+
+def algorithmic_bytes(rows, k, ncols=1):
+    return 2 * rows * k + 2 * k * ncols + 4 * rows * ncols
+
+
+def step_plan():
+    """The decode step as an ordered list of calls: ('round', n, act_id) or
+    ('multi'|'mv'|'logits', [(name, rows)], k, act_id)."""
+    plan = []
+    a = 0
+    for L in range(LAYERS):
+        plan.append(("round", HIDDEN, a))
+        plan.append(("multi", [("l%d.q" % L, Q_ROWS), ("l%d.k" % L, KV_ROWS), ("l%d.v" % L, KV_ROWS)], HIDDEN, a))
+        a += 1
+        plan.append(("round", HIDDEN, a))
+        plan.append(("mv", [("l%d.o" % L, HIDDEN)], HIDDEN, a))
+        a += 1
+        plan.append(("round", HIDDEN, a))
+        plan.append(("multi", [("l%d.gate" % L, FFN), ("l%d.up" % L, FFN)], HIDDEN, a))
+        a += 1
+        plan.append(("round", FFN, a))
+        plan.append(("mv", [("l%d.down" % L, HIDDEN)], FFN, a))
+        a += 1
+    plan.append(("round", HIDDEN, a))
+    plan.append(("logits", [("token_embd", VOCAB)], HIDDEN, a))
+    return plan
+
+
+def step_bytes(plan):
+    tot = gemv = 0
+    for op in plan:
+        if op[0] == "round":
+            tot += 6 * op[1]
+        else:
+            b = sum(algorithmic_bytes(r, op[2]) for _, r in op[1])
+            b -= 2 * op[2] * (len(op[1]) - 1)  # one shared activation read per fused call
+            tot += b
+            gemv += b
+    return tot, gemv
+
+
+def act_sizes(plan):
+    sizes = {}
+    for op in plan:
+        if op[0] == "round":
+            sizes[op[2]] = op[1]
+    return sizes
+
+
+# ----------------------------------------------------------------------------- clocks
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                                          "-i", str(self.index), "-lms", "100"], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self):
+        return time.time()
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        rows = []
+        for t, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((t, float(parts[1]), float(parts[2]), parts[4:9]))
+            except ValueError:
+                continue
+        inside = [r for r in rows if t0 - 0.15 <= r[0] <= t1 + 0.15] or rows[-3:]
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in inside:
+            for n, v in zip(names[1:], r[3][1:]):
+                if v.lower() not in ("not active", "0x0000000000000000", "0", "[n/a]", "n/a"):
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median([r[1] for r in inside])), "sm_max_mhz": max(r[2] for r in inside),
+                "reasons": sorted(reasons), "samples": len(inside)}
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+
+def run_gpu(args, rank, world, local_rank):
+    import torch
+
+    import f16_weight_gemv_gb300 as bm
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    bm.lib()
+    plan = step_plan()
+    tot_bytes, gemv_bytes = step_bytes(plan)
+
+    # ---- weights and activations (seeded, generated on the host once, then resident)
+    weights = {}
+    for op in plan:
+        if op[0] == "round":
+            continue
+        for name, rows in op[1]:
+            w = synth.normal_f16(SEED, "smollm2." + name, W_SIGMA, (rows, op[2]))
+            weights[name] = torch.from_numpy(w.view(np.float16)).to(dev)
+    sizes = act_sizes(plan)
+    offs, o = {}, 0
+    for a in sorted(sizes):
+        offs[a] = o
+        o += (sizes[a] + 7) // 8 * 8  # 32-byte aligned slices
+    act_host = np.zeros(o, dtype=np.float32)
+    for a in sorted(sizes):
+        act_host[offs[a]:offs[a] + sizes[a]] = synth.normal_f32(SEED, "smollm2.act%d" % a, A_SIGMA, sizes[a])
+    act_f32 = torch.from_numpy(act_host).to(dev)
+    act_f16 = torch.empty(o, dtype=torch.float16, device=dev)
+    outs = {}
+    for op in plan:
+        if op[0] != "round":
+            for name, rows in op[1]:
+                outs[name] = torch.empty(rows, dtype=torch.float32, device=dev)
+
+    stream = torch.cuda.Stream(device=dev)
+
+    def run_step(s, gemv_only=False):
+        for op in plan:
+            if op[0] == "round":
+                if not gemv_only:
+                    a = op[2]
+                    bm.bm_to_f16(act_f32[offs[a]:offs[a] + op[1]], act_f16[offs[a]:offs[a] + op[1]], stream=s)
+                continue
+            kind, mats, k, a = op
+            x = act_f16[offs[a]:offs[a] + k]
+            if kind == "multi":
+                bm.bm_f16_matvec_multi([weights[n] for n, _ in mats], x, [outs[n] for n, _ in mats], stream=s)
+            elif kind == "mv":
+                bm.bm_f16_matvec(weights[mats[0][0]], x, outs[mats[0][0]], stream=s)
+            else:
+                bm.bm_f16_logits(weights[mats[0][0]], x.view(1, -1), outs[mats[0][0]].view(1, -1), stream=s)
+
+    launches_per_step = len(plan)
+    gemv_launches = sum(1 for op in plan if op[0] != "round")
+
+    def capture(gemv_only):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            run_step(stream, gemv_only)  # warm (attribute setup happens outside capture)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            run_step(stream, gemv_only)
+        torch.cuda.synchronize()
+        return g
+
+    g_step = capture(False)
+    g_gemv = capture(True)
+
+    def timed(g, steps, warmup):
+        for _ in range(warmup):
+            g.replay()
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(steps):
+                g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        return e0.elapsed_time(e1) / steps  # ms per step
+
+    clocks = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ else
+                          int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local_rank]))
+    clocks.start()
+    time.sleep(0.3)
+    t_begin = time.time()
+    ms = timed(g_step, args.steps, args.warmup)
+    t_end = time.time()
+    ms_gemv = timed(g_gemv, max(args.steps, 20), args.warmup)
+    clk = clocks.summary(t_begin, t_end)
+    clocks.stop()
+
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # ---- end to end through the binding: pinned H2D of the step's activations, eager
+    # calls, D2H of the logits, every step
+    act_pinned = torch.from_numpy(act_host).pin_memory()
+    logits_host = torch.empty(VOCAB, dtype=torch.float32).pin_memory()
+    e2e_steps = max(3, min(args.steps, 50))
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            act_f32.copy_(act_pinned, non_blocking=True)
+            run_step(stream)
+            logits_host.copy_(outs["token_embd"], non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms_e2e = e0.elapsed_time(e1) / e2e_steps
+
+    result = {
+        "ms": ms, "ms_gemv": ms_gemv, "ms_e2e": ms_e2e, "tot_bytes": tot_bytes, "gemv_bytes": gemv_bytes,
+        "launches_per_step": launches_per_step, "gemv_launches": gemv_launches, "clocks": clk,
+        "h2d": int(act_host.nbytes), "d2h": int(VOCAB * 4),
+    }
+    if rank == 0 and not args.no_products:
+        result["products"] = bench_products(bm, dev, stream, torch)
+    return result
+
+
+def bench_products(bm, dev, stream, torch):
+    """Single products at full size: decode GEMV and 512-column tensor-core GEMM."""
+    out = []
+    l2_flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+
+    def time_call(fn, reps=10):
+        with torch.cuda.stream(stream):
+            for _ in range(2):
+                fn()
+            torch.cuda.synchronize()
+            tot = 0.0
+            for _ in range(reps):
+                l2_flush.fill_(1.0)  # evict the previous repetition's operands from L2
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+                torch.cuda.synchronize()
+                tot += e0.elapsed_time(e1)
+        return tot / reps
+
+    shapes = [("llama3_8b.q", 4096, 4096), ("llama3_8b.gate", 14336, 4096), ("llama3_8b.down", 4096, 14336),
+              ("llama3_8b.output", 128256, 4096), ("qwen3_0.6b.logits", 151936, 1024)]
+    for name, rows, k in shapes:
+        W = torch.from_numpy(synth.normal_f16(SEED, name, 0.01 if "llama" in name else 0.02, (rows, k))
+                             .view(np.float16)).to(dev)
+        x = torch.from_numpy(synth.normal_f16(SEED, name + ".x", 1.0, (512, k)).view(np.float16)).to(dev)
+        y = torch.empty(rows, dtype=torch.float32, device=dev)
+        ms = time_call(lambda: bm.bm_f16_matvec(W, x[0], y, stream=stream))
+        gbs = algorithmic_bytes(rows, k) / ms / 1e6
+        out.append({"product": name, "rows": rows, "k": k, "ncols": 1, "ms": round(ms, 5), "GB_s": round(gbs, 1)})
+        Y = torch.empty((512, rows), dtype=torch.float32, device=dev)
+        ms = time_call(lambda: bm.bm_f16_matmul(W, x, Y, stream=stream))
+        tf = 2.0 * rows * k * 512 / ms / 1e9
+        out.append({"product": name, "rows": rows, "k": k, "ncols": 512, "ms": round(ms, 5),
+                    "TFLOP_s": round(tf, 1), "GB_s": round(algorithmic_bytes(rows, k, 512) / ms / 1e6, 1)})
+        del W, x, y, Y
+    return out
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+
+
+def oracle_step_runner():
+    """The decode step on the CPU oracle: returns (run_one_step, bytes_per_step)."""
+    import oracle
+
+    plan = step_plan()
+    tot_bytes, _ = step_bytes(plan)
+    weights = {}
+    for op in plan:
+        if op[0] != "round":
+            for name, rows in op[1]:
+                weights[name] = synth.normal_f16(SEED, "smollm2." + name, W_SIGMA, (rows, op[2]))
+    acts = {a: synth.normal_f32(SEED, "smollm2.act%d" % a, A_SIGMA, n) for a, n in act_sizes(plan).items()}
+
+    def run():
+        h = {}
+        for op in plan:
+            if op[0] == "round":
+                h[op[2]] = oracle.to_f16(acts[op[2]])
+            elif op[0] == "multi":
+                oracle.matvec_multi([weights[n] for n, _ in op[1]], h[op[3]])
+            elif op[0] == "mv":
+                oracle.matvec(weights[op[1][0][0]], h[op[3]])
+            else:
+                oracle.matmul(weights[op[1][0][0]], h[op[3]][None, :])
+
+    return run, tot_bytes, oracle.threads()
+
+
+def cpu_baseline(budget_s=10.0):
+    run, nbytes, cores = oracle_step_runner()
+    run()
+    n = 0
+    t0 = time.perf_counter()
+    while True:
+        run()
+        n += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": round(nbytes * n / dt / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": "%d full SmolLM2-135M decode steps (30 layers + logits, 269 MB of f16 weights each) "
+                      "in %.1f s on the host" % (n, dt)}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    run, nbytes, cores = oracle_step_runner()
+    for _ in range(args.warmup):
+        run()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        run()
+    dt = time.perf_counter() - t0
+    ms = dt * 1e3 / args.steps
+    value = nbytes / (ms / 1e3) / 1e9
+    line = {
+        "impl": "reference", "metric": "decode F16 GEMV HBM GB/s (SmolLM2-135M decode step)",
+        "value": round(value, 4), "unit": "GB/s", "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16 weights, f32 accumulate", "data": "synthetic",
+        "config": {"workload": "smollm2_135m_decode_step", "layers": LAYERS, "hidden": HIDDEN, "ffn": FFN,
+                   "vocab": VOCAB, "ncols": 1, "seed": SEED, "l2": "inputs larger than L2 (269 MB)"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": "%d full decode steps after %d warm-up" % (args.steps, args.warmup)},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------- main
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-products", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl")
+    import __graft_entry__
+    if rank == 0 or not os.path.exists(os.path.join(ROOT, "f16_weight_gemv_gb300", "libbm.so")):
+        __graft_entry__.build()
+    if world > 1:
+        torch.distributed.barrier()
+
+    r = run_gpu(args, rank, world, local_rank)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    if rank != 0:
+        return 0
+
+    gpu_name = torch.cuda.get_device_name()
+    peaks = {}
+    try:
+        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except (OSError, ValueError):
+        pass
+    hbm_peak = float(peaks.get("hbm_gbs", 6800.0))
+    peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
+    value = r["tot_bytes"] * world / (r["ms"] / 1e3) / 1e9
+    achieved = r["gemv_bytes"] / (r["ms_gemv"] / 1e3) / 1e9
+    line = {
+        "metric": "decode F16 GEMV HBM GB/s (SmolLM2-135M decode step)",
+        "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(r["ms"], 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16 weights and activations, f32 accumulate (vec_dot bits)", "data": "synthetic",
+        "config": {"workload": "smollm2_135m_decode_step", "layers": LAYERS, "hidden": HIDDEN, "ffn": FFN,
+                   "q_rows": Q_ROWS, "kv_rows": KV_ROWS, "vocab": VOCAB, "ncols": 1, "seed": SEED,
+                   "weight_bytes": int(sum(2 * rows * op[2] for op in step_plan() if op[0] != "round"
+                                           for _, rows in op[1])),
+                   "l2": "inputs larger than L2 (269 MB of weights per step, cyclic)",
+                   "parallelism": "replicas" if world > 1 else "single GPU", "graph": "CUDA graph of the step"},
+        "pct_of_hbm_peak": round(100.0 * value / world / hbm_peak, 2),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                     "frac": round(achieved / hbm_peak, 4), "traffic": None,
+                     "kernel": "k_vecdot_rows4 (one-column GEMV)", "peak_source": peak_src,
+                     "launches_per_step": r["gemv_launches"],
+                     "how": "graph of the step's GEMV launches alone, CUDA events on the launch stream"},
+        "gpu_launches": r["launches_per_step"] * args.steps,
+        "clocks": r["clocks"],
+        "e2e": {"value": round(r["tot_bytes"] / (r["ms_e2e"] / 1e3) / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
+                "how": "eager calls through the Python binding; pinned host activations in, logits out"},
+        "device": gpu_name,
+    }
+    if "products" in r:
+        line["products"] = r["products"]
+        for p in r["products"]:
+            if p["ncols"] == 1:
+                p["pct_hbm"] = round(100.0 * p["GB_s"] / hbm_peak, 1)
+            else:
+                p["pct_bf16_dense_peak"] = round(100.0 * p["TFLOP_s"] / float(peaks.get("bf16_tflops", 1900.0)), 1)
+    if not args.no_cpu:
+        line["cpu_baseline"] = cpu_baseline()
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,194 @@
+"""Python binding of libbm.so (include/bm.h): argument marshalling only.
+
+Every function has the C entry point's name and takes torch CUDA tensors; f16
+data travels as ``torch.float16`` (or ``torch.int16``/``torch.uint16``) tensors
+whose bits are the IEEE binary16 patterns.  Nothing here computes: each call
+checks shapes, passes pointers and the current (or given) stream, and raises
+``BmError`` with the library's reason on a non-zero status.  There is no
+fallback: when libbm.so is missing the import fails.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import torch
+
+from . import _build
+
+__all__ = [
+    "BmError", "lib", "bm_to_f16", "bm_f16_matvec", "bm_f16_matvec_multi", "bm_f16_matmul",
+    "bm_f16_logits", "bm_takes_sgemm", "bm_device_status", "bm_status_string", "bm_last_error",
+    "bm_selftest_wait_timeout", "EXPORTS", "BM_MAX_K",
+]
+
+BM_OK, BM_ERR_INVALID_ARG, BM_ERR_ALIGNMENT, BM_ERR_UNSUPPORTED_DEVICE, BM_ERR_CUDA, BM_ERR_TIMEOUT = range(6)
+BM_MAX_K = 65536
+
+# Every symbol include/bm.h declares, with (restype, argtypes).
+_vp, _i64, _i = C.c_void_p, C.c_int64, C.c_int
+EXPORTS = {
+    "bm_to_f16": (_i, [_vp, _vp, _i64, _vp]),
+    "bm_f16_matvec": (_i, [_vp, _i64, _i64, _vp, _vp, _vp]),
+    "bm_f16_matvec_multi": (_i, [_i, C.POINTER(_vp), C.POINTER(_i64), _i64, _vp, C.POINTER(_vp), _vp]),
+    "bm_f16_matmul": (_i, [_vp, _i64, _i64, _vp, _i64, _vp, _vp]),
+    "bm_f16_logits": (_i, [_vp, _i64, _i64, _vp, _i64, _vp, _vp]),
+    "bm_takes_sgemm": (_i, [_i64, _i64, _i64]),
+    "bm_device_status": (_i, [_vp]),
+    "bm_selftest_wait_timeout": (_i, [_vp, _vp, _vp, _vp]),
+    "bm_status_string": (C.c_char_p, [_i]),
+    "bm_last_error": (C.c_char_p, []),
+}
+
+_LIB = None
+
+
+def lib(path: str | None = None):
+    """Load libbm.so (built in place by ``_build.build``)."""
+    global _LIB
+    if _LIB is None:
+        p = path or _build.LIB
+        if not os.path.exists(p):
+            raise ImportError("libbm.so is not built (run __graft_entry__.build()); there is no fallback")
+        L = C.CDLL(p)
+        for name, (res, args) in EXPORTS.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _LIB = L
+    return _LIB
+
+
+class BmError(RuntimeError):
+    def __init__(self, status: int, fn: str):
+        self.status = status
+        reason = lib().bm_last_error().decode(errors="replace")
+        text = lib().bm_status_string(status).decode()
+        super().__init__("%s: %s (%d): %s" % (fn, text, status, reason))
+
+
+def _check(status: int, fn: str):
+    if status != BM_OK:
+        raise BmError(status, fn)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+_F16_LIKE = (torch.float16, torch.int16, torch.uint16)
+
+
+def _dev(t: torch.Tensor, name: str, dtypes) -> int:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError("%s must be a CUDA tensor" % name)
+    if t.dtype not in dtypes:
+        raise TypeError("%s has dtype %s, expected one of %s" % (name, t.dtype, dtypes))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    return t.data_ptr()
+
+
+def bm_takes_sgemm(rows: int, k: int, ncols: int) -> bool:
+    return bool(lib().bm_takes_sgemm(rows, k, ncols))
+
+
+def bm_to_f16(x: torch.Tensor, h: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """f32 -> f16 bits, round to nearest even; returns h (torch.float16, same shape)."""
+    if h is None:
+        h = torch.empty(x.shape, dtype=torch.float16, device=x.device)
+    if h.numel() != x.numel():
+        raise ValueError("h must have x's size")
+    _check(lib().bm_to_f16(_dev(x, "x", (torch.float32,)), _dev(h, "h", _F16_LIKE), x.numel(), _stream(stream)),
+           "bm_to_f16")
+    return h
+
+
+def _wk(W: torch.Tensor):
+    if W.dim() != 2:
+        raise ValueError("W must be 2-D [rows][k]")
+    return W.shape[0], W.shape[1]
+
+
+def bm_f16_matvec(W: torch.Tensor, x: torch.Tensor, y: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    rows, k = _wk(W)
+    if x.numel() != k:
+        raise ValueError("x must have k elements")
+    if y is None:
+        y = torch.empty(rows, dtype=torch.float32, device=W.device)
+    if y.numel() != rows:
+        raise ValueError("y must have rows elements")
+    _check(lib().bm_f16_matvec(_dev(W, "W", _F16_LIKE), rows, k, _dev(x, "x", _F16_LIKE),
+                               _dev(y, "y", (torch.float32,)), _stream(stream)), "bm_f16_matvec")
+    return y
+
+
+def bm_f16_matvec_multi(Ws, x: torch.Tensor, ys=None, stream=None):
+    n = len(Ws)
+    k = x.numel()
+    if ys is None:
+        ys = [torch.empty(W.shape[0], dtype=torch.float32, device=x.device) for W in Ws]
+    if len(ys) != n:
+        raise ValueError("one output per matrix")
+    for W, y in zip(Ws, ys):
+        r, kk = _wk(W)
+        if kk != k or y.numel() != r:
+            raise ValueError("shape mismatch in bm_f16_matvec_multi")
+    wp = (C.c_void_p * max(n, 1))(*[_dev(W, "W", _F16_LIKE) for W in Ws])
+    yp = (C.c_void_p * max(n, 1))(*[_dev(y, "y", (torch.float32,)) for y in ys])
+    rows = (C.c_int64 * max(n, 1))(*[W.shape[0] for W in Ws])
+    _check(lib().bm_f16_matvec_multi(n, wp, rows, k, _dev(x, "x", _F16_LIKE), yp, _stream(stream)),
+           "bm_f16_matvec_multi")
+    return ys
+
+
+def _product(fn_name: str, W, X, Y, stream):
+    rows, k = _wk(W)
+    if X.dim() == 1:
+        X = X.view(1, -1)
+    ncols = X.shape[0]
+    if X.shape[1] != k:
+        raise ValueError("X must be [ncols][k]")
+    if Y is None:
+        Y = torch.empty((ncols, rows), dtype=torch.float32, device=W.device)
+    if Y.numel() != rows * ncols:
+        raise ValueError("Y must have ncols*rows elements")
+    fn = getattr(lib(), fn_name)
+    _check(fn(_dev(W, "W", _F16_LIKE), rows, k, _dev(X, "X", _F16_LIKE), ncols, _dev(Y, "Y", (torch.float32,)),
+              _stream(stream)), fn_name)
+    return Y
+
+
+def bm_f16_matmul(W, X, Y=None, stream=None):
+    """Y[c][r] (Y[c*rows + r] in memory) for W [rows][k] and X [ncols][k]."""
+    return _product("bm_f16_matmul", W, X, Y, stream)
+
+
+def bm_f16_logits(E, X, Y=None, stream=None):
+    """Logits over a tied embedding E [vocab][hidden]; Y[c][v]."""
+    return _product("bm_f16_logits", E, X, Y, stream)
+
+
+def bm_device_status(stream=None) -> int:
+    return int(lib().bm_device_status(_stream(stream)))
+
+
+def bm_selftest_wait_timeout(W, X, Y, stream=None) -> int:
+    return int(lib().bm_selftest_wait_timeout(_dev(W, "W", _F16_LIKE), _dev(X, "X", _F16_LIKE),
+                                              _dev(Y, "Y", (torch.float32,)), _stream(stream)))
+
+
+def bm_status_string(status: int) -> str:
+    return lib().bm_status_string(status).decode()
+
+
+def bm_last_error() -> str:
+    return lib().bm_last_error().decode(errors="replace")
+
+
+def build(force: bool = False) -> str:
+    return _build.build(force=force)

@@ -1,0 +1,250 @@
+// bm_api.cu -- the C ABI of include/bm.h: argument validation, path selection
+// and dispatch to the kernels.  Every check happens on the host before any
+// launch, so a non-zero status other than BM_ERR_CUDA means nothing ran.
+#include "../../include/bm.h"
+#include "bm_internal.h"
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+namespace bm {
+
+static thread_local char g_last_error[512];
+
+int fail(int status, const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+    va_end(ap);
+    return status;
+}
+
+static void clear_error() { g_last_error[0] = 0; }
+
+namespace {
+constexpr int kMaxDevices = 64;
+DeviceInfo g_dev[kMaxDevices];
+std::once_flag g_once[kMaxDevices];
+int g_dev_status[kMaxDevices];
+}  // namespace
+
+bool current_device(DeviceInfo *info, int *status)
+{
+    int d = -1;
+    cudaError_t e = cudaGetDevice(&d);
+    if (e != cudaSuccess || d < 0 || d >= kMaxDevices) {
+        *status = fail(BM_ERR_CUDA, "cudaGetDevice failed: %s", cudaGetErrorString(e));
+        return false;
+    }
+    std::call_once(g_once[d], [d] {
+        DeviceInfo &di = g_dev[d];
+        int st = BM_OK;
+        if (cudaDeviceGetAttribute(&di.major, cudaDevAttrComputeCapabilityMajor, d) != cudaSuccess ||
+            cudaDeviceGetAttribute(&di.minor, cudaDevAttrComputeCapabilityMinor, d) != cudaSuccess ||
+            cudaDeviceGetAttribute(&di.sm_count, cudaDevAttrMultiProcessorCount, d) != cudaSuccess ||
+            cudaDeviceGetAttribute(&di.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, d) !=
+                cudaSuccess)
+            st = BM_ERR_CUDA;
+        else if (di.major != 10 || di.minor != 3)
+            st = BM_ERR_UNSUPPORTED_DEVICE;
+        g_dev_status[d] = st;
+    });
+    if (g_dev_status[d] == BM_ERR_CUDA) {
+        *status = fail(BM_ERR_CUDA, "cannot query device %d", d);
+        return false;
+    }
+    if (g_dev_status[d] == BM_ERR_UNSUPPORTED_DEVICE) {
+        *status = fail(BM_ERR_UNSUPPORTED_DEVICE,
+                       "device %d is compute capability %d.%d; this library is built for sm_103a only", d,
+                       g_dev[d].major, g_dev[d].minor);
+        return false;
+    }
+    *info = g_dev[d];
+    return true;
+}
+
+}  // namespace bm
+
+using namespace bm;
+
+namespace {
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// [a, a+na) and [b, b+nb) in bytes overlap.
+bool overlap(const void *a, int64_t na, const void *b, int64_t nb)
+{
+    uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return na > 0 && nb > 0 && x < y + (uintptr_t)nb && y < x + (uintptr_t)na;
+}
+
+// rows * k * 2 bytes must fit an int64 and the products' index arithmetic.
+bool sizes_ok(int64_t rows, int64_t k) { return rows >= 0 && k >= 1 && rows <= (INT64_MAX / 4) / k; }
+
+int check_matrix_args(const char *fn, const uint16_t *W, int64_t rows, int64_t k, const uint16_t *X,
+                      int64_t ncols, const float *Y)
+{
+    if (k < 1 || k > BM_MAX_K) return fail(BM_ERR_INVALID_ARG, "%s: k = %lld outside 1..%d", fn, (long long)k, BM_MAX_K);
+    if (rows < 0 || ncols < 0) return fail(BM_ERR_INVALID_ARG, "%s: negative size", fn);
+    if (!sizes_ok(rows, k) || !sizes_ok(ncols, k) || (rows > 0 && ncols > INT64_MAX / 8 / rows))
+        return fail(BM_ERR_INVALID_ARG, "%s: sizes overflow", fn);
+    if (rows == 0 || ncols == 0) return BM_OK;
+    if (!W || !X || !Y) return fail(BM_ERR_INVALID_ARG, "%s: null pointer", fn);
+    if (!aligned(W, 16) || !aligned(X, 16))
+        return fail(BM_ERR_ALIGNMENT, "%s: W and the activation must be 16-byte aligned", fn);
+    if (!aligned(Y, 4)) return fail(BM_ERR_ALIGNMENT, "%s: the output must be 4-byte aligned", fn);
+    if (overlap(Y, rows * ncols * 4, W, rows * k * 2) || overlap(Y, rows * ncols * 4, X, ncols * k * 2))
+        return fail(BM_ERR_INVALID_ARG, "%s: the output overlaps an input", fn);
+    return BM_OK;
+}
+
+int product(const char *fn, const uint16_t *W, int64_t rows, int64_t k, const uint16_t *X, int64_t ncols,
+            float *Y, bm_stream_t stream)
+{
+    int st = check_matrix_args(fn, W, rows, k, X, ncols, Y);
+    if (st != BM_OK || rows == 0 || ncols == 0) return st;
+    DeviceInfo dev;
+    if (!current_device(&dev, &st)) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (bm_takes_sgemm(rows, k, ncols)) return launch_gemm_tc(W, rows, k, X, ncols, Y, s, dev);
+    VecdotJob job{};
+    job.W[0] = W;
+    job.y[0] = Y;
+    job.rows[0] = rows;
+    job.nmat = 1;
+    job.k = k;
+    job.X = X;
+    job.ncols = ncols;
+    return ncols == 1 ? launch_vecdot_1col(job, s, dev) : launch_vecdot_ncol(job, s, dev);
+}
+
+}  // namespace
+
+extern "C" {
+
+int bm_takes_sgemm(int64_t rows, int64_t k, int64_t ncols)
+{
+    return ncols >= 2 && rows % 4 == 0 && k % 8 == 0;
+}
+
+int bm_to_f16(const float *x, uint16_t *h, int64_t n, bm_stream_t stream)
+{
+    clear_error();
+    if (n < 0 || n > INT64_MAX / 8) return fail(BM_ERR_INVALID_ARG, "bm_to_f16: bad n = %lld", (long long)n);
+    if (n == 0) return BM_OK;
+    if (!x || !h) return fail(BM_ERR_INVALID_ARG, "bm_to_f16: null pointer");
+    if (!aligned(x, 16) || !aligned(h, 16))
+        return fail(BM_ERR_ALIGNMENT, "bm_to_f16: x and h must be 16-byte aligned");
+    if (overlap(x, n * 4, h, n * 2)) return fail(BM_ERR_INVALID_ARG, "bm_to_f16: h overlaps x");
+    int st;
+    DeviceInfo dev;
+    if (!current_device(&dev, &st)) return st;
+    return launch_to_f16(x, h, n, reinterpret_cast<cudaStream_t>(stream), dev);
+}
+
+int bm_f16_matvec(const uint16_t *W, int64_t rows, int64_t k, const uint16_t *x, float *y, bm_stream_t stream)
+{
+    clear_error();
+    int st = check_matrix_args("bm_f16_matvec", W, rows, k, x, 1, y);
+    if (st != BM_OK || rows == 0) return st;
+    DeviceInfo dev;
+    if (!current_device(&dev, &st)) return st;
+    VecdotJob job{};
+    job.W[0] = W;
+    job.y[0] = y;
+    job.rows[0] = rows;
+    job.nmat = 1;
+    job.k = k;
+    job.X = x;
+    job.ncols = 1;
+    return launch_vecdot_1col(job, reinterpret_cast<cudaStream_t>(stream), dev);
+}
+
+int bm_f16_matvec_multi(int nmat, const uint16_t *const *W, const int64_t *rows, int64_t k, const uint16_t *x,
+                        float *const *y, bm_stream_t stream)
+{
+    clear_error();
+    if (nmat < 1 || nmat > 4) return fail(BM_ERR_INVALID_ARG, "bm_f16_matvec_multi: nmat = %d outside 1..4", nmat);
+    if (!W || !rows || !y) return fail(BM_ERR_INVALID_ARG, "bm_f16_matvec_multi: null host array");
+    VecdotJob job{};
+    job.nmat = 0;
+    job.k = k;
+    job.X = x;
+    job.ncols = 1;
+    for (int m = 0; m < nmat; m++) {
+        int st = check_matrix_args("bm_f16_matvec_multi", W[m], rows[m], k, x, 1, y[m]);
+        if (st != BM_OK) return st;
+        for (int q = 0; q < m; q++)
+            if (overlap(y[m], rows[m] * 4, y[q], rows[q] * 4) || overlap(y[m], rows[m] * 4, W[q], rows[q] * k * 2) ||
+                overlap(y[q], rows[q] * 4, W[m], rows[m] * k * 2))
+                return fail(BM_ERR_INVALID_ARG, "bm_f16_matvec_multi: output %d overlaps an input or output", m);
+        if (rows[m] == 0) continue;  // empty matrices take no row groups
+        job.W[job.nmat] = W[m];
+        job.y[job.nmat] = y[m];
+        job.rows[job.nmat] = rows[m];
+        job.nmat++;
+    }
+    if (job.nmat == 0) return BM_OK;
+    int st;
+    DeviceInfo dev;
+    if (!current_device(&dev, &st)) return st;
+    return launch_vecdot_1col(job, reinterpret_cast<cudaStream_t>(stream), dev);
+}
+
+int bm_f16_matmul(const uint16_t *W, int64_t rows, int64_t k, const uint16_t *X, int64_t ncols, float *Y,
+                  bm_stream_t stream)
+{
+    clear_error();
+    return product("bm_f16_matmul", W, rows, k, X, ncols, Y, stream);
+}
+
+int bm_f16_logits(const uint16_t *E, int64_t vocab, int64_t hidden, const uint16_t *X, int64_t ncols, float *Y,
+                  bm_stream_t stream)
+{
+    clear_error();
+    return product("bm_f16_logits", E, vocab, hidden, X, ncols, Y, stream);
+}
+
+int bm_device_status(bm_stream_t stream)
+{
+    clear_error();
+    return read_device_error(reinterpret_cast<cudaStream_t>(stream));
+}
+
+int bm_selftest_wait_timeout(const uint16_t *W, const uint16_t *X, float *Y, bm_stream_t stream)
+{
+    clear_error();
+    int st = check_matrix_args("bm_selftest_wait_timeout", W, 128, 64, X, 16, Y);
+    if (st != BM_OK) return st;
+    DeviceInfo dev;
+    if (!current_device(&dev, &st)) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // Clear any earlier give-up first, so the status read below is this run's.
+    st = read_device_error(s);
+    if (st != BM_OK && st != BM_ERR_TIMEOUT) return st;
+    st = launch_gemm_tc_withheld(W, 128, 64, X, 16, Y, s, dev, 20ull * 1000 * 1000);
+    if (st != BM_OK) return st;
+    st = read_device_error(s);
+    if (st == BM_OK) return fail(BM_ERR_CUDA, "bm_selftest_wait_timeout: the withheld wait did not give up");
+    return st;
+}
+
+const char *bm_status_string(int status)
+{
+    switch (status) {
+    case BM_OK: return "ok";
+    case BM_ERR_INVALID_ARG: return "invalid argument";
+    case BM_ERR_ALIGNMENT: return "misaligned pointer";
+    case BM_ERR_UNSUPPORTED_DEVICE: return "unsupported device (needs sm_103)";
+    case BM_ERR_CUDA: return "CUDA error";
+    case BM_ERR_TIMEOUT: return "device-side bounded wait gave up";
+    default: return "unknown status";
+    }
+}
+
+const char *bm_last_error(void) { return g_last_error; }
+
+}  // extern "C"

@@ -1,0 +1,52 @@
+// bm_internal.h -- shared declarations of the CUDA library behind include/bm.h.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace bm {
+
+// Per-device facts read once.
+struct DeviceInfo {
+    int major = 0, minor = 0;
+    int sm_count = 0;
+    int max_smem_optin = 0;  // bytes of dynamic shared memory a block may opt into
+};
+
+// Fills *info for the current device; returns false (and sets the last error)
+// when the device cannot be queried or is not compute capability 10.3.
+bool current_device(DeviceInfo *info, int *status);
+
+// Records a reason for the calling host thread and returns `status`.
+int fail(int status, const char *fmt, ...);
+
+// Up to four matrices that share one activation (the fused Q/K/V or gate/up
+// products), or one matrix with several activation columns.
+struct VecdotJob {
+    const uint16_t *W[4];
+    float *y[4];
+    int64_t rows[4];
+    int64_t gbeg[5];  // first row group of matrix m; gbeg[nmat] = total groups
+    int nmat;
+    int64_t k;
+    const uint16_t *X;  // activation column(s), [ncols][k]
+    int64_t ncols;
+};
+
+// Launchers (each returns a bm_status; nothing is launched for empty jobs).
+int launch_to_f16(const float *x, uint16_t *h, int64_t n, cudaStream_t s, const DeviceInfo &dev);
+// One column, any k; uses the 16-byte fast kernel when k % 8 == 0.
+int launch_vecdot_1col(const VecdotJob &job, cudaStream_t s, const DeviceInfo &dev);
+// ncols >= 1 columns of one matrix, any k, Y[c*rows + r], bit-exact vec_dot.
+int launch_vecdot_ncol(const VecdotJob &job, cudaStream_t s, const DeviceInfo &dev);
+// Tensor-core product for bm_takes_sgemm shapes (rows % 4 == 0, k % 8 == 0, ncols >= 2).
+int launch_gemm_tc(const uint16_t *W, int64_t rows, int64_t k, const uint16_t *X, int64_t ncols,
+                   float *Y, cudaStream_t s, const DeviceInfo &dev);
+// Self-test of the bounded waits: a 128 x 64 x 16 product whose producer never
+// fills its only stage, so the MMA issuer gives up after `timeout_ns`.
+int launch_gemm_tc_withheld(const uint16_t *W, int64_t rows, int64_t k, const uint16_t *X, int64_t ncols,
+                            float *Y, cudaStream_t s, const DeviceInfo &dev, unsigned long long timeout_ns);
+// Waits for `s` and reads/clears the device error word of the tensor-core kernels.
+int read_device_error(cudaStream_t s);
+
+}  // namespace bm

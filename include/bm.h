@@ -1,0 +1,146 @@
+/*
+ * bm.h -- C ABI of the F16-weight product library for NVIDIA GB300 (sm_103a).
+ *
+ * The operations are those of the page "docs/modules/f16.md" (bankML, the
+ * F16 weights multiplied as ggml b11192 multiplies them):
+ *   - the activation is first rounded to f16, round to nearest even
+ *     (section "Design notes", bullet "Activation");
+ *   - a one-column product is ggml_vec_dot_f16 per row, bit for bit
+ *     (section "Design notes", bullet "vec_dot");
+ *   - a product of two or more columns takes tinyBLAS's 8-lane chain when the
+ *     weight has a multiple of 4 rows and the row a multiple of 8 elements, and
+ *     falls back to vec_dot otherwise (sections "Summary", "Technical usage",
+ *     "Design notes", bullet "sgemm_dot").  Here that tinyBLAS path runs on
+ *     tcgen05 tensor cores and is accurate to 4e-6 * sum|w_i * a_i| of
+ *     tinyBLAS's result; the fallback is bit-exact.
+ *
+ * Conventions shared by every call:
+ *   - f16 values are passed as their IEEE binary16 bit patterns (uint16_t),
+ *     little-endian.  A weight matrix W is row-major [rows][k] (a row is
+ *     contiguous); a column X[c] of a multi-column activation is contiguous, so
+ *     X is [ncols][k] row-major.  The product output is Y[c * rows + r], f32
+ *     (page f16.md, section "Matrix products", "mat_mul_par").
+ *   - Every pointer argument named as device memory must point to memory the
+ *     GPU can read (or write) -- e.g. from cudaMalloc or torch.  The caller
+ *     owns all of it; the library allocates nothing the caller frees and keeps
+ *     no state across calls besides per-device caches of device properties.
+ *   - Input pointers must be 16-byte aligned; output pointers 16-byte aligned
+ *     for bm_to_f16, 4-byte aligned elsewhere.  Outputs are overwritten, never
+ *     accumulated into, and must not overlap any input.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
+ *     default stream) and never synchronise.  A non-zero return means nothing
+ *     was launched, except BM_ERR_CUDA, which reports a launch error.  Device
+ *     side give-ups of bounded waits are reported by bm_device_status().
+ *   - Empty products (n, rows or ncols equal to 0) are valid and launch nothing.
+ *   - All calls are thread-safe; bm_last_error() is per host thread.
+ */
+#ifndef BM_H
+#define BM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t, declared without the CUDA headers. */
+typedef struct CUstream_st *bm_stream_t;
+
+typedef enum {
+    BM_OK = 0,
+    BM_ERR_INVALID_ARG = 1,        /* null pointer, bad size, overlapping output */
+    BM_ERR_ALIGNMENT = 2,          /* a pointer breaks the alignment rule above */
+    BM_ERR_UNSUPPORTED_DEVICE = 3, /* current device is not compute capability 10.3 */
+    BM_ERR_CUDA = 4,               /* a CUDA runtime or driver call failed */
+    BM_ERR_TIMEOUT = 5             /* a kernel gave up a bounded wait (bm_device_status) */
+} bm_status;
+
+/* Largest row length k accepted by the products (the f16 activation of one
+ * column is staged whole in shared memory by the one-column kernels). */
+#define BM_MAX_K 65536
+
+/*
+ * h[i] = f16(x[i]) rounded to nearest, ties to even, for 0 <= i < n
+ * (f16.md, "Design notes", "Activation"; ggml_cpu_fp32_to_fp16).
+ *   x : device, f32[n], 16-byte aligned.     h : device, uint16[n], 16-byte aligned.
+ *   n >= 0.  |x| >= 65520 gives +-inf, f16 subnormals are produced, f32
+ *   subnormals give +-0.  NaN inputs give a NaN (payload unspecified).
+ */
+int bm_to_f16(const float *x, uint16_t *h, int64_t n, bm_stream_t stream);
+
+/*
+ * y[r] = vec_dot(W[r], x) for 0 <= r < rows, bit-exact with ggml_vec_dot_f16
+ * (f16.md, "Matrix products", mat_vec_par; "Design notes", "vec_dot"):
+ * 32 f32 chains (element i of a 32-element step feeds accumulator (i%32)/8,
+ * lane i%8, in increasing i from +0), reduced (a0+a2)+(a1+a3), low half plus
+ * high half, two horizontal adds, then the k%32 tail added in double in order.
+ *   W : device, f16[rows][k].   x : device, f16[k].   y : device, f32[rows].
+ *   rows >= 0, 1 <= k <= BM_MAX_K.
+ */
+int bm_f16_matvec(const uint16_t *W, int64_t rows, int64_t k, const uint16_t *x, float *y,
+                  bm_stream_t stream);
+
+/*
+ * bm_f16_matvec for up to four matrices that share one activation x, in one
+ * launch (f16.md, "Matrix products", mat_vec_multi_par: Q, K and V; gate and up).
+ * Every output row is still one vec_dot, so y[m] equals bm_f16_matvec(W[m], ...)
+ * bit for bit.
+ *   nmat in 1..4.  W, rows and y are HOST arrays of nmat entries; W[m] and y[m]
+ *   are device pointers (f16[rows[m]][k] and f32[rows[m]]); rows[m] >= 0.
+ */
+int bm_f16_matvec_multi(int nmat, const uint16_t *const *W, const int64_t *rows, int64_t k,
+                        const uint16_t *x, float *const *y, bm_stream_t stream);
+
+/*
+ * Y[c*rows + r] = W[r] . X[c] for every row r and column c
+ * (f16.md, "Matrix products", mat_mul_par), with the path ggml takes:
+ *   - bm_takes_sgemm(rows, k, ncols): tcgen05 tensor cores, f32 accumulation,
+ *     |Y - sgemm_dot(W[r], X[c])| <= 4e-6 * sum_i |W[r][i] * X[c][i]|;
+ *   - otherwise: vec_dot per element, bit-exact (ncols == 1 is bm_f16_matvec).
+ *   W : device, f16[rows][k].   X : device, f16[ncols][k].   Y : device, f32[ncols*rows].
+ *   rows, ncols >= 0, 1 <= k <= BM_MAX_K.
+ */
+int bm_f16_matmul(const uint16_t *W, int64_t rows, int64_t k, const uint16_t *X, int64_t ncols,
+                  float *Y, bm_stream_t stream);
+
+/*
+ * Logits over a tied token embedding (page "docs/modules/forward.md", Summary:
+ * with no output.weight the logits read token_embd.weight): the product of
+ * E (f16[vocab][hidden]) with ncols normalised activations X (f16[ncols][hidden]),
+ * Y[c*vocab + v].  It is one product over all columns, so its path follows
+ * bm_takes_sgemm(vocab, hidden, ncols) exactly as bm_f16_matmul's does.
+ */
+int bm_f16_logits(const uint16_t *E, int64_t vocab, int64_t hidden, const uint16_t *X,
+                  int64_t ncols, float *Y, bm_stream_t stream);
+
+/* ggml's path selector (f16.md, "Technical usage"): 1 when
+ * ncols >= 2 && rows % 4 == 0 && k % 8 == 0, else 0.  Pure; never fails. */
+int bm_takes_sgemm(int64_t rows, int64_t k, int64_t ncols);
+
+/* Waits for `stream`, then reads and clears this library's device error word
+ * on the current device: BM_OK, BM_ERR_TIMEOUT (a kernel gave up a bounded
+ * wait and wrote nothing trustworthy), or BM_ERR_CUDA (the wait failed). */
+int bm_device_status(bm_stream_t stream);
+
+/* Self-test of the bounded device waits (no counterpart on the pages; it
+ * checks this library's failure reporting).  Runs one 128 x 64 x 16
+ * tensor-core product whose data producer deliberately never fills its only
+ * pipeline stage, so the consumer's bounded wait gives up after about 20 ms;
+ * the kernel then records the give-up, frees its tensor memory and exits with
+ * the context intact.  Synchronises `stream`.  Returns BM_ERR_TIMEOUT when the
+ * give-up was detected and reported (the expected result), any other status
+ * otherwise.  W: device f16[128][64], X: device f16[16][64], Y: device
+ * f32[16*128] (contents of Y are unspecified afterwards). */
+int bm_selftest_wait_timeout(const uint16_t *W, const uint16_t *X, float *Y, bm_stream_t stream);
+
+/* Static text for a status code. */
+const char *bm_status_string(int status);
+
+/* The reason for the last non-zero status returned on this host thread
+ * ("" if none).  Valid until the next call on this thread. */
+const char *bm_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* BM_H */

@@ -1,0 +1,119 @@
+"""The C-ABI boundary without a GPU: the library builds and loads, exports every
+symbol include/bm.h declares, and rejects bad arguments on the host before any
+CUDA call (every case here returns before the library touches the device)."""
+import ctypes as C
+import json
+import os
+import re
+
+import pytest
+
+from conftest import GOLDEN, ROOT
+
+HEADER = os.path.join(ROOT, "include", "bm.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    from f16_weight_gemv_gb300 import _build
+    import f16_weight_gemv_gb300 as bm
+    _build.build()
+    return bm.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(bm_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ["bm_to_f16", "bm_f16_matvec", "bm_f16_matvec_multi", "bm_f16_matmul", "bm_f16_logits",
+              "bm_takes_sgemm", "bm_status_string", "bm_last_error", "bm_device_status"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    import f16_weight_gemv_gb300 as bm
+    for name in declared_functions():
+        assert hasattr(L, name), name
+        assert name in bm.EXPORTS, name
+        assert hasattr(bm, name), name  # same name in the Python binding
+
+
+def test_takes_sgemm_through_the_abi(L):
+    table = json.load(open(os.path.join(GOLDEN, "takes_sgemm_table.json")))["table"]
+    for rows, k, n, want in table:
+        assert L.bm_takes_sgemm(rows, k, n) == want, (rows, k, n)
+
+
+def test_status_strings(L):
+    for s in range(6):
+        assert L.bm_status_string(s)
+    assert L.bm_status_string(99) == b"unknown status"
+
+
+A = 0x100000  # a 16-byte aligned fake device address; never dereferenced here
+
+
+def st(L, name, *args):
+    return getattr(L, name)(*args)
+
+
+def test_to_f16_host_checks(L):
+    assert st(L, "bm_to_f16", A, A + 4096, -1, None) == 1
+    assert st(L, "bm_to_f16", A, A + 4096, 0, None) == 0
+    assert st(L, "bm_to_f16", None, A, 8, None) == 1
+    assert L.bm_last_error()
+    assert st(L, "bm_to_f16", A + 4, A + 4096, 8, None) == 2
+    assert st(L, "bm_to_f16", A, A + 4098, 8, None) == 2
+    assert st(L, "bm_to_f16", A, A + 16, 8, None) == 1  # h overlaps x
+
+
+def test_matvec_host_checks(L):
+    f = "bm_f16_matvec"
+    assert st(L, f, A, 16, 0, A + 2 ** 20, A + 2 ** 21, None) == 1            # k = 0
+    assert st(L, f, A, 16, 65537, A + 2 ** 24, A + 2 ** 25, None) == 1      # k > BM_MAX_K
+    assert st(L, f, A, -1, 64, A + 2 ** 20, A + 2 ** 21, None) == 1
+    assert st(L, f, A, 0, 64, A + 2 ** 20, A + 2 ** 21, None) == 0           # empty: nothing launched
+    assert L.bm_last_error() == b""
+    assert st(L, f, None, 16, 64, A + 2 ** 20, A + 2 ** 21, None) == 1
+    assert st(L, f, A + 2, 16, 64, A + 2 ** 20, A + 2 ** 21, None) == 2
+    assert st(L, f, A, 16, 64, A + 2 ** 20 + 8, A + 2 ** 21, None) == 2
+    assert st(L, f, A, 16, 64, A + 2 ** 20, A + 2 ** 21 + 2, None) == 2
+    assert st(L, f, A, 16, 64, A + 2 ** 20, A + 64, None) == 1               # y inside W
+    assert st(L, f, A, 2 ** 62, 64, A + 2 ** 20, A + 2 ** 21, None) == 1     # size overflow
+
+
+def test_matvec_multi_host_checks(L):
+    f = L.bm_f16_matvec_multi
+    W = (C.c_void_p * 5)(A, A + 2 ** 20, A + 2 ** 21, A + 2 ** 22, A + 2 ** 23)
+    y = (C.c_void_p * 5)(A + 2 ** 24, A + 2 ** 24 + 4096, A + 2 ** 24 + 8192, A + 2 ** 24 + 12288, A + 2 ** 25)
+    rows = (C.c_int64 * 5)(16, 16, 16, 16, 16)
+    assert f(0, W, rows, 64, A + 2 ** 26, y, None) == 1
+    assert f(5, W, rows, 64, A + 2 ** 26, y, None) == 1
+    assert f(2, None, rows, 64, A + 2 ** 26, y, None) == 1
+    yo = (C.c_void_p * 2)(A + 2 ** 24, A + 2 ** 24 + 32)                    # outputs overlap
+    assert f(2, W, rows, 64, A + 2 ** 26, yo, None) == 1
+    z = (C.c_int64 * 2)(0, 0)
+    assert f(2, W, z, 64, A + 2 ** 26, y, None) == 0                         # all empty
+
+
+def test_matmul_host_checks(L):
+    for f in ("bm_f16_matmul", "bm_f16_logits"):
+        assert st(L, f, A, 16, 64, A + 2 ** 20, 0, A + 2 ** 21, None) == 0
+        assert st(L, f, A, 16, 64, A + 2 ** 20, -3, A + 2 ** 21, None) == 1
+        assert st(L, f, A, 16, 64, A + 2 ** 20 + 4, 2, A + 2 ** 21, None) == 2
+        assert st(L, f, A, 16, 64, A + 2 ** 20, 2, A + 2 ** 20 + 64, None) == 1  # Y overlaps X
+        assert st(L, f, A, 2 ** 40, 64, A + 2 ** 20, 2 ** 30, A + 2 ** 21, None) == 1
+
+
+def test_product_path_is_cuda_only():
+    """The binding has no CPU fallback: it loads libbm.so or fails, and never imports the oracle."""
+    import f16_weight_gemv_gb300 as bm
+    src = open(bm.__file__).read() + open(os.path.join(os.path.dirname(bm.__file__), "_build.py")).read()
+    assert "import oracle" not in src and "from oracle" not in src
+    csrc = os.path.join(os.path.dirname(bm.__file__), "csrc")
+    for fn in os.listdir(csrc):
+        assert "oracle.h" not in open(os.path.join(csrc, fn)).read()
