@@ -415,8 +415,33 @@ def run_reference(args):
 # ----------------------------------------------------------------------------- main
 
 
+def run_single(spec: str, reps: int):
+    """One product ROWSxKxNCOLS, `reps` times (for profilers; prints nothing timed)."""
+    import torch
+
+    import __graft_entry__
+    import f16_weight_gemv_gb300 as bm
+
+    __graft_entry__.build()
+    rows, k, ncols = (int(v) for v in spec.lower().split("x"))
+    dev = torch.device("cuda", 0)
+    W = torch.from_numpy(synth.normal_f16(SEED, "single.w", W_SIGMA, (rows, k)).view(np.float16)).to(dev)
+    X = torch.from_numpy(synth.normal_f16(SEED, "single.x", A_SIGMA, (ncols, k)).view(np.float16)).to(dev)
+    Y = torch.empty((ncols, rows), dtype=torch.float32, device=dev)
+    for _ in range(reps):
+        if ncols == 1:
+            bm.bm_f16_matvec(W, X[0], Y[0])
+        else:
+            bm.bm_f16_matmul(W, X, Y)
+    torch.cuda.synchronize()
+    print(json.dumps({"single": spec, "reps": reps, "status": bm.bm_device_status()}))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
+    ap.add_argument("--single", default=None, help="profile mode: run one product ROWSxKxNCOLS --reps times")
+    ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=20)
@@ -428,6 +453,8 @@ def main():
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
         return run_reference(args)
+    if args.single:
+        return run_single(args.single, args.reps)
 
     import torch
 
