@@ -2,16 +2,19 @@
 """Benchmark of the F16-weight products on one GB300 (or N replicas).
 
 Default workload: a SmolLM2-135M-shaped decode step -- 30 layers of
-[round -> fused Q/K/V GEMV (576+192+192 rows x 576), round -> O (576 x 576),
- round -> fused gate/up GEMV (2 x 1536 x 576), round -> down (576 x 1536)]
-then round -> tied logits (49152 x 576): 1 column, 242 C-ABI calls, 269 MB of
-f16 weights (more than the 129 MB L2), seeded synthetic weights N(0, 0.02)
-and activations N(0, 1).  The step is captured once as a CUDA graph of those
-calls and replayed; `value` is algorithmic bytes per step / time per step.
+[fused Q/K/V product (576+192+192 rows x 576), O (576 x 576), fused gate/up
+(2 x 1536 x 576), down (576 x 1536)] then the tied logits (49152 x 576): one
+column, 121 products over 269 MB of f16 weights (more than the 129 MB L2),
+seeded synthetic weights N(0, 0.02) and f32 activations N(0, 1).  Each product
+is one bm_f16_matvec_act call: the f32 activation is rounded to f16 and
+multiplied in the same launch.  The step is captured once as a CUDA graph
+(programmatic dependent launch on) and replayed; `value` is algorithmic bytes
+per step / time per step.
 
-Extra lines in the same JSON object:
-  roofline     -- the one-column GEMV kernel alone (graph of the step's GEMV
-                  launches, no rounding kernels), achieved GB/s vs measured HBM peak
+Extra objects in the same JSON line:
+  roofline     -- the step's kernel (k_gemv_stream) against the measured HBM peak
+  unfused      -- the same step as bm_to_f16 + bm_f16_matvec[_multi]/bm_f16_logits
+                  (242 launches)
   products     -- single products of the Llama-3-8B / Qwen3-0.6B shapes:
                   decode GB/s and 512-column tensor-core TFLOP/s
   e2e          -- the same step through the Python binding, eagerly, with the
@@ -72,17 +75,19 @@ def step_plan():
     return plan
 
 
-def step_bytes(plan):
-    tot = gemv = 0
+def step_bytes(plan, fused=True):
+    """Algorithmic bytes of one step.  Fused: each product call reads its f32
+    activation (4k) and rounds it in the kernel; unfused: a rounding call (6 bytes
+    per element) then the product reads the f16 activation (2k).  Weights 2*rows*k
+    and outputs 4*rows either way; a fused multi-matrix call reads its activation once."""
+    tot = 0
     for op in plan:
         if op[0] == "round":
-            tot += 6 * op[1]
+            tot += 0 if fused else 6 * op[1]
         else:
-            b = sum(algorithmic_bytes(r, op[2]) for _, r in op[1])
-            b -= 2 * op[2] * (len(op[1]) - 1)  # one shared activation read per fused call
-            tot += b
-            gemv += b
-    return tot, gemv
+            k = op[2]
+            tot += sum(2 * r * k + 4 * r for _, r in op[1]) + (4 * k if fused else 2 * k)
+    return tot
 
 
 def act_sizes(plan):
@@ -168,7 +173,7 @@ def run_gpu(args, rank, world, local_rank):
     torch.cuda.set_device(dev)
     bm.lib()
     plan = step_plan()
-    tot_bytes, gemv_bytes = step_bytes(plan)
+    tot_bytes, unfused_bytes = step_bytes(plan, True), step_bytes(plan, False)
 
     # ---- weights and activations (seeded, generated on the host once, then resident)
     weights = {}
@@ -195,15 +200,22 @@ def run_gpu(args, rank, world, local_rank):
                 outs[name] = torch.empty(rows, dtype=torch.float32, device=dev)
 
     stream = torch.cuda.Stream(device=dev)
+    # The weights are constants: programmatic dependent launch lets each product start
+    # copying its weights while the kernel ahead of it is still running.
+    bm.bm_set_pdl(not args.no_pdl)
 
-    def run_step(s, gemv_only=False):
+    def run_step(s, fused=True):
         for op in plan:
             if op[0] == "round":
-                if not gemv_only:
+                if not fused:
                     a = op[2]
                     bm.bm_to_f16(act_f32[offs[a]:offs[a] + op[1]], act_f16[offs[a]:offs[a] + op[1]], stream=s)
                 continue
             kind, mats, k, a = op
+            if fused:
+                bm.bm_f16_matvec_act([weights[n] for n, _ in mats], act_f32[offs[a]:offs[a] + k],
+                                     [outs[n] for n, _ in mats], stream=s)
+                continue
             x = act_f16[offs[a]:offs[a] + k]
             if kind == "multi":
                 bm.bm_f16_matvec_multi([weights[n] for n, _ in mats], x, [outs[n] for n, _ in mats], stream=s)
@@ -212,21 +224,20 @@ def run_gpu(args, rank, world, local_rank):
             else:
                 bm.bm_f16_logits(weights[mats[0][0]], x.view(1, -1), outs[mats[0][0]].view(1, -1), stream=s)
 
-    launches_per_step = len(plan)
-    gemv_launches = sum(1 for op in plan if op[0] != "round")
+    launches_per_step = sum(1 for op in plan if op[0] != "round")
 
-    def capture(gemv_only):
+    def capture(fused):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.stream(stream):
-            run_step(stream, gemv_only)  # warm (attribute setup happens outside capture)
+            run_step(stream, fused)  # warm (attribute setup happens outside capture)
         torch.cuda.synchronize()
         with torch.cuda.graph(g, stream=stream):
-            run_step(stream, gemv_only)
+            run_step(stream, fused)
         torch.cuda.synchronize()
         return g
 
-    g_step = capture(False)
-    g_gemv = capture(True)
+    g_step = capture(True)
+    g_unfused = capture(False)
 
     def timed(g, steps, warmup):
         for _ in range(warmup):
@@ -253,7 +264,7 @@ def run_gpu(args, rank, world, local_rank):
     t_begin = time.time()
     ms = timed(g_step, args.steps, args.warmup)
     t_end = time.time()
-    ms_gemv = timed(g_gemv, max(args.steps, 20), args.warmup)
+    ms_unfused = timed(g_unfused, max(args.steps, 20), args.warmup)
     clk = clocks.summary(t_begin, t_end)
     clocks.stop()
 
@@ -287,36 +298,53 @@ def run_gpu(args, rank, world, local_rank):
     ms_e2e = e0.elapsed_time(e1) / e2e_steps
 
     result = {
-        "ms": ms, "ms_gemv": ms_gemv, "ms_e2e": ms_e2e, "tot_bytes": tot_bytes, "gemv_bytes": gemv_bytes,
-        "launches_per_step": launches_per_step, "gemv_launches": gemv_launches, "clocks": clk,
+        "ms": ms, "ms_unfused": ms_unfused, "ms_e2e": ms_e2e, "tot_bytes": tot_bytes,
+        "unfused_bytes": unfused_bytes, "launches_per_step": launches_per_step, "clocks": clk,
         "h2d": int(act_host.nbytes), "d2h": int(VOCAB * 4),
     }
     if rank == 0 and not args.no_products:
         result["products"] = bench_products(bm, dev, stream, torch)
+        result["llama3_8b_decode_step"] = bench_llama_decode(bm, dev, stream, torch)
     return result
 
 
-def bench_products(bm, dev, stream, torch):
-    """Single products at full size: decode GEMV and 512-column tensor-core GEMM."""
-    out = []
-    l2_flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
-
-    def time_call(fn, reps=10):
+def graph_time(torch, stream, fn, reps=3, pre=None):
+    """Capture fn() once as a CUDA graph; median ms of `reps` replays (pre() runs
+    before each replay, outside the timed events)."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        fn()
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(reps):
         with torch.cuda.stream(stream):
-            for _ in range(2):
-                fn()
-            torch.cuda.synchronize()
-            tot = 0.0
-            for _ in range(reps):
-                l2_flush.fill_(1.0)  # evict the previous repetition's operands from L2
-                e0 = torch.cuda.Event(enable_timing=True)
-                e1 = torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
-                fn()
-                e1.record(stream)
-                torch.cuda.synchronize()
-                tot += e0.elapsed_time(e1)
-        return tot / reps
+            if pre is not None:
+                pre()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    return float(np.median(ts))
+
+
+def bench_products(bm, dev, stream, torch):
+    """Full-size single products.  One column: a graph of back-to-back products that
+    cycle through weight replicas larger than twice the L2 (every launch streams its
+    weights from HBM, as in a decode step), programmatic dependent launch on.
+    512 columns: one launch after an L2 flush by a read of a 512 MB buffer."""
+    out = []
+    l2_flush = torch.ones(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    l2_sink = torch.zeros((), dtype=torch.float32, device=dev)
+
+    def flush():
+        # a read leaves clean lines, so no write-back lands inside the timed product
+        l2_sink.copy_(l2_flush.sum())
 
     shapes = [("llama3_8b.q", 4096, 4096), ("llama3_8b.gate", 14336, 4096), ("llama3_8b.down", 4096, 14336),
               ("llama3_8b.output", 128256, 4096), ("qwen3_0.6b.logits", 151936, 1024)]
@@ -324,17 +352,63 @@ def bench_products(bm, dev, stream, torch):
         W = torch.from_numpy(synth.normal_f16(SEED, name, 0.01 if "llama" in name else 0.02, (rows, k))
                              .view(np.float16)).to(dev)
         x = torch.from_numpy(synth.normal_f16(SEED, name + ".x", 1.0, (512, k)).view(np.float16)).to(dev)
+        nrep = max(2, min(16, -(-2 * 129 * 2 ** 20 // (2 * rows * k))))
+        reps = [W] + [W.clone() for _ in range(nrep - 1)]
         y = torch.empty(rows, dtype=torch.float32, device=dev)
-        ms = time_call(lambda: bm.bm_f16_matvec(W, x[0], y, stream=stream))
+        launches = 2 * nrep
+
+        def chain():
+            for i in range(launches):
+                bm.bm_f16_matvec(reps[i % nrep], x[0], y, stream=stream)
+
+        ms = graph_time(torch, stream, chain) / launches
         gbs = algorithmic_bytes(rows, k) / ms / 1e6
-        out.append({"product": name, "rows": rows, "k": k, "ncols": 1, "ms": round(ms, 5), "GB_s": round(gbs, 1)})
+        out.append({"product": name, "rows": rows, "k": k, "ncols": 1, "ms": round(ms, 5), "GB_s": round(gbs, 1),
+                    "how": "%d back-to-back launches over %d weight replicas, PDL" % (launches, nrep)})
         Y = torch.empty((512, rows), dtype=torch.float32, device=dev)
-        ms = time_call(lambda: bm.bm_f16_matmul(W, x, Y, stream=stream))
+        ms = graph_time(torch, stream, lambda: bm.bm_f16_matmul(W, x, Y, stream=stream), reps=5, pre=flush)
         tf = 2.0 * rows * k * 512 / ms / 1e9
         out.append({"product": name, "rows": rows, "k": k, "ncols": 512, "ms": round(ms, 5),
                     "TFLOP_s": round(tf, 1), "GB_s": round(algorithmic_bytes(rows, k, 512) / ms / 1e6, 1)})
-        del W, x, y, Y
+        del W, x, y, Y, reps
     return out
+
+
+def bench_llama_decode(bm, dev, stream, torch, steps=10):
+    """A Llama-3-8B-shaped decode step: 32 layers of [fused Q/K/V (4096+1024+1024 x
+    4096), O (4096 x 4096), fused gate/up (2 x 14336 x 4096), down (4096 x 14336)]
+    then the output product (128256 x 4096): 129 bm_f16_matvec_act calls over 15 GB
+    of f16 weights N(0, 0.01).  One layer's weights are drawn and copied to all 32
+    layers (distinct memory: every product still streams from HBM)."""
+    hid, ffn, kv, vocab, layers = 4096, 14336, 1024, 128256, 32
+    base = {n: torch.from_numpy(synth.normal_f16(SEED, "llama3_8b." + n, 0.01, (r, c)).view(np.float16)).to(dev)
+            for n, r, c in [("q", hid, hid), ("k", kv, hid), ("v", kv, hid), ("o", hid, hid), ("gate", ffn, hid),
+                            ("up", ffn, hid), ("down", hid, ffn)]}
+    lw = [{n: (t if L == 0 else t.clone()) for n, t in base.items()} for L in range(layers)]
+    out_w = torch.from_numpy(synth.normal_f16(SEED, "llama3_8b.output", 0.01, (vocab, hid)).view(np.float16)).to(dev)
+    xa = torch.from_numpy(synth.normal_f32(SEED, "llama3_8b.act", 1.0, hid)).to(dev)
+    xf = torch.from_numpy(synth.normal_f32(SEED, "llama3_8b.act_ffn", 1.0, ffn)).to(dev)
+    ys = {n: torch.empty(t.shape[0], dtype=torch.float32, device=dev) for n, t in base.items()}
+    logits = torch.empty(vocab, dtype=torch.float32, device=dev)
+    nbytes = 0
+    for n, t in base.items():
+        nbytes += layers * (2 * t.numel() + 4 * t.shape[0])
+    nbytes += layers * 4 * (hid + hid + hid + ffn) + 2 * vocab * hid + 4 * vocab + 4 * hid
+
+    def step():
+        for L in range(layers):
+            w = lw[L]
+            bm.bm_f16_matvec_act([w["q"], w["k"], w["v"]], xa, [ys["q"], ys["k"], ys["v"]], stream=stream)
+            bm.bm_f16_matvec_act([w["o"]], xa, [ys["o"]], stream=stream)
+            bm.bm_f16_matvec_act([w["gate"], w["up"]], xa, [ys["gate"], ys["up"]], stream=stream)
+            bm.bm_f16_matvec_act([w["down"]], xf, [ys["down"]], stream=stream)
+        bm.bm_f16_matvec_act([out_w], xa, [logits], stream=stream)
+
+    ms = graph_time(torch, stream, step, reps=steps)
+    res = {"ms_per_step": round(ms, 4), "GB_s": round(nbytes / ms / 1e6, 1), "weight_GB": round(
+        (sum(t.numel() for t in base.values()) * layers + out_w.numel()) * 2 / 1e9, 3), "launches": 4 * layers + 1}
+    del lw, out_w, base
+    return res
 
 
 # ----------------------------------------------------------------------------- CPU oracle
@@ -345,7 +419,7 @@ def oracle_step_runner():
     import oracle
 
     plan = step_plan()
-    tot_bytes, _ = step_bytes(plan)
+    tot_bytes = step_bytes(plan, True)  # the same byte count the GPU arm's value uses
     weights = {}
     for op in plan:
         if op[0] != "round":
@@ -448,6 +522,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-products", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-pdl", action="store_true", help="launch without programmatic dependent launch")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -485,7 +560,7 @@ def main():
     hbm_peak = float(peaks.get("hbm_gbs", 6800.0))
     peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
     value = r["tot_bytes"] * world / (r["ms"] / 1e3) / 1e9
-    achieved = r["gemv_bytes"] / (r["ms_gemv"] / 1e3) / 1e9
+    achieved = r["tot_bytes"] / (r["ms"] / 1e3) / 1e9
     line = {
         "metric": "decode F16 GEMV HBM GB/s (SmolLM2-135M decode step)",
         "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -496,13 +571,19 @@ def main():
                    "weight_bytes": int(sum(2 * rows * op[2] for op in step_plan() if op[0] != "round"
                                            for _, rows in op[1])),
                    "l2": "inputs larger than L2 (269 MB of weights per step, cyclic)",
-                   "parallelism": "replicas" if world > 1 else "single GPU", "graph": "CUDA graph of the step"},
+                   "parallelism": "replicas" if world > 1 else "single GPU", "graph": "CUDA graph of the step",
+                   "pdl": not args.no_pdl},
         "pct_of_hbm_peak": round(100.0 * value / world / hbm_peak, 2),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(achieved / hbm_peak, 4), "traffic": None,
-                     "kernel": "k_vecdot_rows4 (one-column GEMV)", "peak_source": peak_src,
-                     "launches_per_step": r["gemv_launches"],
-                     "how": "graph of the step's GEMV launches alone, CUDA events on the launch stream"},
+                     "kernel": "k_gemv_stream (rounding + one-column GEMV)", "peak_source": peak_src,
+                     "launches_per_step": r["launches_per_step"],
+                     "how": "the step's only kernel: algorithmic bytes of its launches / CUDA-event time of the "
+                            "step graph on the launch stream"},
+        "unfused": {"ms_per_step": round(r["ms_unfused"], 5),
+                    "value": round(r["unfused_bytes"] / (r["ms_unfused"] / 1e3) / 1e9, 2),
+                    "launches_per_step": 2 * r["launches_per_step"],
+                    "how": "bm_to_f16 then bm_f16_matvec[_multi] / bm_f16_logits per product"},
         "gpu_launches": r["launches_per_step"] * args.steps,
         "clocks": r["clocks"],
         "e2e": {"value": round(r["tot_bytes"] / (r["ms_e2e"] / 1e3) / 1e9, 2), "unit": "GB/s",
@@ -510,6 +591,9 @@ def main():
                 "how": "eager calls through the Python binding; pinned host activations in, logits out"},
         "device": gpu_name,
     }
+    if "llama3_8b_decode_step" in r:
+        r["llama3_8b_decode_step"]["pct_hbm"] = round(100.0 * r["llama3_8b_decode_step"]["GB_s"] / hbm_peak, 1)
+        line["llama3_8b_decode_step"] = r["llama3_8b_decode_step"]
     if "products" in r:
         line["products"] = r["products"]
         for p in r["products"]:

@@ -17,9 +17,9 @@ import torch
 from . import _build
 
 __all__ = [
-    "BmError", "lib", "bm_to_f16", "bm_f16_matvec", "bm_f16_matvec_multi", "bm_f16_matmul",
+    "BmError", "lib", "bm_to_f16", "bm_f16_matvec", "bm_f16_matvec_multi", "bm_f16_matvec_act", "bm_f16_matmul",
     "bm_f16_logits", "bm_takes_sgemm", "bm_device_status", "bm_status_string", "bm_last_error",
-    "bm_selftest_wait_timeout", "EXPORTS", "BM_MAX_K",
+    "bm_selftest_wait_timeout", "bm_set_pdl", "EXPORTS", "BM_MAX_K",
 ]
 
 BM_OK, BM_ERR_INVALID_ARG, BM_ERR_ALIGNMENT, BM_ERR_UNSUPPORTED_DEVICE, BM_ERR_CUDA, BM_ERR_TIMEOUT = range(6)
@@ -31,10 +31,12 @@ EXPORTS = {
     "bm_to_f16": (_i, [_vp, _vp, _i64, _vp]),
     "bm_f16_matvec": (_i, [_vp, _i64, _i64, _vp, _vp, _vp]),
     "bm_f16_matvec_multi": (_i, [_i, C.POINTER(_vp), C.POINTER(_i64), _i64, _vp, C.POINTER(_vp), _vp]),
+    "bm_f16_matvec_act": (_i, [_i, C.POINTER(_vp), C.POINTER(_i64), _i64, _vp, _vp, C.POINTER(_vp), _vp]),
     "bm_f16_matmul": (_i, [_vp, _i64, _i64, _vp, _i64, _vp, _vp]),
     "bm_f16_logits": (_i, [_vp, _i64, _i64, _vp, _i64, _vp, _vp]),
     "bm_takes_sgemm": (_i, [_i64, _i64, _i64]),
     "bm_device_status": (_i, [_vp]),
+    "bm_set_pdl": (_i, [_i]),
     "bm_selftest_wait_timeout": (_i, [_vp, _vp, _vp, _vp]),
     "bm_status_string": (C.c_char_p, [_i]),
     "bm_last_error": (C.c_char_p, []),
@@ -146,6 +148,30 @@ def bm_f16_matvec_multi(Ws, x: torch.Tensor, ys=None, stream=None):
     return ys
 
 
+def bm_f16_matvec_act(Ws, x: torch.Tensor, ys=None, h: torch.Tensor | None = None, stream=None):
+    """Round the f32 activation x to f16 and multiply it by each matrix in Ws, in one
+    launch; h (optional) receives the rounded activation.  Returns ys."""
+    n = len(Ws)
+    k = x.numel()
+    if ys is None:
+        ys = [torch.empty(W.shape[0], dtype=torch.float32, device=x.device) for W in Ws]
+    if len(ys) != n:
+        raise ValueError("one output per matrix")
+    for W, y in zip(Ws, ys):
+        r, kk = _wk(W)
+        if kk != k or y.numel() != r:
+            raise ValueError("shape mismatch in bm_f16_matvec_act")
+    if h is not None and h.numel() != k:
+        raise ValueError("h must have k elements")
+    wp = (C.c_void_p * max(n, 1))(*[_dev(W, "W", _F16_LIKE) for W in Ws])
+    yp = (C.c_void_p * max(n, 1))(*[_dev(y, "y", (torch.float32,)) for y in ys])
+    rows = (C.c_int64 * max(n, 1))(*[W.shape[0] for W in Ws])
+    hp = _dev(h, "h", _F16_LIKE) if h is not None else None
+    _check(lib().bm_f16_matvec_act(n, wp, rows, k, _dev(x, "x", (torch.float32,)), hp, yp, _stream(stream)),
+           "bm_f16_matvec_act")
+    return ys
+
+
 def _product(fn_name: str, W, X, Y, stream):
     rows, k = _wk(W)
     if X.dim() == 1:
@@ -180,6 +206,11 @@ def bm_device_status(stream=None) -> int:
 def bm_selftest_wait_timeout(W, X, Y, stream=None) -> int:
     return int(lib().bm_selftest_wait_timeout(_dev(W, "W", _F16_LIKE), _dev(X, "X", _F16_LIKE),
                                               _dev(Y, "Y", (torch.float32,)), _stream(stream)))
+
+
+def bm_set_pdl(enable: bool) -> bool:
+    """Turn programmatic dependent launch of the products on or off; returns the old setting."""
+    return bool(lib().bm_set_pdl(1 if enable else 0))
 
 
 def bm_status_string(status: int) -> str:

@@ -7,6 +7,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 
 namespace bm {
@@ -29,7 +30,40 @@ constexpr int kMaxDevices = 64;
 DeviceInfo g_dev[kMaxDevices];
 std::once_flag g_once[kMaxDevices];
 int g_dev_status[kMaxDevices];
+std::atomic<int> g_pdl{0};
+unsigned int *g_err_addr[kMaxDevices];
+std::once_flag g_err_once[kMaxDevices];
 }  // namespace
+
+// BM_OK, or BM_ERR_TIMEOUT once a kernel gave up a bounded wait; one per device.
+__device__ unsigned int g_device_error;
+
+unsigned int *device_error_word()
+{
+    int d = -1;
+    if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDevices) return nullptr;
+    std::call_once(g_err_once[d], [d] {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_error) == cudaSuccess) g_err_addr[d] = static_cast<unsigned int *>(p);
+    });
+    return g_err_addr[d];
+}
+
+bool pdl_enabled() { return g_pdl.load(std::memory_order_relaxed) != 0; }
+
+int read_device_error(cudaStream_t s)
+{
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return fail(BM_ERR_CUDA, "stream synchronize failed: %s", cudaGetErrorString(e));
+    unsigned int *w = device_error_word();
+    if (!w) return fail(BM_ERR_CUDA, "device error word unavailable");
+    unsigned int v = 0, zero = 0;
+    e = cudaMemcpy(&v, w, sizeof v, cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess) e = cudaMemcpy(w, &zero, sizeof zero, cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return fail(BM_ERR_CUDA, "reading the device error word failed: %s", cudaGetErrorString(e));
+    if (v != 0) return fail((int)v, "a kernel gave up a bounded wait");
+    return BM_OK;
+}
 
 bool current_device(DeviceInfo *info, int *status)
 {
@@ -194,6 +228,51 @@ int bm_f16_matvec_multi(int nmat, const uint16_t *const *W, const int64_t *rows,
     return launch_vecdot_1col(job, reinterpret_cast<cudaStream_t>(stream), dev);
 }
 
+int bm_f16_matvec_act(int nmat, const uint16_t *const *W, const int64_t *rows, int64_t k, const float *x,
+                      uint16_t *h, float *const *y, bm_stream_t stream)
+{
+    clear_error();
+    if (nmat < 1 || nmat > 4) return fail(BM_ERR_INVALID_ARG, "bm_f16_matvec_act: nmat = %d outside 1..4", nmat);
+    if (!W || !rows || !y) return fail(BM_ERR_INVALID_ARG, "bm_f16_matvec_act: null host array");
+    if (k < 1 || k > BM_MAX_K) return fail(BM_ERR_INVALID_ARG, "bm_f16_matvec_act: k = %lld outside 1..%d", (long long)k, BM_MAX_K);
+    if (!x) return fail(BM_ERR_INVALID_ARG, "bm_f16_matvec_act: null activation");
+    if (!aligned(x, 16) || (h && !aligned(h, 16)))
+        return fail(BM_ERR_ALIGNMENT, "bm_f16_matvec_act: x and h must be 16-byte aligned");
+    if (h && overlap(h, k * 2, x, k * 4)) return fail(BM_ERR_INVALID_ARG, "bm_f16_matvec_act: h overlaps x");
+    VecdotJob job{};
+    job.k = k;
+    job.ncols = 1;
+    for (int m = 0; m < nmat; m++) {
+        // the products' checks, with the activation standing in as X (same size in bytes or larger)
+        int st = check_matrix_args("bm_f16_matvec_act", W[m], rows[m], k, reinterpret_cast<const uint16_t *>(x), 1, y[m]);
+        if (st != BM_OK) return st;
+        if (overlap(y[m], rows[m] * 4, x, k * 4) || (h && (overlap(h, k * 2, y[m], rows[m] * 4) ||
+                                                          overlap(h, k * 2, W[m], rows[m] * k * 2))))
+            return fail(BM_ERR_INVALID_ARG, "bm_f16_matvec_act: output %d overlaps an input or output", m);
+        for (int q = 0; q < m; q++)
+            if (overlap(y[m], rows[m] * 4, y[q], rows[q] * 4) || overlap(y[m], rows[m] * 4, W[q], rows[q] * k * 2) ||
+                overlap(y[q], rows[q] * 4, W[m], rows[m] * k * 2))
+                return fail(BM_ERR_INVALID_ARG, "bm_f16_matvec_act: output %d overlaps an input or output", m);
+        if (rows[m] == 0) continue;
+        job.W[job.nmat] = W[m];
+        job.y[job.nmat] = y[m];
+        job.rows[job.nmat] = rows[m];
+        job.nmat++;
+    }
+    int st;
+    DeviceInfo dev;
+    if (!current_device(&dev, &st)) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (job.nmat == 0) return h ? launch_to_f16(x, h, k, s, dev) : BM_OK;
+    if (k % 8 == 0) return launch_gemv_stream(job, x, h, s, dev);
+    // rows that are not 16-byte aligned: round into h, then the lane-per-chain kernel
+    if (!h) return fail(BM_ERR_INVALID_ARG, "bm_f16_matvec_act: k %% 8 != 0 needs the h buffer");
+    st = launch_to_f16(x, h, k, s, dev);
+    if (st != BM_OK) return st;
+    job.X = h;
+    return launch_vecdot_1col(job, s, dev);
+}
+
 int bm_f16_matmul(const uint16_t *W, int64_t rows, int64_t k, const uint16_t *X, int64_t ncols, float *Y,
                   bm_stream_t stream)
 {
@@ -206,6 +285,12 @@ int bm_f16_logits(const uint16_t *E, int64_t vocab, int64_t hidden, const uint16
 {
     clear_error();
     return product("bm_f16_logits", E, vocab, hidden, X, ncols, Y, stream);
+}
+
+int bm_set_pdl(int enable)
+{
+    clear_error();
+    return g_pdl.exchange(enable ? 1 : 0);
 }
 
 int bm_device_status(bm_stream_t stream)

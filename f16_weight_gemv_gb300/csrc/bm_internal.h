@@ -20,6 +20,13 @@ bool current_device(DeviceInfo *info, int *status);
 // Records a reason for the calling host thread and returns `status`.
 int fail(int status, const char *fmt, ...);
 
+// Device address of this library's error word on the current device (kernels
+// that give up a bounded wait write BM_ERR_TIMEOUT there), or null on failure.
+unsigned int *device_error_word();
+
+// Whether products are launched with programmatic dependent launch (bm_set_pdl).
+bool pdl_enabled();
+
 // Up to four matrices that share one activation (the fused Q/K/V or gate/up
 // products), or one matrix with several activation columns.
 struct VecdotJob {
@@ -37,6 +44,11 @@ struct VecdotJob {
 int launch_to_f16(const float *x, uint16_t *h, int64_t n, cudaStream_t s, const DeviceInfo &dev);
 // One column, any k; uses the 16-byte fast kernel when k % 8 == 0.
 int launch_vecdot_1col(const VecdotJob &job, cudaStream_t s, const DeviceInfo &dev);
+// One column, k % 8 == 0: rows streamed through shared memory by TMA.  With
+// x_f32 non-null the activation is read in f32 and rounded in the kernel
+// (job.X is then unused); h_out, if non-null, receives the rounded activation.
+int launch_gemv_stream(const VecdotJob &job, const float *x_f32, uint16_t *h_out, cudaStream_t s,
+                       const DeviceInfo &dev);
 // ncols >= 1 columns of one matrix, any k, Y[c*rows + r], bit-exact vec_dot.
 int launch_vecdot_ncol(const VecdotJob &job, cudaStream_t s, const DeviceInfo &dev);
 // Tensor-core product for bm_takes_sgemm shapes (rows % 4 == 0, k % 8 == 0, ncols >= 2).

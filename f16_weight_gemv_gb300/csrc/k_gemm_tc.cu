@@ -22,6 +22,7 @@
 // work, waits (bounded) for the copies and MMAs it has in flight, frees its
 // TMEM and exits.
 #include "../../include/bm.h"
+#include "bm_device.cuh"
 #include "bm_internal.h"
 
 #include <cuda.h>
@@ -29,9 +30,6 @@
 #include <mutex>
 
 namespace bm {
-
-// BM_OK or BM_ERR_TIMEOUT, written by any CTA that gave up a wait.
-__device__ unsigned int g_device_error;
 
 namespace {
 
@@ -50,62 +48,22 @@ struct GemmParams {
     int stages;
     uint32_t tmem_cols;  // power of two >= 32, >= bn
     unsigned long long timeout_ns;
+    unsigned int *err;        // device error word
     int withhold_first_load;  // self-test only: the producer never fills stage 0
 };
 
 // ----------------------------------------------------------------------------- PTX wrappers
 
-__device__ __forceinline__ uint32_t smem_u32(const void *p)
-{
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
+using dev::mbar_expect_tx;
+using dev::mbar_init;
+using dev::mbar_try_wait;
+using dev::now_ns;
+using dev::smem_u32;
 
-__device__ __forceinline__ unsigned long long now_ns()
-{
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
-{
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes)
-{
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// Waits for the phase of parity `parity` to complete; gives up when the CTA's
-// abort flag is raised or after `timeout_ns`, raising the flag itself.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                                  unsigned long long timeout_ns)
+                                                  unsigned long long timeout_ns, unsigned int *err)
 {
-    if (mbar_try_wait(bar, parity)) return true;
-    const unsigned long long t0 = now_ns();
-    while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if (*abort_flag) return false;
-        if (now_ns() - t0 > timeout_ns) {
-            *abort_flag = 1;
-            atomicExch(&g_device_error, (unsigned)BM_ERR_TIMEOUT);
-            return false;
-        }
-    }
+    return dev::mbar_wait(bar, parity, abort_flag, timeout_ns, err);
 }
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int32_t c0, int32_t c1,
@@ -204,8 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         abort_flag = 0;
         issued_slot = 0;
         consumed_slot = 0;
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        dev::fence_barrier_init();
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -229,7 +186,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kb = 0; kb < p.num_kb; kb++) {
             const int s = kb % p.stages;
             const uint32_t ph = (uint32_t)(kb / p.stages) & 1u;
-            if (!mbar_wait_bounded(smem_u32(&empty_bar[s]), ph ^ 1u, abort_v, p.timeout_ns)) break;
+            if (!mbar_wait_bounded(smem_u32(&empty_bar[s]), ph ^ 1u, abort_v, p.timeout_ns, p.err)) break;
             if (p.withhold_first_load && kb == 0) continue;  // self-test: stage 0 is never filled
             const uint32_t a_dst = ring_u32 + (uint32_t)s * stage_bytes;
             const uint32_t b_dst = a_dst + kTileABytes;
@@ -247,7 +204,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kb = 0; kb < p.num_kb; kb++) {
             const int s = kb % p.stages;
             const uint32_t ph = (uint32_t)(kb / p.stages) & 1u;
-            if (!mbar_wait_bounded(smem_u32(&full_bar[s]), ph, abort_v, p.timeout_ns)) break;
+            if (!mbar_wait_bounded(smem_u32(&full_bar[s]), ph, abort_v, p.timeout_ns, p.err)) break;
             tc_fence_after();
             const uint32_t a_addr = ring_u32 + (uint32_t)s * stage_bytes;
             const uint32_t b_addr = a_addr + kTileABytes;
@@ -266,7 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
 
     // ---------------- epilogue: TMEM -> registers -> Y
-    const bool done_ok = mbar_wait_bounded(smem_u32(&done_bar), 0, abort_v, p.timeout_ns);
+    const bool done_ok = mbar_wait_bounded(smem_u32(&done_bar), 0, abort_v, p.timeout_ns, p.err);
     tc_fence_after();
     // tcgen05.ld is warp-collective: the decision must be the same for all 32 lanes.
     const bool go = __all_sync(0xffffffffu, done_ok && !*abort_v);
@@ -369,6 +326,8 @@ int launch_impl(const uint16_t *W, int64_t rows, int64_t k, const uint16_t *X, i
     if (p.stages > kMaxStages) p.stages = kMaxStages;
     if (p.stages < 2) return fail(BM_ERR_CUDA, "tensor-core product: not enough shared memory");
     p.timeout_ns = timeout_ns;
+    p.err = device_error_word();
+    if (!p.err) return fail(BM_ERR_CUDA, "tensor-core product: device error word unavailable");
     p.withhold_first_load = withhold;
 
     CUtensorMap mw, mx;
@@ -405,18 +364,6 @@ int launch_gemm_tc_withheld(const uint16_t *W, int64_t rows, int64_t k, const ui
                             cudaStream_t s, const DeviceInfo &dev, unsigned long long timeout_ns)
 {
     return launch_impl(W, rows, k, X, ncols, Y, s, dev, timeout_ns, 1);
-}
-
-int read_device_error(cudaStream_t s)
-{
-    cudaError_t e = cudaStreamSynchronize(s);
-    if (e != cudaSuccess) return fail(BM_ERR_CUDA, "stream synchronize failed: %s", cudaGetErrorString(e));
-    unsigned int v = 0, zero = 0;
-    e = cudaMemcpyFromSymbol(&v, g_device_error, sizeof v);
-    if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_device_error, &zero, sizeof zero);
-    if (e != cudaSuccess) return fail(BM_ERR_CUDA, "reading the device error word failed: %s", cudaGetErrorString(e));
-    if (v != 0) return fail((int)v, "a tensor-core kernel gave up a bounded wait");
-    return BM_OK;
 }
 
 }  // namespace bm

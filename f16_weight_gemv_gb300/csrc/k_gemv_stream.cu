@@ -1,0 +1,424 @@
+// k_gemv_stream.cu -- the one-column product (ggml_vec_dot_f16 per row, bit for
+// bit) for rows of k % 8 == 0 elements, streamed through shared memory by TMA.
+//
+// The order is that of the page "docs/modules/f16.md" (Design notes, "vec_dot"):
+// 32 f32 chains per row (element 32s + c feeds chain c = 8j + l, accumulator j,
+// lane l), each adding its products in increasing s from +0; then
+// (a0+a2)+(a1+a3) lane-wise, low four lanes + high four lanes, two horizontal
+// adds, and the k%32 tail added in double in order.  Optionally the activation
+// arrives in f32 and is first rounded to f16, nearest-even (Design notes,
+// "Activation"), once per CTA -- the same bits bm_to_f16 gives.
+//
+// Layout on the GPU.  Each matrix's rows are cut into groups of 8; the groups
+// of all (up to four) matrices are split evenly between the CTAs (CTA b owns
+// groups [G*b/n, G*(b+1)/n)), so every SM streams the same number of rows at any
+// product size.  A CTA walks its groups in sub-blocks of up to eight groups of
+// one matrix, and each sub-block in k-slices: a stage holds 32 TMA boxes of
+// 8 rows x 64 elements, i.e. 4, 8, 16 or 32 boxes per group for 8, 4, 2 or 1
+// groups (slices of 256 to 2048 elements).  The boxes of a stage are issued in
+// parallel by 16 threads in four producer warps, two TMA instructions each (one
+// issuing thread cannot keep HBM busy with 1 KB boxes; issue spreads best across
+// warps), each thread arriving on the stage's barrier with its own byte count.
+// Boxes are stored with the
+// 128-byte swizzle (16-byte chunk c of row r lands at chunk c ^ (r % 8)).  Rows
+// past the matrix and columns past k are zero-filled and never used.  Consumer
+// warp w owns group w of the sub-block: four threads per row, thread j holding
+// accumulator j (chains 8j..8j+7) and reading the 16 bytes at element 32s + 8j
+// of each step, the activation's matching 16 bytes as a broadcast.  Lanes
+// 4t..4t+3 serve row (t >> 1) | ((t & 1) << 2), so the two rows of every
+// 8-lane phase differ in bit 2 and their swizzled chunks fall in disjoint
+// banks.  The reduction is two xor-shuffles across the row's four threads,
+// then the lane pairs in registers.
+//
+// Programmatic dependent launch: the producer issues its first ring's worth of
+// weight copies at once -- the weights are not written by the kernel ahead of
+// this one -- while the consumers wait for that kernel (griddepcontrol.wait)
+// before they read the activation; all output writes follow.
+//
+// Every mbarrier wait is bounded; on a give-up the CTA records BM_ERR_TIMEOUT,
+// drains the copies it issued (bounded) and exits.
+#include "../../include/bm.h"
+#include "bm_device.cuh"
+#include "bm_internal.h"
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_fp16.h>
+
+#include <algorithm>
+#include <mutex>
+
+namespace bm {
+namespace {
+
+constexpr int kConsumerWarps = 8;
+constexpr int kProducerWarps = 4;
+constexpr int kIssuersPerWarp = 4;  // lanes of a producer warp that issue TMA copies
+constexpr int kIssuers = kProducerWarps * kIssuersPerWarp;
+constexpr int kThreads = 32 * (kConsumerWarps + kProducerWarps);
+constexpr int kGroupRows = 8;                   // rows per TMA box
+constexpr int kGroupsPerBlock = kConsumerWarps; // sub-block: one group per consumer warp
+constexpr int kBoxCols = 64;                    // 128 bytes: one swizzle row
+constexpr uint32_t kBoxBytes = kGroupRows * kBoxCols * 2;  // 1 KB
+constexpr int kBoxesPerStage = 32;
+constexpr uint32_t kStageBytes = kBoxesPerStage * kBoxBytes;  // 32 KB
+constexpr int kMaxStages = 8;
+constexpr unsigned long long kTimeoutNs = 2000000000ull;
+constexpr unsigned kFull = 0xffffffffu;
+
+// Boxes per group in one stage for a sub-block of ng groups: the stage always
+// holds up to 32 boxes, so a sub-block of few groups takes a wider k-slice.
+__host__ __device__ __forceinline__ int boxes_per_group(int ng)
+{
+    return ng <= 1 ? 32 : ng <= 2 ? 16 : ng <= 4 ? 8 : 4;
+}
+
+struct StreamJob {
+    CUtensorMap map[4];  // W[m] as [rows[m]][k] 16-bit elements, box 64 x 8, 128-byte swizzle
+    float *y[4];
+    int64_t rows[4];
+    int64_t gbeg[5];     // first 8-row group of matrix m; gbeg[nmat] = total groups
+    const void *x;       // activation: f16 bits, or f32 when x_is_f32
+    uint16_t *h_out;     // optional: the rounded activation (written by CTA 0)
+    int x_is_f32;
+    int nmat;
+    int k;
+    int stages;
+    unsigned int *err;
+    unsigned long long timeout_ns;
+};
+
+// a0 += w.lo * x.lo, a1 += w.hi * x.hi: the mixed-precision FMA takes the f16
+// operands as their exact values and rounds once to f32 -- the page's FMA step,
+// since an f16 x f16 product is exact in f32.
+__device__ __forceinline__ void fma2(float &a0, float &a1, uint32_t w, uint32_t x)
+{
+    asm("{\n\t.reg .b16 wl, wh, xl, xh;\n\t"
+        "mov.b32 {wl, wh}, %2;\n\t"
+        "mov.b32 {xl, xh}, %3;\n\t"
+        "fma.rn.f32.f16 %0, wl, xl, %0;\n\t"
+        "fma.rn.f32.f16 %1, wh, xh, %1;\n\t}"
+        : "+f"(a0), "+f"(a1)
+        : "r"(w), "r"(x));
+}
+
+// Lanes l = 0..7 of one accumulator: elements 8j + l of a step.
+__device__ __forceinline__ void fma8(float (&acc)[8], const uint4 &w, const uint4 &x)
+{
+    fma2(acc[0], acc[1], w.x, x.x);
+    fma2(acc[2], acc[3], w.y, x.y);
+    fma2(acc[4], acc[5], w.z, x.z);
+    fma2(acc[6], acc[7], w.w, x.w);
+}
+
+__device__ __forceinline__ float widen(uint16_t h) { return __half2float(__ushort_as_half(h)); }
+
+__device__ __forceinline__ uint32_t pack_rn(float lo, float hi)
+{
+    __half2 p = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&p);
+}
+
+__device__ __forceinline__ int matrix_of(const StreamJob &job, int64_t g)
+{
+    int m = 0;
+#pragma unroll
+    for (int q = 1; q < 4; q++)
+        if (q < job.nmat && g >= job.gbeg[q]) m = q;
+    return m;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int32_t c0, int32_t c1,
+                                            uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+        "[%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+        : "memory");
+}
+
+// Named barrier of the eight consumer warps (the producer warp never joins it).
+__device__ __forceinline__ void consumers_sync() { asm volatile("bar.sync 1, %0;" ::"n"(32 * kConsumerWarps)); }
+
+__global__ void __launch_bounds__(kThreads, 2) k_gemv_stream(const __grid_constant__ StreamJob job)
+{
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t full_bar[kMaxStages];
+    __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
+    __shared__ int abort_flag;
+    __shared__ int issued_slot;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int k = job.k;
+    const int S = job.stages;
+    const uint32_t xbytes = (uint32_t)((2 * k + 1023) / 1024 * 1024);
+    // 1024-byte alignment: the swizzle pattern of the TMA boxes repeats every 1024 bytes
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint16_t *xs = reinterpret_cast<uint16_t *>(smem);  // the f16 activation
+    const uint32_t ring_u = dev::smem_u32(smem) + xbytes;
+    volatile int *abort_v = &abort_flag;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; s++) {
+            dev::mbar_init(dev::smem_u32(&full_bar[s]), kIssuers);
+            dev::mbar_init(dev::smem_u32(&empty_bar[s]), kConsumerWarps);
+        }
+        abort_flag = 0;
+        issued_slot = 0;
+        dev::fence_barrier_init();
+    }
+    __syncthreads();
+    dev::pdl_trigger();  // the next kernel may start its own weight copies
+
+    const int64_t G = job.gbeg[job.nmat];
+    const int64_t glo = G * blockIdx.x / gridDim.x, ghi = G * (blockIdx.x + 1) / gridDim.x;
+    const int nsteps = k >> 5;
+
+    if (warp >= kConsumerWarps) {
+        // ------------------------------------------------------------ producers
+        int t = 0;
+        bool ok = true;
+        for (int64_t g = glo; g < ghi && ok;) {
+            const int m = matrix_of(job, g);
+            const int ng = (int)min((int64_t)kGroupsPerBlock, min(ghi, job.gbeg[m + 1]) - g);
+            const int bpg = boxes_per_group(ng);
+            const int sw = bpg * kBoxCols;  // slice width in elements
+            const int nslices = (k + sw - 1) / sw;
+            const int32_t row0 = (int32_t)((g - job.gbeg[m]) * kGroupRows);
+            for (int sl = 0; sl < nslices; sl++, t++) {
+                const int slot = t % S;
+                const uint32_t ph = (uint32_t)(t / S) & 1u;
+                if (!dev::mbar_wait_warp(dev::smem_u32(&empty_bar[slot]), ph ^ 1u, abort_v, job.timeout_ns, job.err)) {
+                    ok = false;
+                    break;
+                }
+                const int kc0 = sl * sw;
+                const int nb = min(bpg, (k - kc0 + kBoxCols - 1) / kBoxCols);  // boxes per group in this slice
+                if (lane < kIssuersPerWarp) {
+                    // each of the 16 issuers arrives once per stage, announcing the bytes of its own boxes
+                    const int me = (warp - kConsumerWarps) * kIssuersPerWarp + lane;
+                    const uint32_t fb = dev::smem_u32(&full_bar[slot]);
+                    const uint32_t dst = ring_u + (uint32_t)slot * kStageBytes;
+                    const int nbox = ng * nb;  // <= 32 boxes per stage, two per issuer at most
+                    const int mine = (me < nbox ? 1 : 0) + (me + kIssuers < nbox ? 1 : 0);
+                    dev::mbar_expect_tx(fb, (uint32_t)mine * kBoxBytes);
+                    for (int i = me; i < nbox; i += kIssuers) {
+                        const int q = i / nb, b = i % nb;
+                        tma_load_2d(dst + (uint32_t)(q * bpg + b) * kBoxBytes, &job.map[m], kc0 + b * kBoxCols,
+                                    row0 + q * kGroupRows, fb);
+                    }
+                }
+                if (warp == kConsumerWarps && lane == 0) issued_slot = t + 1;
+            }
+            g += ng;
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ consumers
+        dev::pdl_wait();  // the activation is the previous kernel's output; outputs follow too
+        if (job.x_is_f32) {
+            const float4 *xf = reinterpret_cast<const float4 *>(job.x);
+            uint2 *xo = reinterpret_cast<uint2 *>(xs);
+            for (int i = threadIdx.x; i < (k >> 2); i += 32 * kConsumerWarps) {
+                const float4 v = __ldg(xf + i);
+                const uint2 p = make_uint2(pack_rn(v.x, v.y), pack_rn(v.z, v.w));
+                xo[i] = p;
+                if (job.h_out && blockIdx.x == 0) reinterpret_cast<uint2 *>(job.h_out)[i] = p;
+            }
+        } else {
+            const uint4 *xg = reinterpret_cast<const uint4 *>(job.x);
+            uint4 *xo = reinterpret_cast<uint4 *>(xs);
+            for (int i = threadIdx.x; i < (k >> 3); i += 32 * kConsumerWarps) xo[i] = __ldg(xg + i);
+        }
+        consumers_sync();
+
+        const int j = lane & 3;                                   // accumulator (chains 8j..8j+7)
+        const int t4 = lane >> 2;
+        const int rho = (t4 >> 1) | ((t4 & 1) << 2);              // row in the group
+        const uint4 *x4 = reinterpret_cast<const uint4 *>(xs) + j;  // x[32s + 8j] at x4[4s]
+        bool ok = true;
+        int t = 0;
+        for (int64_t g = glo; g < ghi && ok;) {
+            const int m = matrix_of(job, g);
+            const int ng = (int)min((int64_t)kGroupsPerBlock, min(ghi, job.gbeg[m + 1]) - g);
+            const int bpg = boxes_per_group(ng);
+            const int sw = bpg * kBoxCols;
+            const int nslices = (k + sw - 1) / sw;
+            const int64_t row = (g - job.gbeg[m] + warp) * kGroupRows + rho;  // this thread's row
+            const bool active = warp < ng;                                     // warp-uniform
+            float acc[8];
+#pragma unroll
+            for (int e = 0; e < 8; e++) acc[e] = 0.0f;
+            for (int sl = 0; sl < nslices; sl++, t++) {
+                const int slot = t % S;
+                const uint32_t ph = (uint32_t)(t / S) & 1u;
+                if (!dev::mbar_wait_warp(dev::smem_u32(&full_bar[slot]), ph, abort_v, job.timeout_ns, job.err)) {
+                    ok = false;
+                    break;
+                }
+                const int kc0 = sl * sw;
+                // this thread's row inside the stage: group `warp`, box b at +b KB, 128-byte rows
+                const uint8_t *rbase = smem + xbytes + (size_t)slot * kStageBytes +
+                                       (size_t)(warp * bpg) * kBoxBytes + rho * 128;
+                if (active) {
+                    const int nst = min(2 * bpg, nsteps - kc0 / 32);  // chain steps in this slice
+                    int s = 0;
+                    for (; s + 2 <= nst; s += 2) {  // one 64-element box: two steps
+                        const uint8_t *bx = rbase + (s >> 1) * kBoxBytes;
+                        const uint4 w0 = *reinterpret_cast<const uint4 *>(bx + ((j) ^ rho) * 16);
+                        const uint4 w1 = *reinterpret_cast<const uint4 *>(bx + ((4 + j) ^ rho) * 16);
+                        const int S0 = kc0 / 32 + s;
+                        fma8(acc, w0, x4[4 * S0]);
+                        fma8(acc, w1, x4[4 * S0 + 4]);
+                    }
+                    if (s < nst) {
+                        const uint8_t *bx = rbase + (s >> 1) * kBoxBytes;
+                        const uint4 w0 = *reinterpret_cast<const uint4 *>(bx + ((j) ^ rho) * 16);
+                        fma8(acc, w0, x4[4 * (kc0 / 32 + s)]);
+                    }
+                }
+                if (sl == nslices - 1) {
+                    // (a0 + a2) + (a1 + a3) lane by lane: partners j^2 then j^1 among the row's four threads
+#pragma unroll
+                    for (int e = 0; e < 8; e++) acc[e] += __shfl_xor_sync(kFull, acc[e], 2);
+#pragma unroll
+                    for (int e = 0; e < 8; e++) acc[e] += __shfl_xor_sync(kFull, acc[e], 1);
+                    // low four lanes + high four lanes, then the two horizontal adds
+                    const float t0 = acc[0] + acc[4], t1 = acc[1] + acc[5], t2 = acc[2] + acc[6], t3 = acc[3] + acc[7];
+                    const float red = (t0 + t1) + (t2 + t3);
+                    if (active && j == 0 && row < job.rows[m]) {
+                        float out = red;
+                        if (32 * nsteps < k) {
+                            double sum = (double)red;
+                            for (int e = 32 * nsteps; e < k; e++) {
+                                const int cc = e - kc0;  // column inside the slice
+                                const int b = cc >> 6, c = ((cc & 63) >> 3) ^ rho;
+                                const uint16_t w = *reinterpret_cast<const uint16_t *>(rbase + b * kBoxBytes + c * 16 +
+                                                                                       (cc & 7) * 2);
+                                sum += (double)__fmul_rn(widen(w), widen(xs[e]));
+                            }
+                            out = (float)sum;
+                        }
+                        job.y[m][row] = out;
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) dev::mbar_arrive(dev::smem_u32(&empty_bar[slot]));
+            }
+            g += ng;
+        }
+    }
+
+    // ---------------------------------------------------------------- teardown
+    __syncthreads();
+    if (*abort_v && threadIdx.x == 0) {
+        // every copy issued must land before this CTA's shared memory is released
+        const int issued = issued_slot;
+        for (int s = 0; s < S && s < issued; s++) {
+            const int last = issued - 1 - ((issued - 1 - s) % S);  // last stage issued into slot s
+            dev::mbar_drain(dev::smem_u32(&full_bar[s]), (uint32_t)(last / S) & 1u, job.timeout_ns);
+        }
+    }
+    __syncthreads();
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool encoder()
+{
+    std::call_once(g_encode_once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    return g_encode != nullptr;
+}
+
+bool make_row_map(CUtensorMap *map, const uint16_t *W, int64_t rows, int64_t k)
+{
+    cuuint64_t dims[2] = {(cuuint64_t)k, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)k * 2};
+    cuuint32_t box[2] = {(cuuint32_t)kBoxCols, (cuuint32_t)kGroupRows};
+    cuuint32_t estr[2] = {1, 1};
+    return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<uint16_t *>(W), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+constexpr int kMaxDevices = 64;
+std::once_flag g_attr_once[kMaxDevices];
+
+}  // namespace
+
+int launch_gemv_stream(const VecdotJob &vj, const float *x_f32, uint16_t *h_out, cudaStream_t s,
+                       const DeviceInfo &dev)
+{
+    if (!encoder()) return fail(BM_ERR_CUDA, "vec_dot: cuTensorMapEncodeTiled unavailable");
+    if (vj.k > 0x7fffffffLL) return fail(BM_ERR_INVALID_ARG, "vec_dot: k too large");
+    StreamJob job{};
+    job.nmat = vj.nmat;
+    job.k = (int)vj.k;
+    job.x = x_f32 ? static_cast<const void *>(x_f32) : static_cast<const void *>(vj.X);
+    job.x_is_f32 = x_f32 != nullptr;
+    job.h_out = h_out;
+    job.gbeg[0] = 0;
+    for (int m = 0; m < vj.nmat; m++) {
+        if (vj.rows[m] > 0x7fffffffLL) return fail(BM_ERR_INVALID_ARG, "vec_dot: rows must be below 2^31");
+        if (!make_row_map(&job.map[m], vj.W[m], vj.rows[m], vj.k))
+            return fail(BM_ERR_CUDA, "vec_dot: tensor map encoding failed");
+        job.y[m] = vj.y[m];
+        job.rows[m] = vj.rows[m];
+        job.gbeg[m + 1] = job.gbeg[m] + (vj.rows[m] + kGroupRows - 1) / kGroupRows;
+    }
+    for (int m = vj.nmat; m < 4; m++) job.gbeg[m + 1] = job.gbeg[vj.nmat];
+    const int64_t G = job.gbeg[vj.nmat];
+    job.err = device_error_word();
+    if (!job.err) return fail(BM_ERR_CUDA, "vec_dot: device error word unavailable");
+    job.timeout_ns = kTimeoutNs;
+
+    const uint32_t xbytes = (uint32_t)((2 * job.k + 1023) / 1024 * 1024);
+    // Two CTAs per SM, each with a ring as deep as its share of the work needs (2..8
+    // stages of 32 boxes); when the activation leaves no room for two stages at two
+    // CTAs per SM (very long rows), one CTA per SM.
+    int64_t grid = std::min<int64_t>((int64_t)dev.sm_count * 2, G);
+    const int64_t groups_per_cta = (G + grid - 1) / grid;
+    const int64_t boxes_per_cta = groups_per_cta * ((job.k + kBoxCols - 1) / kBoxCols);
+    const int64_t stages_needed = (boxes_per_cta + kBoxesPerStage - 1) / kBoxesPerStage + 1;
+    const int64_t want = std::max<int64_t>(2, std::min<int64_t>(kMaxStages, stages_needed));
+    int64_t room = ((int64_t)dev.max_smem_optin / 2 - 2048 - 1024 - (int64_t)xbytes) / kStageBytes;
+    if (room < 2) {
+        grid = std::min<int64_t>(grid, dev.sm_count);
+        room = ((int64_t)dev.max_smem_optin - 2048 - 1024 - (int64_t)xbytes) / kStageBytes;  // >= 5 for k <= BM_MAX_K
+    }
+    const int stages = (int)std::min<int64_t>(want, room);
+    job.stages = stages;
+    const size_t smem = xbytes + (size_t)stages * kStageBytes + 1024;
+
+    int dev_id = 0;
+    cudaGetDevice(&dev_id);
+    std::call_once(g_attr_once[dev_id & (kMaxDevices - 1)], [&] {
+        cudaFuncSetAttribute(k_gemv_stream, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             dev.max_smem_optin - 1024);
+    });
+
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_enabled() ? 1 : 0;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, k_gemv_stream, job);
+    if (e != cudaSuccess) return fail(BM_ERR_CUDA, "vec_dot (stream): launch failed: %s", cudaGetErrorString(e));
+    return BM_OK;
+}
+
+}  // namespace bm

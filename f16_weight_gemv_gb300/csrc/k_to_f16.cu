@@ -7,6 +7,7 @@
 // cvt.rn.f16x2.f32 rounds to nearest even, keeps f16 subnormals and sends
 // |x| >= 65520 to infinity, which is the IEEE binary16 conversion.
 #include "../../include/bm.h"
+#include "bm_device.cuh"
 #include "bm_internal.h"
 
 #include <cuda_fp16.h>
@@ -24,6 +25,10 @@ __device__ __forceinline__ uint32_t pack_rn(float lo, float hi)
 
 __global__ void __launch_bounds__(kThreads) k_to_f16(const float *__restrict__ x, uint16_t *__restrict__ h, int64_t n)
 {
+    // Under programmatic dependent launch: let the next kernel be scheduled now, and
+    // touch x and h only once the kernel ahead of this one has finished.
+    dev::pdl_trigger();
+    dev::pdl_wait();
     const int64_t nv = n >> 3;
     const int64_t stride = (int64_t)gridDim.x * kThreads;
     const float4 *xv = reinterpret_cast<const float4 *>(x);
@@ -55,8 +60,16 @@ int launch_to_f16(const float *x, uint16_t *h, int64_t n, cudaStream_t s, const 
     int64_t cap = (int64_t)dev.sm_count * 8;  // 8 resident blocks of 256 threads per SM
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    k_to_f16<<<(unsigned)blocks, kThreads, 0, s>>>(x, h, n);
-    cudaError_t e = cudaGetLastError();
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(kThreads);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_enabled() ? 1 : 0;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, k_to_f16, x, h, n);
     if (e != cudaSuccess) return fail(BM_ERR_CUDA, "bm_to_f16: launch failed: %s", cudaGetErrorString(e));
     return BM_OK;
 }

@@ -12,20 +12,15 @@
 // give identical bits.  No split of a chain is ever made; the thread layout
 // decides only who computes a chain, never its order.
 //
-// Two kernels:
-//   rows4 -- one column, k % 8 == 0: four threads per row, thread j owns
-//            accumulator j and streams 16 bytes (8 f16) at element 32s + 8j,
-//            so a row's four threads read one contiguous 64-byte span per step.
-//            The activation is staged in shared memory and read as a broadcast.
-//   lanes -- any k and any number of columns: lane c of a warp owns chain c
-//            (element 32s + c) for a tile of R rows x C columns, with 2-byte
-//            loads (rows need not be 16-byte aligned); the reduction is five
-//            warp shuffles per output.
+// This file holds the lane-per-chain kernel, used for rows whose k % 8 != 0 (not
+// 16-byte aligned, so not TMA-able) and for the multi-column vec_dot fallback:
+// lane c of a warp owns chain c (element 32s + c) for a tile of R rows x C
+// columns, with 2-byte loads; the reduction is five warp shuffles per output.
+// One-column products with k % 8 == 0 go to k_gemv_stream.cu.
 #include "../../include/bm.h"
 #include "bm_internal.h"
 
 #include <cuda_fp16.h>
-#include <mutex>
 
 namespace bm {
 namespace {
@@ -34,43 +29,13 @@ constexpr int kWarps = 8;
 constexpr int kThreads = 32 * kWarps;
 constexpr unsigned kFull = 0xffffffffu;
 
-// a0 += w.lo * x.lo and a1 += w.hi * x.hi, f16 operands, f32 accumulate, one rounding.
-__device__ __forceinline__ void fma2(float &a0, float &a1, uint32_t w, uint32_t x)
-{
-    asm("{\n\t.reg .b16 wl, wh, xl, xh;\n\t"
-        "mov.b32 {wl, wh}, %2;\n\t"
-        "mov.b32 {xl, xh}, %3;\n\t"
-        "fma.rn.f32.f16 %0, wl, xl, %0;\n\t"
-        "fma.rn.f32.f16 %1, wh, xh, %1;\n\t}"
-        : "+f"(a0), "+f"(a1)
-        : "r"(w), "r"(x));
-}
-
 __device__ __forceinline__ void fma1(float &a, uint16_t w, uint16_t x)
 {
     asm("fma.rn.f32.f16 %0, %1, %2, %0;" : "+f"(a) : "h"(w), "h"(x));
 }
 
-// Eight lanes l = 0..7 of one accumulator: element 8j + l of the step.
-__device__ __forceinline__ void fma8(float (&acc)[8], const uint4 &w, const uint4 &x)
-{
-    fma2(acc[0], acc[1], w.x, x.x);
-    fma2(acc[2], acc[3], w.y, x.y);
-    fma2(acc[4], acc[5], w.z, x.z);
-    fma2(acc[6], acc[7], w.w, x.w);
-}
-
 // Weights are read once: no L1 allocation, and a 256-byte L2 prefetch so the
 // next steps of the row are already on their way.
-__device__ __forceinline__ uint4 ld_weights16(const uint4 *p)
-{
-    uint4 v;
-    asm("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
-        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-        : "l"(p));
-    return v;
-}
-
 __device__ __forceinline__ uint16_t ld_weights2(const uint16_t *p)
 {
     uint16_t v;
@@ -96,58 +61,6 @@ __device__ __forceinline__ int matrix_of(const VecdotJob &job, int64_t g)
     for (int q = 1; q < 4; q++)
         if (q < job.nmat && g >= job.gbeg[q]) m = q;
     return m;
-}
-
-// ---------------------------------------------------------------------------
-// rows4: one column, k % 8 == 0, 8 rows per warp, 4 threads per row.
-template <int U>
-__global__ void __launch_bounds__(kThreads) k_vecdot_rows4(const __grid_constant__ VecdotJob job)
-{
-    extern __shared__ uint4 xs4[];
-    const int64_t k = job.k;
-    {
-        const uint4 *xg = reinterpret_cast<const uint4 *>(job.X);
-        for (int64_t i = threadIdx.x; i < (k >> 3); i += kThreads) xs4[i] = __ldg(xg + i);
-    }
-    __syncthreads();
-
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t g = (int64_t)blockIdx.x * kWarps + warp;
-    if (g >= job.gbeg[job.nmat]) return;
-    const int m = matrix_of(job, g);
-    const int64_t rows = job.rows[m];
-    const int j = lane & 3;
-    int64_t r = (g - job.gbeg[m]) * 8 + (lane >> 2);
-    const bool valid = r < rows;
-    if (!valid) r = rows - 1;  // the group's last rows are computed on a copy and dropped
-    const uint16_t *wrow = job.W[m] + r * k;
-    const uint4 *wp = reinterpret_cast<const uint4 *>(wrow) + j;  // element 32s + 8j at wp[4s]
-    const uint4 *xp = xs4 + j;
-    const int64_t nsteps = k >> 5;
-
-    float acc[8];
-#pragma unroll
-    for (int e = 0; e < 8; e++) acc[e] = 0.0f;
-    int64_t s = 0;
-    for (; s + U <= nsteps; s += U) {
-        uint4 wv[U];
-#pragma unroll
-        for (int u = 0; u < U; u++) wv[u] = ld_weights16(wp + 4 * (s + u));
-#pragma unroll
-        for (int u = 0; u < U; u++) fma8(acc, wv[u], xp[4 * (s + u)]);
-    }
-    for (; s < nsteps; s++) fma8(acc, ld_weights16(wp + 4 * s), xp[4 * s]);
-
-    // (a0 + a2) + (a1 + a3), lane by lane: the partner j^2, then j^1, of the row's four threads.
-#pragma unroll
-    for (int e = 0; e < 8; e++) acc[e] += __shfl_xor_sync(kFull, acc[e], 2);
-#pragma unroll
-    for (int e = 0; e < 8; e++) acc[e] += __shfl_xor_sync(kFull, acc[e], 1);
-    // low four lanes + high four lanes, then two horizontal adds
-    const float t0 = acc[0] + acc[4], t1 = acc[1] + acc[5], t2 = acc[2] + acc[6], t3 = acc[3] + acc[7];
-    const float red = (t0 + t1) + (t2 + t3);
-    if (j == 0 && valid)
-        job.y[m][r] = add_tail(red, wrow, reinterpret_cast<const uint16_t *>(xs4), nsteps << 5, k);
 }
 
 // ---------------------------------------------------------------------------
@@ -234,10 +147,6 @@ __global__ void __launch_bounds__(kThreads) k_vecdot_lanes(const __grid_constant
     }
 }
 
-constexpr int kRows4Unroll = 8;
-constexpr int kMaxDevices = 64;
-std::once_flag g_attr_once[kMaxDevices];
-
 int finish(const char *what)
 {
     cudaError_t e = cudaGetLastError();
@@ -273,18 +182,7 @@ int launch_vecdot_1col(const VecdotJob &job_in, cudaStream_t s, const DeviceInfo
     VecdotJob job = job_in;
     job.ncols = 1;
     if (job.k % 8 != 0) return launch_lanes<8, 1>(job, s);
-    int dev_id = 0;
-    cudaGetDevice(&dev_id);
-    std::call_once(g_attr_once[dev_id & (kMaxDevices - 1)], [&] {
-        cudaFuncSetAttribute(k_vecdot_rows4<kRows4Unroll>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             dev.max_smem_optin);
-    });
-    const int64_t groups = set_groups(job, 8);
-    const int64_t blocks = (groups + kWarps - 1) / kWarps;
-    if (blocks > 0x7fffffffLL) return fail(BM_ERR_INVALID_ARG, "vec_dot: product too large for one launch");
-    const size_t smem = (size_t)job.k * 2;
-    k_vecdot_rows4<kRows4Unroll><<<(unsigned)blocks, kThreads, smem, s>>>(job);
-    return finish("vec_dot (rows4)");
+    return launch_gemv_stream(job, nullptr, nullptr, s, dev);
 }
 
 int launch_vecdot_ncol(const VecdotJob &job, cudaStream_t s, const DeviceInfo &)

@@ -92,6 +92,19 @@ int bm_f16_matvec_multi(int nmat, const uint16_t *const *W, const int64_t *rows,
                         const uint16_t *x, float *const *y, bm_stream_t stream);
 
 /*
+ * The activation rounding and the fused one-column products in one launch:
+ * h = bm_to_f16(x), then y[m] = vec_dot(W[m][r], h) for up to four matrices
+ * (f16.md, "Design notes", "Activation" and "vec_dot"; forward.md, Advantages,
+ * "Shared activations": one rounded activation feeds Q, K and V, or gate and
+ * up).  Every bit equals bm_to_f16 followed by bm_f16_matvec_multi.
+ *   x : device, f32[k], 16-byte aligned.  h : device, uint16[k], 16-byte aligned,
+ *   or NULL to skip storing the rounded activation (it is needed, and must be
+ *   given, when k % 8 != 0).  W, rows, y as for bm_f16_matvec_multi (nmat 1..4).
+ */
+int bm_f16_matvec_act(int nmat, const uint16_t *const *W, const int64_t *rows, int64_t k,
+                      const float *x, uint16_t *h, float *const *y, bm_stream_t stream);
+
+/*
  * Y[c*rows + r] = W[r] . X[c] for every row r and column c
  * (f16.md, "Matrix products", mat_mul_par), with the path ggml takes:
  *   - bm_takes_sgemm(rows, k, ncols): tcgen05 tensor cores, f32 accumulation,
@@ -116,6 +129,18 @@ int bm_f16_logits(const uint16_t *E, int64_t vocab, int64_t hidden, const uint16
 /* ggml's path selector (f16.md, "Technical usage"): 1 when
  * ncols >= 2 && rows % 4 == 0 && k % 8 == 0, else 0.  Pure; never fails. */
 int bm_takes_sgemm(int64_t rows, int64_t k, int64_t ncols);
+
+/*
+ * Programmatic dependent launch for the products (default off; process-wide).
+ * When on, a one-column product is launched so that it may start before the
+ * kernel ahead of it on the stream has finished: it begins copying its weight
+ * matrix into shared memory at once and waits for that kernel only before it
+ * reads its activation and writes its output.  Precondition while on: the
+ * kernel immediately ahead of a product on its stream must not write that
+ * product's weight matrix (weights are constants in a forward pass).  Results
+ * are identical either way.  Returns the previous setting.
+ */
+int bm_set_pdl(int enable);
 
 /* Waits for `stream`, then reads and clears this library's device error word
  * on the current device: BM_OK, BM_ERR_TIMEOUT (a kernel gave up a bounded

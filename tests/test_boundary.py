@@ -117,3 +117,19 @@ def test_product_path_is_cuda_only():
     csrc = os.path.join(os.path.dirname(bm.__file__), "csrc")
     for fn in os.listdir(csrc):
         assert "oracle.h" not in open(os.path.join(csrc, fn)).read()
+
+
+def test_matvec_act_host_checks(L):
+    f = L.bm_f16_matvec_act
+    W = (C.c_void_p * 2)(A, A + 2 ** 20)
+    y = (C.c_void_p * 2)(A + 2 ** 24, A + 2 ** 24 + 4096)
+    rows = (C.c_int64 * 2)(16, 16)
+    x, h = A + 2 ** 26, A + 2 ** 27
+    assert f(0, W, rows, 64, x, h, y, None) == 1
+    assert f(2, W, rows, 0, x, h, y, None) == 1
+    assert f(2, W, rows, 64, None, h, y, None) == 1
+    assert f(2, W, rows, 64, x + 4, h, y, None) == 2
+    assert f(2, W, rows, 64, x, h + 2, y, None) == 2
+    assert f(2, W, rows, 64, x, x + 16, y, None) == 1      # h overlaps x
+    yo = (C.c_void_p * 2)(A + 2 ** 24, x + 8)               # y overlaps x
+    assert f(2, W, rows, 64, x, h, yo, None) == 1

@@ -199,3 +199,87 @@ def test_matmul_fallback_bit_exact(bm, rows, k, ncols):
 
 def test_device_status_clean(bm):
     assert bm.bm_device_status() == 0
+
+
+# --------------------------------------------------------------------------- programmatic dependent launch
+
+
+def test_pdl_chain_in_a_graph_is_bit_exact(bm):
+    """A decode-like chain (round -> fused QKV -> round -> O -> round -> fused gate/up ->
+    round -> down) with programmatic dependent launch on, eager and captured in a CUDA
+    graph: every output equals the oracle bit for bit, and so does a repeat."""
+    import torch
+    hid, ffn = 576, 1536
+    Wq, Wk, Wv = rnd_f16(80, (576, hid)), rnd_f16(81, (192, hid)), rnd_f16(82, (192, hid))
+    Wo, Wg, Wu, Wd = rnd_f16(83, (hid, hid)), rnd_f16(84, (ffn, hid)), rnd_f16(85, (ffn, hid)), rnd_f16(86, (hid, ffn))
+    acts = [synth.normal_f32(0, 90 + i, 1.0, n) for i, n in enumerate([hid, hid, hid, ffn])]
+    dW = [to_dev(w) for w in (Wq, Wk, Wv, Wo, Wg, Wu, Wd)]
+    dA = [to_dev(a) for a in acts]
+    dH = [torch.empty(a.size, dtype=torch.float16, device="cuda") for a in acts]
+    outs = [torch.empty(w.shape[0], dtype=torch.float32, device="cuda") for w in (Wq, Wk, Wv, Wo, Wg, Wu, Wd)]
+    s = torch.cuda.Stream()
+
+    def chain():
+        bm.bm_to_f16(dA[0], dH[0], stream=s)
+        bm.bm_f16_matvec_multi(dW[0:3], dH[0], outs[0:3], stream=s)
+        bm.bm_to_f16(dA[1], dH[1], stream=s)
+        bm.bm_f16_matvec(dW[3], dH[1], outs[3], stream=s)
+        bm.bm_to_f16(dA[2], dH[2], stream=s)
+        bm.bm_f16_matvec_multi(dW[4:6], dH[2], outs[4:6], stream=s)
+        bm.bm_to_f16(dA[3], dH[3], stream=s)
+        bm.bm_f16_matvec(dW[6], dH[3], outs[6], stream=s)
+
+    hs = [oracle.to_f16(a) for a in acts]
+    want = [oracle.matvec(Wq, hs[0]), oracle.matvec(Wk, hs[0]), oracle.matvec(Wv, hs[0]), oracle.matvec(Wo, hs[1]),
+            oracle.matvec(Wg, hs[2]), oracle.matvec(Wu, hs[2]), oracle.matvec(Wd, hs[3])]
+    old = bm.bm_set_pdl(True)
+    try:
+        with torch.cuda.stream(s):
+            chain()
+        torch.cuda.synchronize()
+        for o, w in zip(outs, want):
+            assert np.array_equal(bits32(o), bits32(w))
+        for o in outs:
+            o.fill_(float("nan"))
+        g = torch.cuda.CUDAGraph()
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=s):
+            chain()
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        for o, w in zip(outs, want):
+            assert np.array_equal(bits32(o), bits32(w))
+    finally:
+        bm.bm_set_pdl(old)
+    assert bm.bm_device_status() == 0
+
+
+# --------------------------------------------------------------------------- fused rounding + products
+
+
+@pytest.mark.parametrize("rows_list,k,store_h", [
+    ((576, 192, 192), 576, True), ((1536, 1536), 576, False), ((576,), 1536, True), ((49152,), 576, False),
+    ((4096, 1024, 1024), 4096, True), ((13, 5, 300, 1), 1000, True), ((7, 8), 33, True), ((20,), 8, False),
+    ((4096,), 14336, True), ((300,), 65536, False),
+])
+def test_matvec_act_equals_round_then_matvec(bm, rows_list, k, store_h):
+    import torch
+    Ws = [rnd_f16(100 + i, (r, k)) for i, r in enumerate(rows_list)]
+    xf = synth.normal_f32(0, 110, 1.0, k)
+    xf[:3] = [70000.0, -1e-30, 3e-8]  # overflow, f32 subnormal, f16 subnormal
+    h = torch.full((k,), float("nan"), dtype=torch.float16, device="cuda") if store_h else None
+    ys = bm.bm_f16_matvec_act([to_dev(W) for W in Ws], to_dev(xf), h=h)
+    hx = oracle.to_f16(xf)
+    for W, y in zip(Ws, ys):
+        assert np.array_equal(bits32(y), bits32(oracle.matvec(W, hx)))
+    if store_h:
+        assert np.array_equal(h.cpu().numpy().view(np.uint16), hx)
+
+
+def test_matvec_act_unaligned_k_needs_h(bm):
+    import torch
+    W = to_dev(rnd_f16(120, (10, 33)))
+    x = to_dev(synth.normal_f32(0, 121, 1.0, 33))
+    with pytest.raises(bm.BmError):
+        bm.bm_f16_matvec_act([W], x)
