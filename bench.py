@@ -365,6 +365,19 @@ def bench_products(bm, dev, stream, torch):
         gbs = algorithmic_bytes(rows, k) / ms / 1e6
         out.append({"product": name, "rows": rows, "k": k, "ncols": 1, "ms": round(ms, 5), "GB_s": round(gbs, 1),
                     "how": "%d back-to-back launches over %d weight replicas, PDL" % (launches, nrep)})
+        for nc in ([2, 3, 8, 64] if name in ("llama3_8b.q", "llama3_8b.gate") else []):
+            # few columns: HBM-bound, timed like the one-column products
+            Yn = torch.empty((nc, rows), dtype=torch.float32, device=dev)
+            xn = x[:nc].contiguous()
+
+            def chain_n():
+                for i in range(launches):
+                    bm.bm_f16_matmul(reps[i % nrep], xn, Yn, stream=stream)
+
+            ms = graph_time(torch, stream, chain_n) / launches
+            out.append({"product": name, "rows": rows, "k": k, "ncols": nc, "ms": round(ms, 5),
+                        "GB_s": round(algorithmic_bytes(rows, k, nc) / ms / 1e6, 1),
+                        "TFLOP_s": round(2.0 * rows * k * nc / ms / 1e9, 2)})
         Y = torch.empty((512, rows), dtype=torch.float32, device=dev)
         ms = graph_time(torch, stream, lambda: bm.bm_f16_matmul(W, x, Y, stream=stream), reps=5, pre=flush)
         tf = 2.0 * rows * k * 512 / ms / 1e9
@@ -597,7 +610,7 @@ def main():
     if "products" in r:
         line["products"] = r["products"]
         for p in r["products"]:
-            if p["ncols"] == 1:
+            if p["ncols"] <= 64:
                 p["pct_hbm"] = round(100.0 * p["GB_s"] / hbm_peak, 1)
             else:
                 p["pct_bf16_dense_peak"] = round(100.0 * p["TFLOP_s"] / float(peaks.get("bf16_tflops", 1900.0)), 1)

@@ -7,26 +7,40 @@
 // accumulation: Y[c*rows + r] = sum_i W[r][i] * X[c][i].  The result is not
 // tinyBLAS's bit pattern; it is within 4e-6 * sum_i |W[r][i] * X[c][i]| of it.
 //
-// Structure (one 128 x BN output tile per CTA, cta_group::1):
-//   warp 0, one lane : TMA producer.  W tile 128 rows x 64 k and X tile BN
-//                      columns x 64 k, both K-major with the 128-byte swizzle,
-//                      into a ring of shared-memory stages (mbarrier complete_tx).
-//   warp 1, one lane : MMA issuer.  Four tcgen05.mma (K = 16 each) per stage,
-//                      accumulating in TMEM; tcgen05.commit frees the stage.
-//   warps 0..3       : epilogue.  tcgen05.ld 32 lanes x 16 columns per trip and
-//                      masked, coalesced f32 stores (a column of the tile is a
-//                      contiguous run of rows in Y).
+// Persistent, warp-specialised kernel (cta_group::1, one CTA per SM):
+//   warp 0, one lane : TMA producer.  For each k-block a W tile (128 rows x 64)
+//                      and an X tile (BN columns x 64), K-major with the
+//                      128-byte swizzle, into a ring of shared-memory stages.
+//   warp 1, one lane : MMA issuer.  Four tcgen05.mma (K = 16) per k-block into
+//                      one of two TMEM accumulators; tcgen05.commit frees the
+//                      stage, and after a unit's last k-block signals the
+//                      epilogue.  Warp 1 also owns the TMEM allocation.
+//   warps 2..5       : epilogue.  tcgen05.ld (32 lanes x 32 columns per trip)
+//                      then coalesced f32 stores: a column of a tile is a
+//                      contiguous run of rows in Y.  The accumulator is handed
+//                      back to the MMA warp as soon as it has been read, so the
+//                      epilogue of one unit overlaps the MMAs of the next.
+// Work units are (row tile, column tile, k-split).  With S > 1 splits each unit
+// writes its partial tile to a workspace, and for every 32-row quarter of the
+// tile the last of the S units to finish (an atomic counter per quarter) sums
+// the S partials in split order 0..S-1 and writes Y -- so the result does not
+// depend on which unit finishes last.  The split count comes from a cost model
+// of waves x (k-blocks per unit + partial traffic).
+//
 // Out-of-range rows, columns and the k % 64 end are zero-filled by TMA and add
 // +0 exactly.  Every mbarrier wait is bounded by the global timer; on a
-// give-up the CTA records BM_ERR_TIMEOUT in a device word, stops issuing
-// work, waits (bounded) for the copies and MMAs it has in flight, frees its
-// TMEM and exits.
+// give-up the CTA records BM_ERR_TIMEOUT in the device error word, stops
+// issuing work, waits (bounded) for the copies and MMAs it has in flight,
+// frees its TMEM and exits.
 #include "../../include/bm.h"
 #include "bm_device.cuh"
 #include "bm_internal.h"
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
 #include <mutex>
 
 namespace bm {
@@ -36,35 +50,34 @@ namespace {
 constexpr int kBM = 128;          // tile rows (MMA M)
 constexpr int kBK = 64;           // k per stage: one 128-byte swizzle row of f16
 constexpr int kUmmaK = 16;        // k per tcgen05.mma of kind::f16
-constexpr int kThreads = 128;
+constexpr int kEpiWarps = 4;
+constexpr int kThreads = 32 * (2 + kEpiWarps);
 constexpr int kTileABytes = kBM * kBK * 2;  // 16 KB
+constexpr int kMaxStages = 8;
+constexpr int kMaxSplits = 8;
 constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;  // 2 s
 
 struct GemmParams {
     float *Y;
-    int64_t rows, ncols, k;
-    int num_kb;          // ceil(k / 64)
-    int bn;              // tile columns (MMA N), multiple of 16, <= 256
+    float *ws;                // partial tiles, [unit][BN][128] (split count > 1 only)
+    unsigned int *counters;   // one per 32-row quarter of each output tile (split count > 1 only)
+    int rows, ncols, k;
+    int num_kb;               // ceil(k / 64)
+    int bn;                   // tile columns (MMA N), multiple of 16, <= 256
+    int bn_alloc;             // TMEM columns per accumulator: power of two >= max(32, bn)
+    int mt, nt;               // row tiles, column tiles
+    int splits;
     int stages;
-    uint32_t tmem_cols;  // power of two >= 32, >= bn
     unsigned long long timeout_ns;
     unsigned int *err;        // device error word
-    int withhold_first_load;  // self-test only: the producer never fills stage 0
+    int withhold_first_load;  // self-test only: the producer never fills its first stage
 };
-
-// ----------------------------------------------------------------------------- PTX wrappers
 
 using dev::mbar_expect_tx;
 using dev::mbar_init;
 using dev::mbar_try_wait;
 using dev::now_ns;
 using dev::smem_u32;
-
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                                  unsigned long long timeout_ns, unsigned int *err)
-{
-    return dev::mbar_wait(bar, parity, abort_flag, timeout_ns, err);
-}
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int32_t c0, int32_t c1,
                                             uint32_t bar)
@@ -119,147 +132,242 @@ __device__ __forceinline__ void mma_commit(uint32_t bar)
                  : "memory");
 }
 
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16])
+// 32 consecutive accumulator columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32])
 {
     asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-        "%15}, [%16];"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
         : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
-          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]),
+          "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]),
+          "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
         : "r"(taddr));
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-// ----------------------------------------------------------------------------- kernel
+struct Unit {
+    int m0, n0, s, tile, kb0, kb1;
+};
 
-constexpr int kMaxStages = 8;
+// Units are ordered column tile fastest, then split, then row tile: CTAs that
+// run side by side share a W block (the column tiles) through L2.
+__device__ __forceinline__ Unit unit_of(const GemmParams &p, int u)
+{
+    Unit x;
+    const int nt = u % p.nt;
+    const int rest = u / p.nt;
+    x.s = rest % p.splits;
+    const int mt = rest / p.splits;
+    x.m0 = mt * kBM;
+    x.n0 = nt * p.bn;
+    x.tile = mt * p.nt + nt;
+    x.kb0 = (int)((int64_t)p.num_kb * x.s / p.splits);
+    x.kb1 = (int)((int64_t)p.num_kb * (x.s + 1) / p.splits);
+    return x;
+}
 
 __global__ void __launch_bounds__(kThreads, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_x,
               const GemmParams p)
 {
-    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[kMaxStages];
     __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
+    __shared__ __align__(8) uint64_t acc_full[2];
+    __shared__ __align__(8) uint64_t acc_empty[2];
     __shared__ __align__(8) uint64_t done_bar;
     __shared__ uint32_t tmem_base_slot;
     __shared__ int abort_flag;
-    __shared__ int issued_slot, consumed_slot;
+    __shared__ int issued_slot;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // 1024-byte alignment of the stage ring (the swizzle pattern repeats every 1024 bytes)
     uint8_t *ring = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t ring_u32 = smem_u32(ring);
-    const uint32_t tile_b_bytes = (uint32_t)p.bn * kBK * 2;
-    const uint32_t stage_bytes = kTileABytes + tile_b_bytes;
+    const uint32_t stage_bytes = kTileABytes + (uint32_t)p.bn * kBK * 2;
+    volatile int *abort_v = &abort_flag;
+    const int units = p.mt * p.nt * p.splits;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.stages; s++) {
             mbar_init(smem_u32(&full_bar[s]), 1);
             mbar_init(smem_u32(&empty_bar[s]), 1);
         }
+        for (int b = 0; b < 2; b++) {
+            mbar_init(smem_u32(&acc_full[b]), 1);
+            mbar_init(smem_u32(&acc_empty[b]), kEpiWarps);
+        }
         mbar_init(smem_u32(&done_bar), 1);
         abort_flag = 0;
         issued_slot = 0;
-        consumed_slot = 0;
         dev::fence_barrier_init();
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          smem_u32(&tmem_base_slot)),
-                     "r"(p.tmem_cols)
+                     "r"(2 * p.bn_alloc)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem_d = tmem_base_slot;
+    const uint32_t tmem_base = tmem_base_slot;
 
-    const int64_t m0 = (int64_t)blockIdx.y * kBM;
-    const int64_t n0 = (int64_t)blockIdx.x * p.bn;
-    volatile int *abort_v = &abort_flag;
-
-    if (warp == 0 && lane == 0) {
-        // ---------------- TMA producer
-        int issued = 0;
-        for (int kb = 0; kb < p.num_kb; kb++) {
-            const int s = kb % p.stages;
-            const uint32_t ph = (uint32_t)(kb / p.stages) & 1u;
-            if (!mbar_wait_bounded(smem_u32(&empty_bar[s]), ph ^ 1u, abort_v, p.timeout_ns, p.err)) break;
-            if (p.withhold_first_load && kb == 0) continue;  // self-test: stage 0 is never filled
-            const uint32_t a_dst = ring_u32 + (uint32_t)s * stage_bytes;
-            const uint32_t b_dst = a_dst + kTileABytes;
-            const uint32_t fb = smem_u32(&full_bar[s]);
-            mbar_expect_tx(fb, stage_bytes);
-            tma_load_2d(a_dst, &map_w, kb * kBK, (int32_t)m0, fb);
-            tma_load_2d(b_dst, &map_x, kb * kBK, (int32_t)n0, fb);
-            issued = kb + 1;
-        }
-        issued_slot = issued;
-    } else if (warp == 1 && lane == 0) {
-        // ---------------- MMA issuer
-        const uint32_t idesc = instr_desc_f16(kBM, p.bn);
-        int consumed = 0;
-        for (int kb = 0; kb < p.num_kb; kb++) {
-            const int s = kb % p.stages;
-            const uint32_t ph = (uint32_t)(kb / p.stages) & 1u;
-            if (!mbar_wait_bounded(smem_u32(&full_bar[s]), ph, abort_v, p.timeout_ns, p.err)) break;
-            tc_fence_after();
-            const uint32_t a_addr = ring_u32 + (uint32_t)s * stage_bytes;
-            const uint32_t b_addr = a_addr + kTileABytes;
-#pragma unroll
-            for (int kk = 0; kk < kBK / kUmmaK; kk++) {
-                const uint64_t ad = smem_desc_sw128(a_addr + kk * kUmmaK * 2);
-                const uint64_t bd = smem_desc_sw128(b_addr + kk * kUmmaK * 2);
-                mma_f16(tmem_d, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+    if (warp == 0) {
+        // ---------------------------------------------------------------- TMA producer
+        if (lane == 0) {
+            int t = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+                const Unit x = unit_of(p, u);
+                for (int kb = x.kb0; kb < x.kb1; kb++, t++) {
+                    const int s = t % p.stages;
+                    const uint32_t ph = (uint32_t)(t / p.stages) & 1u;
+                    if (!dev::mbar_wait(smem_u32(&empty_bar[s]), ph ^ 1u, abort_v, p.timeout_ns, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    if (p.withhold_first_load && t == 0) continue;  // self-test: stage 0 is never filled
+                    const uint32_t a_dst = ring_u32 + (uint32_t)s * stage_bytes;
+                    const uint32_t fb = smem_u32(&full_bar[s]);
+                    mbar_expect_tx(fb, stage_bytes);
+                    tma_load_2d(a_dst, &map_w, kb * kBK, x.m0, fb);
+                    tma_load_2d(a_dst + kTileABytes, &map_x, kb * kBK, x.n0, fb);
+                    issued_slot = t + 1;
+                }
             }
-            mma_commit(smem_u32(&empty_bar[s]));  // the stage is free once these MMAs have read it
-            consumed = kb + 1;
         }
-        consumed_slot = consumed;
-        mma_commit(smem_u32(&done_bar));  // always: signals when every issued MMA has finished
-    }
-    __syncwarp();
-
-    // ---------------- epilogue: TMEM -> registers -> Y
-    const bool done_ok = mbar_wait_bounded(smem_u32(&done_bar), 0, abort_v, p.timeout_ns, p.err);
-    tc_fence_after();
-    // tcgen05.ld is warp-collective: the decision must be the same for all 32 lanes.
-    const bool go = __all_sync(0xffffffffu, done_ok && !*abort_v);
-    if (go) {
-        const int64_t row = m0 + warp * 32 + lane;
-        const uint32_t t_row = tmem_d + ((uint32_t)(warp * 32) << 16);
-        for (int c = 0; c < p.bn; c += 16) {
-            uint32_t v[16];
-            tmem_ld16(t_row + (uint32_t)c, v);
-            if (row < p.rows) {
+        __syncwarp();
+    } else if (warp == 1) {
+        // ---------------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc = instr_desc_f16(kBM, p.bn);
+            int t = 0, i = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; u < units && ok; u += gridDim.x, i++) {
+                const Unit x = unit_of(p, u);
+                const int b = i & 1;
+                if (!dev::mbar_wait(smem_u32(&acc_empty[b]), (((uint32_t)i >> 1) & 1u) ^ 1u, abort_v, p.timeout_ns,
+                                    p.err))
+                    break;
+                tc_fence_after();
+                const uint32_t d = tmem_base + (uint32_t)(b * p.bn_alloc);
+                for (int kb = x.kb0; kb < x.kb1; kb++, t++) {
+                    const int s = t % p.stages;
+                    const uint32_t ph = (uint32_t)(t / p.stages) & 1u;
+                    if (!dev::mbar_wait(smem_u32(&full_bar[s]), ph, abort_v, p.timeout_ns, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_addr = ring_u32 + (uint32_t)s * stage_bytes;
+                    const uint32_t b_addr = a_addr + kTileABytes;
 #pragma unroll
-                for (int i = 0; i < 16; i++) {
-                    const int64_t col = n0 + c + i;
-                    if (col < p.ncols) p.Y[col * p.rows + row] = __uint_as_float(v[i]);
+                    for (int kk = 0; kk < kBK / kUmmaK; kk++)
+                        mma_f16(d, smem_desc_sw128(a_addr + kk * kUmmaK * 2), smem_desc_sw128(b_addr + kk * kUmmaK * 2),
+                                idesc, (kb > x.kb0 || kk > 0) ? 1u : 0u);
+                    mma_commit(smem_u32(&empty_bar[s]));  // the stage is free once these MMAs have read it
+                }
+                if (!ok) break;
+                mma_commit(smem_u32(&acc_full[b]));  // the accumulator is complete
+            }
+            mma_commit(smem_u32(&done_bar));  // always: completes when every issued MMA has finished
+        }
+        __syncwarp();
+    } else {
+        // ---------------------------------------------------------------- epilogue
+        const int quarter = warp & 3;                 // TMEM lanes 32*quarter .. +31 (warp % 4 rule)
+        const int rloc = quarter * 32 + lane;         // row inside the tile
+        int i = 0;
+        for (int u = blockIdx.x; u < units; u += gridDim.x, i++) {
+            const Unit x = unit_of(p, u);
+            const int b = i & 1;
+            if (!dev::mbar_wait_warp(smem_u32(&acc_full[b]), ((uint32_t)i >> 1) & 1u, abort_v, p.timeout_ns, p.err))
+                break;
+            tc_fence_after();
+            const uint32_t taddr = tmem_base + (uint32_t)(b * p.bn_alloc) + ((uint32_t)(quarter * 32) << 16);
+            const int row = x.m0 + rloc;
+            float *ws_unit = p.splits > 1 ? p.ws + ((size_t)x.tile * p.splits + x.s) * (size_t)p.bn * kBM : nullptr;
+            for (int c = 0; c < p.bn; c += 32) {
+                uint32_t v[32];
+                tmem_ld32(taddr + (uint32_t)c, v);
+                if (p.splits > 1) {
+#pragma unroll
+                    for (int q = 0; q < 32; q++)
+                        if (c + q < p.bn) ws_unit[(size_t)(c + q) * kBM + rloc] = __uint_as_float(v[q]);
+                } else if (row < p.rows) {
+#pragma unroll
+                    for (int q = 0; q < 32; q++) {
+                        const int col = x.n0 + c + q;
+                        if (c + q < p.bn && col < p.ncols) p.Y[(size_t)col * p.rows + row] = __uint_as_float(v[q]);
+                    }
+                }
+            }
+            // hand the accumulator back to the MMA warp
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) dev::mbar_arrive(smem_u32(&acc_empty[b]));
+
+            if (p.splits > 1) {
+                // the last of the S units of this tile quarter sums the partials in split order
+                __threadfence();
+                __syncwarp();
+                unsigned old = 0;
+                if (lane == 0) old = atomicAdd(&p.counters[x.tile * 4 + quarter], 1u);
+                old = __shfl_sync(0xffffffffu, old, 0);
+                if (old == (unsigned)(p.splits - 1)) {
+                    __threadfence();
+                    const float *ws_row = p.ws + (size_t)x.tile * p.splits * (size_t)p.bn * kBM + rloc;
+                    if (row < p.rows) {
+                        // 32 columns per trip, all of a split's loads in flight at once;
+                        // the sum starts from split 0 and adds the others in order
+                        for (int c0 = 0; c0 < p.bn; c0 += 32) {
+                            float acc[32];
+#pragma unroll
+                            for (int q = 0; q < 32; q++)
+                                acc[q] = (c0 + q < p.bn) ? __ldcg(ws_row + (size_t)(c0 + q) * kBM) : 0.0f;
+                            for (int s = 1; s < p.splits; s++) {
+                                float v[32];
+#pragma unroll
+                                for (int q = 0; q < 32; q++)
+                                    v[q] = (c0 + q < p.bn) ? __ldcg(ws_row + ((size_t)s * p.bn + c0 + q) * kBM) : 0.0f;
+#pragma unroll
+                                for (int q = 0; q < 32; q++) acc[q] += v[q];
+                            }
+#pragma unroll
+                            for (int q = 0; q < 32; q++) {
+                                const int col = x.n0 + c0 + q;
+                                if (c0 + q < p.bn && col < p.ncols) p.Y[(size_t)col * p.rows + row] = acc[q];
+                            }
+                        }
+                    }
+                    if (lane == 0) p.counters[x.tile * 4 + quarter] = 0;  // ready for the next launch
                 }
             }
         }
     }
 
-    // ---------------- teardown
+    // ---------------------------------------------------------------- teardown
     tc_fence_before();
     __syncthreads();
-    if (*abort_v && threadIdx.x == 0) {
-        // Copies issued but never consumed must land before the CTA's shared memory goes away.
-        for (int kb = consumed_slot; kb < issued_slot; kb++) {
-            const int s = kb % p.stages;
-            const uint32_t ph = (uint32_t)(kb / p.stages) & 1u;
-            const unsigned long long t0 = now_ns();
-            while (!mbar_try_wait(smem_u32(&full_bar[s]), ph) && now_ns() - t0 < p.timeout_ns) {
+    if (threadIdx.x == 0) {
+        // no MMA may still be writing TMEM, and on a give-up no copy may still be
+        // landing in shared memory, when the CTA releases them
+        dev::mbar_drain(smem_u32(&done_bar), 0, p.timeout_ns);
+        if (*abort_v) {
+            const int issued = issued_slot;
+            for (int s = 0; s < p.stages && s < issued; s++) {
+                const int last = issued - 1 - ((issued - 1 - s) % p.stages);  // last stage issued into slot s
+                dev::mbar_drain(smem_u32(&full_bar[s]), (uint32_t)(last / p.stages) & 1u, p.timeout_ns);
             }
         }
     }
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_d), "r"(p.tmem_cols)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(2 * p.bn_alloc)
                      : "memory");
     }
 }
@@ -295,58 +403,110 @@ bool make_map(CUtensorMap *map, const uint16_t *base, int64_t outer, int64_t k, 
     return r == CUDA_SUCCESS;
 }
 
-uint32_t pow2_at_least(uint32_t v)
+int pow2_at_least(int v)
 {
-    uint32_t p = 32;
+    int p = 32;
     while (p < v) p <<= 1;
     return p;
 }
 
+// Split count minimising waves x (k-blocks per unit + the partial tile's write and
+// read, counted in k-blocks: about 0.5 + 10 * BN/256 of them -- a wide partial tile
+// costs as much as several k-blocks of operand traffic, a narrow one almost nothing).
+int choose_splits(int tiles, int num_kb, int bn, int ctas)
+{
+    const double partial = 0.5 + 10.0 * bn / 256.0;
+    int best = 1;
+    double best_cost = 1e300;
+    for (int s = 1; s <= kMaxSplits && s <= num_kb; s++) {
+        const double waves = std::ceil((double)tiles * s / ctas);
+        const double cost = waves * ((double)num_kb / s + (s > 1 ? partial : 0.0));
+        if (cost < best_cost - 1e-9) {
+            best_cost = cost;
+            best = s;
+        }
+    }
+    return best;
+}
+
 constexpr int kMaxDevices = 64;
 std::once_flag g_attr_once[kMaxDevices];
+std::once_flag g_pool_once[kMaxDevices];
+cudaMemPool_t g_pool[kMaxDevices];
 
-int launch_impl(const uint16_t *W, int64_t rows, int64_t k, const uint16_t *X, int64_t ncols, float *Y,
-                cudaStream_t s, const DeviceInfo &dev, unsigned long long timeout_ns, int withhold)
+// This library's own stream-ordered memory pool for split-k workspaces (one per
+// device), keeping freed blocks for reuse instead of returning them at every
+// synchronisation.
+cudaMemPool_t workspace_pool(int dev_id)
 {
-    if (!get_encoder()) return fail(BM_ERR_CUDA, "tensor-core product: cuTensorMapEncodeTiled unavailable");
-    if (rows > 0x7fffffffLL || ncols > 0x7fffffffLL)
-        return fail(BM_ERR_INVALID_ARG, "tensor-core product: rows and ncols must be below 2^31");
-    GemmParams p{};
-    p.Y = Y;
-    p.rows = rows;
-    p.ncols = ncols;
-    p.k = k;
+    std::call_once(g_pool_once[dev_id], [dev_id] {
+        cudaMemPoolProps props{};
+        props.allocType = cudaMemAllocationTypePinned;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev_id;
+        cudaMemPool_t pool = nullptr;
+        if (cudaMemPoolCreate(&pool, &props) == cudaSuccess) {
+            uint64_t keep = UINT64_MAX;
+            cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
+            g_pool[dev_id] = pool;
+        }
+    });
+    return g_pool[dev_id];
+}
+
+struct Plan {
+    GemmParams p;
+    int grid;
+    size_t smem;
+    size_t ws_bytes, counter_bytes;
+};
+
+int plan_gemm(Plan *pl, int64_t rows, int64_t k, int64_t ncols, const DeviceInfo &dev, bool allow_split)
+{
+    if (rows > 0x7fffffffLL || ncols > 0x7fffffffLL || k > 0x7fffffffLL)
+        return fail(BM_ERR_INVALID_ARG, "tensor-core product: rows, k and ncols must be below 2^31");
+    GemmParams &p = pl->p;
+    p = GemmParams{};
+    p.rows = (int)rows;
+    p.ncols = (int)ncols;
+    p.k = (int)k;
     p.num_kb = (int)((k + kBK - 1) / kBK);
     const int64_t n16 = (ncols + 15) / 16 * 16;
     p.bn = (int)(n16 < 256 ? n16 : 256);
-    p.tmem_cols = pow2_at_least((uint32_t)p.bn);
+    p.bn_alloc = pow2_at_least(p.bn);
+    p.mt = (int)((rows + kBM - 1) / kBM);
+    p.nt = (int)((ncols + p.bn - 1) / p.bn);
+    const int64_t tiles = (int64_t)p.mt * p.nt;
+    if (tiles * kMaxSplits > 0x7fffffffLL) return fail(BM_ERR_INVALID_ARG, "tensor-core product: too many tiles");
+    p.splits = allow_split ? choose_splits((int)tiles, p.num_kb, p.bn, dev.sm_count) : 1;
     const int stage_bytes = kTileABytes + p.bn * kBK * 2;
     const int budget = dev.max_smem_optin - 1024 - 1024;  // alignment slack and static shared memory
-    p.stages = budget / stage_bytes;
-    if (p.stages > kMaxStages) p.stages = kMaxStages;
+    p.stages = std::min(kMaxStages, budget / stage_bytes);
     if (p.stages < 2) return fail(BM_ERR_CUDA, "tensor-core product: not enough shared memory");
-    p.timeout_ns = timeout_ns;
-    p.err = device_error_word();
-    if (!p.err) return fail(BM_ERR_CUDA, "tensor-core product: device error word unavailable");
-    p.withhold_first_load = withhold;
+    const int64_t units = tiles * p.splits;
+    pl->grid = (int)std::min<int64_t>(units, dev.sm_count);
+    // One CTA per SM (this request is more than half of the SM's shared memory), so the
+    // two accumulators of up to 256 columns each never exceed the SM's 512 TMEM columns.
+    const size_t smem = (size_t)p.stages * stage_bytes + 1024;
+    const size_t one_per_sm = (size_t)dev.max_smem_optin / 2 + 4096;
+    pl->smem = std::max(smem, one_per_sm);
+    pl->ws_bytes = p.splits > 1 ? (size_t)tiles * p.splits * p.bn * kBM * sizeof(float) : 0;
+    pl->counter_bytes = p.splits > 1 ? (size_t)tiles * 4 * sizeof(unsigned int) : 0;
+    return BM_OK;
+}
 
+int launch_plan(const Plan &pl, const uint16_t *W, const uint16_t *X, cudaStream_t s, const DeviceInfo &dev)
+{
+    if (!get_encoder()) return fail(BM_ERR_CUDA, "tensor-core product: cuTensorMapEncodeTiled unavailable");
     CUtensorMap mw, mx;
-    if (!make_map(&mw, W, rows, k, kBM) || !make_map(&mx, X, ncols, k, p.bn))
+    if (!make_map(&mw, W, pl.p.rows, pl.p.k, kBM) || !make_map(&mx, X, pl.p.ncols, pl.p.k, pl.p.bn))
         return fail(BM_ERR_CUDA, "tensor-core product: tensor map encoding failed");
-
     int dev_id = 0;
     cudaGetDevice(&dev_id);
     std::call_once(g_attr_once[dev_id & (kMaxDevices - 1)], [&] {
         cudaFuncSetAttribute(k_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, dev.max_smem_optin - 1024);
     });
-    // One CTA per SM at most (the launch bounds and this shared-memory request),
-    // so the TMEM allocations of co-resident CTAs never exceed 512 columns.
-    const size_t smem = (size_t)p.stages * stage_bytes + 1024;
-    const size_t one_per_sm = 120 * 1024;
-    const size_t smem_req = smem < one_per_sm ? one_per_sm : smem;
-    dim3 grid((unsigned)((ncols + p.bn - 1) / p.bn), (unsigned)((rows + kBM - 1) / kBM));
-    if (grid.y > 65535u) return fail(BM_ERR_INVALID_ARG, "tensor-core product: too many row tiles");
-    k_gemm_tc<<<grid, kThreads, smem_req, s>>>(mw, mx, p);
+    k_gemm_tc<<<pl.grid, kThreads, pl.smem, s>>>(mw, mx, pl.p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail(BM_ERR_CUDA, "tensor-core product: launch failed: %s", cudaGetErrorString(e));
     return BM_OK;
@@ -357,13 +517,51 @@ int launch_impl(const uint16_t *W, int64_t rows, int64_t k, const uint16_t *X, i
 int launch_gemm_tc(const uint16_t *W, int64_t rows, int64_t k, const uint16_t *X, int64_t ncols, float *Y,
                    cudaStream_t s, const DeviceInfo &dev)
 {
-    return launch_impl(W, rows, k, X, ncols, Y, s, dev, kDefaultTimeoutNs, 0);
+    unsigned int *err = device_error_word();
+    if (!err) return fail(BM_ERR_CUDA, "tensor-core product: device error word unavailable");
+    Plan pl;
+    int st = plan_gemm(&pl, rows, k, ncols, dev, true);
+    if (st != BM_OK) return st;
+    pl.p.Y = Y;
+    pl.p.err = err;
+    pl.p.timeout_ns = kDefaultTimeoutNs;
+    if (pl.p.splits == 1) return launch_plan(pl, W, X, s, dev);
+
+    // Split-k workspace: partial tiles and per-quarter counters, stream-ordered (so
+    // concurrent products on other streams never share it, and graph capture
+    // records it as an allocation node).  The counters start at zero.
+    int dev_id = 0;
+    cudaGetDevice(&dev_id);
+    cudaMemPool_t pool = workspace_pool(dev_id & (kMaxDevices - 1));
+    if (!pool) return fail(BM_ERR_CUDA, "tensor-core product: workspace pool unavailable");
+    void *ws = nullptr;
+    cudaError_t e = cudaMallocFromPoolAsync(&ws, pl.ws_bytes + pl.counter_bytes, pool, s);
+    if (e != cudaSuccess)
+        return fail(BM_ERR_CUDA, "tensor-core product: workspace allocation failed: %s", cudaGetErrorString(e));
+    pl.p.ws = static_cast<float *>(ws);
+    pl.p.counters = reinterpret_cast<unsigned int *>(static_cast<char *>(ws) + pl.ws_bytes);
+    e = cudaMemsetAsync(pl.p.counters, 0, pl.counter_bytes, s);
+    st = e == cudaSuccess ? launch_plan(pl, W, X, s, dev)
+                          : fail(BM_ERR_CUDA, "tensor-core product: counter reset failed: %s", cudaGetErrorString(e));
+    cudaError_t e2 = cudaFreeAsync(ws, s);
+    if (st == BM_OK && e2 != cudaSuccess)
+        return fail(BM_ERR_CUDA, "tensor-core product: workspace release failed: %s", cudaGetErrorString(e2));
+    return st;
 }
 
 int launch_gemm_tc_withheld(const uint16_t *W, int64_t rows, int64_t k, const uint16_t *X, int64_t ncols, float *Y,
                             cudaStream_t s, const DeviceInfo &dev, unsigned long long timeout_ns)
 {
-    return launch_impl(W, rows, k, X, ncols, Y, s, dev, timeout_ns, 1);
+    unsigned int *err = device_error_word();
+    if (!err) return fail(BM_ERR_CUDA, "tensor-core product: device error word unavailable");
+    Plan pl;
+    int st = plan_gemm(&pl, rows, k, ncols, dev, false);
+    if (st != BM_OK) return st;
+    pl.p.Y = Y;
+    pl.p.err = err;
+    pl.p.timeout_ns = timeout_ns;
+    pl.p.withhold_first_load = 1;
+    return launch_plan(pl, W, X, s, dev);
 }
 
 }  // namespace bm

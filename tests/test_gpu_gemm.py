@@ -124,3 +124,52 @@ def test_bounded_wait_gives_up_and_context_survives(bm):
     Y2 = bm.bm_f16_matmul(to_dev(Wn), to_dev(Xn)).cpu().numpy()
     check_within(Y2, Wn, Xn)
     assert bm.bm_device_status() == 0
+
+
+SPLIT_SHAPES = [(4096, 4096, 512), (4096, 14336, 512), (4096, 4096, 8), (1024, 8192, 2), (256, 16384, 37)]
+
+
+@pytest.mark.parametrize("rows,k,ncols", SPLIT_SHAPES)
+def test_split_k_shapes_within_bound_and_repeatable(bm, rows, k, ncols):
+    """Shapes with few output tiles take k-splits (partials summed in split order):
+    within the bound, and bit-identical on a second call (the counters reset)."""
+    W = rnd_f16(80, (rows, k))
+    X = act(81, (ncols, k))
+    dW, dX = to_dev(W), to_dev(X)
+    Y1 = bm.bm_f16_matmul(dW, dX)
+    Y2 = bm.bm_f16_matmul(dW, dX)
+    assert np.array_equal(bits32(Y1), bits32(Y2))
+    rng = np.random.default_rng(k + ncols)
+    ri = np.concatenate([[0, rows - 1], rng.integers(0, rows, 2000)])
+    ci = np.concatenate([[ncols - 1, 0], rng.integers(0, ncols, 2000)])
+    check_within(Y1.cpu().numpy(), W, X, (ri, ci))
+
+
+def test_split_k_in_a_cuda_graph_and_concurrent_streams(bm):
+    """The split-k workspace is stream-ordered: the product captures into a CUDA graph
+    and two products on two streams at once do not share it."""
+    import torch
+    rows, k, ncols = 4096, 8192, 64
+    Wa, Wb = rnd_f16(82, (rows, k)), rnd_f16(83, (rows, k))
+    Xa, Xb = act(84, (ncols, k)), act(85, (ncols, k))
+    dWa, dWb, dXa, dXb = to_dev(Wa), to_dev(Wb), to_dev(Xa), to_dev(Xb)
+    ref_a = bits32(bm.bm_f16_matmul(dWa, dXa))
+    ref_b = bits32(bm.bm_f16_matmul(dWb, dXb))
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    Ya = torch.empty((ncols, rows), dtype=torch.float32, device="cuda")
+    Yb = torch.empty((ncols, rows), dtype=torch.float32, device="cuda")
+    torch.cuda.synchronize()
+    for _ in range(3):
+        bm.bm_f16_matmul(dWa, dXa, Ya, stream=s1)
+        bm.bm_f16_matmul(dWb, dXb, Yb, stream=s2)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits32(Ya), ref_a) and np.array_equal(bits32(Yb), ref_b)
+    g = torch.cuda.CUDAGraph()
+    Ya.fill_(float("nan"))
+    with torch.cuda.graph(g, stream=s1):
+        bm.bm_f16_matmul(dWa, dXa, Ya, stream=s1)
+    g.replay()
+    g.replay()
+    torch.cuda.synchronize()
+    assert np.array_equal(bits32(Ya), ref_a)
+    assert bm.bm_device_status() == 0
