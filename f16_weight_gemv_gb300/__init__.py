@@ -17,7 +17,7 @@ import torch
 from . import _build
 
 __all__ = [
-    "BmError", "lib", "bm_to_f16", "bm_f16_matvec", "bm_f16_matvec_multi", "bm_f16_matvec_act", "bm_f16_matmul",
+    "BmError", "lib", "bm_to_f16", "bm_f16_matvec", "bm_f16_matvec_multi", "bm_f16_matvec_act", "bm_f16_matmul", "bm_f16_matmul_noalloc",
     "bm_f16_logits", "bm_takes_sgemm", "bm_device_status", "bm_status_string", "bm_last_error",
     "bm_selftest_wait_timeout", "bm_set_pdl", "EXPORTS", "BM_MAX_K",
 ]
@@ -34,6 +34,7 @@ EXPORTS = {
     "bm_f16_matvec_act": (_i, [_i, C.POINTER(_vp), C.POINTER(_i64), _i64, _vp, _vp, C.POINTER(_vp), _vp]),
     "bm_f16_matmul": (_i, [_vp, _i64, _i64, _vp, _i64, _vp, _vp]),
     "bm_f16_logits": (_i, [_vp, _i64, _i64, _vp, _i64, _vp, _vp]),
+    "bm_f16_matmul_noalloc": (_i, [_vp, _i64, _i64, _vp, _i64, _vp, _vp]),
     "bm_takes_sgemm": (_i, [_i64, _i64, _i64]),
     "bm_device_status": (_i, [_vp]),
     "bm_set_pdl": (_i, [_i]),
@@ -192,6 +193,15 @@ def _product(fn_name: str, W, X, Y, stream):
 def bm_f16_matmul(W, X, Y=None, stream=None):
     """Y[c][r] (Y[c*rows + r] in memory) for W [rows][k] and X [ncols][k]."""
     return _product("bm_f16_matmul", W, X, Y, stream)
+
+
+def bm_f16_matmul_noalloc(W, X, Y, stream=None):
+    """bm_f16_matmul without any device allocation: the library's static scratch
+    replaces the split-k workspace.  Y [ncols][rows] f32 is required (this wrapper
+    allocates nothing either).  Calls that overlap on the GPU race on the scratch."""
+    if Y is None:
+        raise ValueError("bm_f16_matmul_noalloc needs the output tensor Y")
+    return _product("bm_f16_matmul_noalloc", W, X, Y, stream)
 
 
 def bm_f16_logits(E, X, Y=None, stream=None):

@@ -280,6 +280,28 @@ int bm_f16_matmul(const uint16_t *W, int64_t rows, int64_t k, const uint16_t *X,
     return product("bm_f16_matmul", W, rows, k, X, ncols, Y, stream);
 }
 
+int bm_f16_matmul_noalloc(const uint16_t *W, int64_t rows, int64_t k, const uint16_t *X, int64_t ncols, float *Y,
+                          bm_stream_t stream)
+{
+    clear_error();
+    int st = check_matrix_args("bm_f16_matmul_noalloc", W, rows, k, X, ncols, Y);
+    if (st != BM_OK || rows == 0 || ncols == 0) return st;
+    DeviceInfo dev;
+    if (!current_device(&dev, &st)) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (bm_takes_sgemm(rows, k, ncols)) return launch_gemm_tc_noalloc(W, rows, k, X, ncols, Y, s, dev);
+    // the vec_dot kernels use no scratch memory
+    VecdotJob job{};
+    job.W[0] = W;
+    job.y[0] = Y;
+    job.rows[0] = rows;
+    job.nmat = 1;
+    job.k = k;
+    job.X = X;
+    job.ncols = ncols;
+    return ncols == 1 ? launch_vecdot_1col(job, s, dev) : launch_vecdot_ncol(job, s, dev);
+}
+
 int bm_f16_logits(const uint16_t *E, int64_t vocab, int64_t hidden, const uint16_t *X, int64_t ncols, float *Y,
                   bm_stream_t stream)
 {

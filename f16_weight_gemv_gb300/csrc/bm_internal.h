@@ -54,6 +54,10 @@ int launch_vecdot_ncol(const VecdotJob &job, cudaStream_t s, const DeviceInfo &d
 // Tensor-core product for bm_takes_sgemm shapes (rows % 4 == 0, k % 8 == 0, ncols >= 2).
 int launch_gemm_tc(const uint16_t *W, int64_t rows, int64_t k, const uint16_t *X, int64_t ncols,
                    float *Y, cudaStream_t s, const DeviceInfo &dev);
+// As launch_gemm_tc, with the split-k workspace in a static device array instead of
+// a stream-ordered allocation (no allocation of any kind).
+int launch_gemm_tc_noalloc(const uint16_t *W, int64_t rows, int64_t k, const uint16_t *X, int64_t ncols,
+                           float *Y, cudaStream_t s, const DeviceInfo &dev);
 // Self-test of the bounded waits: a 128 x 64 x 16 product whose producer never
 // fills its only stage, so the MMA issuer gives up after `timeout_ns`.
 int launch_gemm_tc_withheld(const uint16_t *W, int64_t rows, int64_t k, const uint16_t *X, int64_t ncols,

@@ -549,6 +549,64 @@ int launch_gemm_tc(const uint16_t *W, int64_t rows, int64_t k, const uint16_t *X
     return st;
 }
 
+// ----------------------------------------------------------------------------- no-allocation variant
+//
+// The same tensor-core product for callers that cannot allocate device memory:
+// its split-k workspace is this file-scope array instead of a stream-ordered
+// allocation.  The array is part of the library's module, so every GPU that
+// loads the library holds it until the process exits.
+
+constexpr size_t kNoAllocScratchBytes = BM_NOALLOC_SCRATCH_BYTES;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+std::once_flag g_scratch_once[kMaxDevices];
+unsigned char *g_scratch_ptr[kMaxDevices];
+cudaError_t g_scratch_status[kMaxDevices];
+}  // namespace
+
+int launch_gemm_tc_noalloc(const uint16_t *W, int64_t rows, int64_t k, const uint16_t *X, int64_t ncols, float *Y,
+                           cudaStream_t s, const DeviceInfo &dev)
+{
+    unsigned int *err = device_error_word();
+    if (!err) return fail(BM_ERR_CUDA, "no-allocation product: device error word unavailable");
+    Plan pl;
+    int st = plan_gemm(&pl, rows, k, ncols, dev, true);
+    if (st != BM_OK) return st;
+    const size_t need = pl.ws_bytes + pl.counter_bytes;
+    if (need > kNoAllocScratchBytes)
+        return fail(BM_ERR_INVALID_ARG,
+                    "bm_f16_matmul_noalloc: this product needs %zu bytes of split-k scratch; the static scratch "
+                    "holds %zu (use bm_f16_matmul)",
+                    need, kNoAllocScratchBytes);
+    pl.p.Y = Y;
+    pl.p.err = err;
+    pl.p.timeout_ns = kDefaultTimeoutNs;
+    if (pl.p.splits > 1) {
+        // In host code g_noalloc_scratch names a host-side stand-in, not device memory:
+        // the kernel gets the device address, looked up once per device with that
+        // device current.
+        int d = -1;
+        if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDevices)
+            return fail(BM_ERR_CUDA, "bm_f16_matmul_noalloc: cannot query the current device");
+        std::call_once(g_scratch_once[d], [d] {
+            void *ptr = nullptr;
+            g_scratch_status[d] = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+            g_scratch_ptr[d] = static_cast<unsigned char *>(ptr);
+        });
+        if (g_scratch_status[d] != cudaSuccess || !g_scratch_ptr[d])
+            return fail(BM_ERR_CUDA, "bm_f16_matmul_noalloc: scratch address lookup failed: %s",
+                        cudaGetErrorString(g_scratch_status[d]));
+        pl.p.ws = reinterpret_cast<float *>(g_scratch_ptr[d]);
+        pl.p.counters = reinterpret_cast<unsigned int *>(g_scratch_ptr[d] + pl.ws_bytes);
+        // the previous call leaves its contents behind: the counters must start at zero
+        cudaError_t e = cudaMemsetAsync(pl.p.counters, 0, pl.counter_bytes, s);
+        if (e != cudaSuccess)
+            return fail(BM_ERR_CUDA, "bm_f16_matmul_noalloc: counter reset failed: %s", cudaGetErrorString(e));
+    }
+    return launch_plan(pl, W, X, s, dev);
+}
+
 int launch_gemm_tc_withheld(const uint16_t *W, int64_t rows, int64_t k, const uint16_t *X, int64_t ncols, float *Y,
                             cudaStream_t s, const DeviceInfo &dev, unsigned long long timeout_ns)
 {

@@ -116,6 +116,35 @@ int bm_f16_matvec_act(int nmat, const uint16_t *const *W, const int64_t *rows, i
 int bm_f16_matmul(const uint16_t *W, int64_t rows, int64_t k, const uint16_t *X, int64_t ncols,
                   float *Y, bm_stream_t stream);
 
+/* Size of the static device scratch that bm_f16_matmul_noalloc uses (8 MiB). */
+#define BM_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+/*
+ * bm_f16_matmul for callers that cannot allocate device memory (no counterpart
+ * on the pages: a property of this library).  Some callers may not call
+ * cudaMalloc or any allocator at all: a serving engine that reserved the whole
+ * device for its own arena at start-up, a plugin living inside a host whose
+ * allocator owns every byte, or a latency-critical thread where an allocation
+ * could block or synchronise.  bm_f16_matmul needs a temporary device workspace
+ * when it splits a product along k; this entry point uses instead a scratch
+ * array that is part of the library's device code, BM_NOALLOC_SCRATCH_BYTES
+ * large, held by every GPU that loads the library until the process exits.
+ * It allocates nothing: no cudaMalloc, no stream-ordered allocation, no
+ * allocating library routine.  The caller still passes W, X and Y, with the
+ * same layout, validation, path selection and results as bm_f16_matmul.
+ *   - A product whose split-k workspace would exceed the scratch is refused with
+ *     BM_ERR_INVALID_ARG and a reason (bm_last_error); nothing is launched.
+ *   - The first call on a device looks up the scratch's device address (once per
+ *     device, with that device current); make that first call before any stream
+ *     capture.
+ *   - Every call shares the one scratch array, which keeps the last call's
+ *     contents; the parts that must start at zero are cleared on the stream by
+ *     each call.  Calls whose kernels overlap on the GPU (e.g. on two streams at
+ *     once) race on the scratch and must be ordered by the caller.
+ */
+int bm_f16_matmul_noalloc(const uint16_t *W, int64_t rows, int64_t k, const uint16_t *X,
+                          int64_t ncols, float *Y, bm_stream_t stream);
+
 /*
  * Logits over a tied token embedding (page "docs/modules/forward.md", Summary:
  * with no output.weight the logits read token_embd.weight): the product of

@@ -133,3 +133,11 @@ def test_matvec_act_host_checks(L):
     assert f(2, W, rows, 64, x, x + 16, y, None) == 1      # h overlaps x
     yo = (C.c_void_p * 2)(A + 2 ** 24, x + 8)               # y overlaps x
     assert f(2, W, rows, 64, x, h, yo, None) == 1
+
+
+def test_matmul_noalloc_host_checks(L):
+    f = "bm_f16_matmul_noalloc"
+    assert st(L, f, A, 16, 64, A + 2 ** 20, 0, A + 2 ** 21, None) == 0
+    assert st(L, f, A, 16, 0, A + 2 ** 20, 2, A + 2 ** 21, None) == 1
+    assert st(L, f, A + 2, 16, 64, A + 2 ** 20, 2, A + 2 ** 21, None) == 2
+    assert st(L, f, A, 16, 64, A + 2 ** 20, 2, A + 2 ** 20 + 64, None) == 1
