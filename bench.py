@@ -48,6 +48,23 @@ SEED = 0
 W_SIGMA, A_SIGMA = 0.02, 1.0
 
 
+# DRAM traffic per launch of the step's kernel, from the ncu launch list of one
+# timed step (profiles/decode_step_smollm2_launches.md), valid only for the kernel
+# source it was measured on (sha256 prefix of k_gemv_stream.cu).
+NCU_TRAFFIC = {"kernel": "k_gemv_stream", "source": "f16_weight_gemv_gb300/csrc/k_gemv_stream.cu",
+               "sha256_16": "b8a74b9ef1768469", "bytes_per_launch": 2254251}
+
+
+def ncu_traffic():
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, NCU_TRAFFIC["source"]), "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()[:16]
+    except OSError:
+        return None
+    return NCU_TRAFFIC["bytes_per_launch"] if sha == NCU_TRAFFIC["sha256_16"] else None
+
+
 def algorithmic_bytes(rows, k, ncols=1):
     return 2 * rows * k + 2 * k * ncols + 4 * rows * ncols
 
@@ -588,7 +605,9 @@ def main():
                    "pdl": not args.no_pdl},
         "pct_of_hbm_peak": round(100.0 * value / world / hbm_peak, 2),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
-                     "frac": round(achieved / hbm_peak, 4), "traffic": None,
+                     "frac": round(achieved / hbm_peak, 4), "traffic": ncu_traffic(),
+                     "traffic_unit": "bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)",
+                     "algorithmic_bytes_per_launch": int(r["tot_bytes"] / r["launches_per_step"]),
                      "kernel": "k_gemv_stream (rounding + one-column GEMV)", "peak_source": peak_src,
                      "launches_per_step": r["launches_per_step"],
                      "how": "the step's only kernel: algorithmic bytes of its launches / CUDA-event time of the "
