@@ -143,7 +143,9 @@ int product(const char *fn, const uint16_t *W, int64_t rows, int64_t k, const ui
     DeviceInfo dev;
     if (!current_device(&dev, &st)) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (bm_takes_sgemm(rows, k, ncols)) return launch_gemm_tc(W, rows, k, X, ncols, Y, s, dev);
+    if (bm_takes_sgemm(rows, k, ncols))
+        return ncols <= kSgemmStreamMaxCols ? launch_sgemm_stream(W, rows, k, X, ncols, Y, s, dev)
+                                            : launch_gemm_tc(W, rows, k, X, ncols, Y, s, dev);
     VecdotJob job{};
     job.W[0] = W;
     job.y[0] = Y;
@@ -289,8 +291,10 @@ int bm_f16_matmul_noalloc(const uint16_t *W, int64_t rows, int64_t k, const uint
     DeviceInfo dev;
     if (!current_device(&dev, &st)) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (bm_takes_sgemm(rows, k, ncols)) return launch_gemm_tc_noalloc(W, rows, k, X, ncols, Y, s, dev);
-    // the vec_dot kernels use no scratch memory
+    // the CUDA-core kernels use no scratch memory
+    if (bm_takes_sgemm(rows, k, ncols))
+        return ncols <= kSgemmStreamMaxCols ? launch_sgemm_stream(W, rows, k, X, ncols, Y, s, dev)
+                                            : launch_gemm_tc_noalloc(W, rows, k, X, ncols, Y, s, dev);
     VecdotJob job{};
     job.W[0] = W;
     job.y[0] = Y;

@@ -51,6 +51,13 @@ int launch_gemv_stream(const VecdotJob &job, const float *x_f32, uint16_t *h_out
                        const DeviceInfo &dev);
 // ncols >= 1 columns of one matrix, any k, Y[c*rows + r], bit-exact vec_dot.
 int launch_vecdot_ncol(const VecdotJob &job, cudaStream_t s, const DeviceInfo &dev);
+// Most columns taken by the CUDA-core tinyBLAS kernel (launch_sgemm_stream); wider
+// bm_takes_sgemm products go to the tensor cores.
+constexpr int kSgemmStreamMaxCols = 16;
+// bm_takes_sgemm shapes with 2..kSgemmStreamMaxCols columns: tinyBLAS's sgemm_dot per
+// element, bit for bit, on the CUDA cores, weights streamed through shared memory by TMA.
+int launch_sgemm_stream(const uint16_t *W, int64_t rows, int64_t k, const uint16_t *X, int64_t ncols, float *Y,
+                        cudaStream_t s, const DeviceInfo &dev);
 // Tensor-core product for bm_takes_sgemm shapes (rows % 4 == 0, k % 8 == 0, ncols >= 2).
 int launch_gemm_tc(const uint16_t *W, int64_t rows, int64_t k, const uint16_t *X, int64_t ncols,
                    float *Y, cudaStream_t s, const DeviceInfo &dev);

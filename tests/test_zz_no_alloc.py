@@ -29,7 +29,9 @@ def act(tid, shape):
     return oracle.to_f16(synth.normal_f32(0, tid, 1.0, shape))
 
 
-@pytest.mark.parametrize("rows,k,ncols", [(4096, 4096, 8), (4096, 4096, 64), (1024, 8192, 3), (1536, 576, 4)])
+# split along k (the scratch in use) for 20..64 columns; 3..8 columns take the CUDA-core kernel
+@pytest.mark.parametrize("rows,k,ncols", [(4096, 4096, 64), (4096, 4096, 32), (1024, 8192, 20), (4096, 4096, 8),
+                                          (1024, 8192, 3), (1536, 576, 4)])
 def test_noalloc_matches_matmul_twice(bm, rows, k, ncols):
     import torch
     W = rnd_f16(200, (rows, k))
