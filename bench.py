@@ -383,8 +383,8 @@ def bench_products(bm, dev, stream, torch):
         out.append({"product": name, "rows": rows, "k": k, "ncols": 1, "ms": round(ms, 5), "GB_s": round(gbs, 1),
                     "how": "%d back-to-back launches over %d weight replicas, PDL" % (launches, nrep)})
         for nc in ([2, 3, 5, 8, 16, 17, 64] if name in ("llama3_8b.q", "llama3_8b.gate") else []):
-            # few columns: HBM-bound, timed like the one-column products (2..16 columns on
-            # the CUDA-core tinyBLAS kernel, 17 and 64 on the tensor cores)
+            # few columns: HBM-bound, timed like the one-column products (2..8 columns on
+            # the CUDA-core tinyBLAS kernel, 16, 17 and 64 on the tensor cores)
             Yn = torch.empty((nc, rows), dtype=torch.float32, device=dev)
             xn = x[:nc].contiguous()
 

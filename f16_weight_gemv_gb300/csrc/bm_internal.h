@@ -53,7 +53,7 @@ int launch_gemv_stream(const VecdotJob &job, const float *x_f32, uint16_t *h_out
 int launch_vecdot_ncol(const VecdotJob &job, cudaStream_t s, const DeviceInfo &dev);
 // Most columns taken by the CUDA-core tinyBLAS kernel (launch_sgemm_stream); wider
 // bm_takes_sgemm products go to the tensor cores.
-constexpr int kSgemmStreamMaxCols = 16;
+constexpr int kSgemmStreamMaxCols = 8;
 // bm_takes_sgemm shapes with 2..kSgemmStreamMaxCols columns: tinyBLAS's sgemm_dot per
 // element, bit for bit, on the CUDA cores, weights streamed through shared memory by TMA.
 int launch_sgemm_stream(const uint16_t *W, int64_t rows, int64_t k, const uint16_t *X, int64_t ncols, float *Y,

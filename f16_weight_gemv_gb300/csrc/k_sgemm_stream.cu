@@ -1,37 +1,44 @@
-// k_sgemm_stream.cu -- products of 2..16 columns on tinyBLAS's path, bit for bit,
+// k_sgemm_stream.cu -- products of 2..8 columns on tinyBLAS's path, bit for bit,
 // for the shapes bm_takes_sgemm accepts (rows % 4 == 0, k % 8 == 0).
 //
 // Page "docs/modules/f16.md" (Design notes, "sgemm_dot"): every output
 // Y[c*rows + r] is eight f32 chains -- lane l adds W[r][8t+l] * X[c][8t+l] in
 // increasing t, from +0 -- folded as ((l0+l4)+(l2+l6))+((l1+l5)+(l3+l7)).  With a
-// few columns the product is bound by streaming W from HBM (2..16 flops per
+// few columns the product is bound by streaming W from HBM (2..8 flops per
 // weight byte), where tensor cores buy nothing; on the CUDA cores the chains keep
 // their order, so the result is tinyBLAS's bit pattern.
 //
 // Layout on the GPU.  One CTA per SM.  Groups of 8 weight rows are split evenly
-// between the CTAs; a CTA walks its groups in sub-blocks of up to 16 groups, and
-// each sub-block in k-slices of 64-element blocks (2 to 8 blocks per slice, more when
-// the sub-block has fewer groups).  A ring slot holds one slice: a TMA box of 8 rows
-// x 64 elements per group and block (128-byte swizzle: 16-byte chunk c of a 128-byte
-// row r lands at c ^ (r % 8)), one box of NCP columns x 64 elements of X per block
-// (NCP = ncols rounded up to even; columns past ncols and elements past k are
-// zero-filled and never stored), and the f32 copy of those X boxes.  Warp roles:
-//   - four issue warps, four lanes each, load the weight boxes of a slot (each of the
-//     16 lanes arrives on the slot's barrier with its own byte count) and, on a
-//     barrier of their own, its X boxes -- as far ahead as the ring allows;
+// between the CTAs; a CTA walks its groups in sub-blocks (R groups per consumer
+// warp) and each sub-block in k-slices of bps 64-element blocks.  A ring slot
+// holds one slice: a TMA box of 8 rows x 64 elements per group and block (128-byte
+// swizzle: 16-byte chunk c of a 128-byte row r lands at c ^ (r % 8)), one box of
+// NCP columns x 64 elements of X per block (NCP = ncols rounded up to even; columns
+// past ncols and elements past k are zero-filled and never stored), and the f32
+// copy of those X boxes.  The slot layout is fixed per launch from the number of
+// groups a CTA owns, so that the ring holds as many weight bytes in flight as
+// shared memory allows (the streaming rate follows the bytes in flight).
+// Warp roles:
+//   - eight issue warps, four lanes each, load the weight boxes of a slot (each of the
+//     32 lanes arrives on the slot's barrier with its own byte count) and, on a
+//     barrier of their own, its X boxes -- as far ahead as the ring allows.  One lane
+//     cannot issue 1 KB boxes fast enough to keep HBM busy, and issue spreads over
+//     warps, not over lanes of one warp (measured);
 //   - two convert warps, alternating slots, widen a slot's X boxes to f32 once they
 //     have landed and signal the slot; the products then read f32 operands only;
-//   - eight consumer warps, 16 rows each: lane 2*r + h holds row r and chains
-//     l = 4h..4h+3 of every column.  Each 8-element step reads the row's 8 bytes
-//     (16 rows per warp in two conflict-free wavefronts, by the swizzle), widens them
-//     once, and for each column reads 16 bytes of widened X (two addresses per warp)
-//     and issues two paired f32 FMAs (fma.rn.f32x2: chains l and l+1).  Every
-//     operand is an exactly widened f16, so every product is exact and every FMA
-//     rounds once, as tinyBLAS's does.  (The mixed-precision f16 x f16 + f32 FMA
-//     would give the same bits but issues at half the f32 FMA rate, which a kernel
-//     doing up to 16 FMAs per weight element cannot afford.)  At the end of a
-//     sub-block the two halves of each chain set meet by one shuffle and the thread
-//     with h == c % 2 folds and stores column c.
+//   - eight consumer warps.  Lane 4*rs + lp of warp w holds row rs of each of the
+//     warp's R groups and chains 2lp, 2lp+1 of every column: 2*R*NCP accumulators.
+//     Each 8-element step reads 4 bytes of each of its R rows (eight rows per warp
+//     and group: one conflict-free wavefront by the swizzle), widens them once, and
+//     for each column reads 8 bytes of widened X (four addresses per warp), which
+//     then feed R rows from registers through paired f32 FMAs (fma.rn.f32x2: chains
+//     2lp and 2lp+1).  Every operand is an exactly widened f16, so every product is
+//     exact and every FMA rounds once, as tinyBLAS's does.  (The mixed-precision
+//     f16 x f16 + f32 FMA would give the same bits but issues at half the f32 FMA
+//     rate, which a kernel doing up to 8 FMAs per weight element cannot afford.)
+//     At the end of a sub-block the four lane pairs of each row meet by two
+//     shuffles: xor 2 forms (l0+l4, l1+l5) and (l2+l6, l3+l7), xor 1 brings the
+//     other pair, and the lane with lp == c % 4 stores column c.
 //
 // Programmatic dependent launch: the weight boxes are issued without waiting for
 // the kernel ahead (weights are constants); the X boxes, which read that kernel's
@@ -53,59 +60,44 @@ namespace bm {
 namespace {
 
 constexpr int kConsumerWarps = 8;
-constexpr int kIssueWarps = 4;      // weight boxes: four lanes of each issue TMA copies
+constexpr int kIssueWarps = 8;  // weight boxes: four lanes of each issue TMA copies
 constexpr int kIssuersPerWarp = 4;
 constexpr int kIssuers = kIssueWarps * kIssuersPerWarp;
-constexpr int kConvertWarps = 2;    // X: load, widen to f32, signal (alternate stages)
+constexpr int kConvertWarps = 2;  // X: widen to f32, signal (alternate slots)
 constexpr int kIssueWarp0 = kConsumerWarps;
 constexpr int kConvertWarp0 = kConsumerWarps + kIssueWarps;
 constexpr int kThreads = 32 * (kConsumerWarps + kIssueWarps + kConvertWarps);
 constexpr int kGroupRows = 8;
-constexpr int kGroupsPerWarp = 2;                              // 16 rows per consumer warp
-constexpr int kGroupsPerBlock = kConsumerWarps * kGroupsPerWarp;  // sub-block of 128 rows
 constexpr int kBoxCols = 64;                                // 128 bytes: one swizzle row
 constexpr uint32_t kWBoxBytes = kGroupRows * kBoxCols * 2;  // 1 KB
-constexpr int kWBoxesPerStage = 32;
-constexpr uint32_t kWBytes = kWBoxesPerStage * kWBoxBytes;  // 32 KB of weights per stage at most
-constexpr int kMaxStages = 8;
+constexpr int kMaxWBoxes = 32;                              // weight boxes per slot
+constexpr int kMaxBlocks = 8;                               // 64-element blocks per slot
+constexpr int kMaxStages = 16;
 constexpr unsigned long long kTimeoutNs = 2000000000ull;
 
-constexpr uint32_t round_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
+// Bytes between consecutive X boxes of a slot: NCP 128-byte rows, padded to whole
+// 1 KB swizzle periods so that column c of every box is swizzle row c % 8.
+__host__ __device__ constexpr uint32_t x16_slot(int ncp) { return ncp <= 8 ? 1024u : 2048u; }
 
-// Shared-memory geometry of one stage for NCP columns (ncols rounded up to even):
-//   [W boxes: 32 KB][X boxes as loaded, f16][X widened to f32]
-// X box b (NCP columns x 64 elements, 128-byte swizzle) sits at a 1 KB-aligned slot so
-// that its column c is swizzle row c % 8; the widened copy holds, per block, NCP rows
-// of 64 f32 (256 bytes each).
-template <int NCP>
-struct Geo {
-    static constexpr int kMaxBlocks = NCP <= 4 ? 8 : 4;  // 64-element blocks per stage at most
-    static constexpr uint32_t kX16Slot = NCP <= 8 ? 1024u : 2048u;
-    static constexpr uint32_t kX16BoxBytes = NCP * 128u;
-    static constexpr uint32_t kX32Block = NCP * 256u;
-    static constexpr uint32_t kX16Off = kWBytes;
-    static constexpr uint32_t kX32Off = kWBytes + kMaxBlocks * kX16Slot;
-    static constexpr uint32_t kStageBytes = round_up(kX32Off + kMaxBlocks * kX32Block, 1024);
-};
-
-// 64-element blocks per stage for a sub-block of ng groups: up to 32 weight boxes, and
-// no more blocks than the X regions of a stage hold.
-template <int NCP>
-__host__ __device__ __forceinline__ int blocks_per_stage(int ng)
-{
-    const int w = ng <= 1 ? 32 : ng <= 2 ? 16 : ng <= 4 ? 8 : ng <= 8 ? 4 : 2;
-    return w < Geo<NCP>::kMaxBlocks ? w : Geo<NCP>::kMaxBlocks;
-}
+// Rows per consumer thread: each widened X value feeds R rows from registers, each
+// widened weight value feeds all NCP columns (2 * R * NCP <= 32 accumulators keep
+// the 576-thread CTA within its registers).
+constexpr int kRowsPerThread = 2;
 
 struct SgemmJob {
     CUtensorMap wmap;  // W as [rows][k] 16-bit elements, box 64 x 8, 128-byte swizzle
     CUtensorMap xmap;  // X as [ncols][k] 16-bit elements, box 64 x NCP, 128-byte swizzle
     float *Y;
     int64_t rows;
-    int64_t groups;    // ceil(rows / 8)
+    int64_t groups;       // ceil(rows / 8)
     int ncols;
     int k;
     int stages;
+    int sub;              // groups per sub-block (<= 8 * R)
+    int bps;              // 64-element blocks per slot (sub * bps <= 32)
+    uint32_t x16_off;     // slot offsets: X boxes, widened X; slot size
+    uint32_t x32_off;
+    uint32_t slot_bytes;
     unsigned int *err;
     unsigned long long timeout_ns;
 };
@@ -121,14 +113,12 @@ __device__ __forceinline__ void widen8(float (&f)[8], const uint4 &h)
         : "r"(h.x), "r"(h.y), "r"(h.z), "r"(h.w));
 }
 
-// Widens the four f16 of an 8-byte chunk to f32 (exact).
-__device__ __forceinline__ void widen4(float (&f)[4], const uint2 &h)
+// Widens the two f16 of a 4-byte word to f32 (exact).
+__device__ __forceinline__ void widen2(float &lo, float &hi, uint32_t h)
 {
-    asm("{\n\t.reg .b16 a, b, c, d;\n\t"
-        "mov.b32 {a, b}, %4;\n\tmov.b32 {c, d}, %5;\n\t"
-        "cvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;\n\tcvt.f32.f16 %2, c;\n\tcvt.f32.f16 %3, d;\n\t}"
-        : "=f"(f[0]), "=f"(f[1]), "=f"(f[2]), "=f"(f[3])
-        : "r"(h.x), "r"(h.y));
+    asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;\n\t}"
+        : "=f"(lo), "=f"(hi)
+        : "r"(h));
 }
 
 // (a0, a1) = (w0 * x0 + a0, w1 * x1 + a1), each rounded once to f32: with f16 operands
@@ -153,40 +143,43 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
-// The walk every role takes: sub-blocks of up to 16 groups of the CTA's range, each in
-// k-slices of blocks_per_stage 64-element blocks; stage t of the walk uses ring slot t % S.
-template <int NCP, typename F>
-__device__ __forceinline__ void walk(int64_t glo, int64_t ghi, int k, F &&f)
+// The walk every role takes: sub-blocks of up to job.sub groups of the CTA's range,
+// each in k-slices of job.bps 64-element blocks; step t of the walk uses ring slot
+// t % stages.  f(t, first group, groups, first column, blocks in the slice, last
+// slice of the sub-block) returns false to stop.
+template <typename F>
+__device__ __forceinline__ void walk(const SgemmJob &job, int64_t glo, int64_t ghi, F &&f)
 {
+    const int k = job.k, sw = job.bps * kBoxCols;
+    const int nslices = (k + sw - 1) / sw;
     int t = 0;
     for (int64_t g = glo; g < ghi;) {
-        const int ng = (int)min((int64_t)kGroupsPerBlock, ghi - g);
-        const int bps = blocks_per_stage<NCP>(ng);
-        const int sw = bps * kBoxCols;
-        const int nslices = (k + sw - 1) / sw;
+        const int ng = (int)min((int64_t)job.sub, ghi - g);
         for (int sl = 0; sl < nslices; sl++, t++)
-            if (!f(t, g, ng, bps, sl * sw, min(bps, (k - sl * sw + kBoxCols - 1) / kBoxCols), sl == nslices - 1))
+            if (!f(t, g, ng, sl * sw, min(job.bps, (k - sl * sw + kBoxCols - 1) / kBoxCols), sl == nslices - 1))
                 return;
         g += ng;
     }
 }
 
-template <int NCP>
+template <int NCP, int R>
 __global__ void __launch_bounds__(kThreads, 1) k_sgemm_stream(const __grid_constant__ SgemmJob job)
 {
-    using G_ = Geo<NCP>;
+    constexpr uint32_t kX16Slot = x16_slot(NCP);
+    constexpr uint32_t kX16BoxBytes = NCP * 128u;
+    constexpr uint32_t kX32Block = NCP * 256u;
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t wfull_bar[kMaxStages];   // weight boxes landed (16 issuer arrivals + bytes)
     __shared__ __align__(8) uint64_t xfull_bar[kMaxStages];   // X boxes landed (1 arrival + bytes)
     __shared__ __align__(8) uint64_t xready_bar[kMaxStages];  // X widened (1 arrival)
     __shared__ __align__(8) uint64_t empty_bar[kMaxStages];   // slot consumed (8 consumer warps)
     __shared__ int abort_flag;
-    __shared__ int w_issued;              // stages whose weight boxes were issued
-    __shared__ int x_last[kMaxStages];    // last stage whose X boxes were issued into slot s
+    __shared__ int w_issued;            // walk steps whose weight boxes were issued
+    __shared__ int x_last[kMaxStages];  // last walk step whose X boxes were issued into slot s
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int k = job.k;
     const int S = job.stages;
+    const int bps = job.bps;
     // 1024-byte alignment: the swizzle pattern of the TMA boxes repeats every 1024 bytes.
     // (Offsetting the __shared__ array itself keeps the pointer in the shared window, so
     // the reads below compile to shared-memory loads, not generic ones.)
@@ -215,21 +208,21 @@ __global__ void __launch_bounds__(kThreads, 1) k_sgemm_stream(const __grid_const
     if (warp >= kConvertWarp0) {
         // ------------------------------------------------------------ X: widen to f32, signal
         const int cw = warp - kConvertWarp0;
-        walk<NCP>(glo, ghi, k, [&](int t, int64_t, int, int, int, int nb, bool) {
+        walk(job, glo, ghi, [&](int t, int64_t, int, int, int nb, bool) {
             if (t % kConvertWarps != cw) return true;
             const int slot = t % S;
             const uint32_t ph = (uint32_t)(t / S) & 1u;
             if (!dev::mbar_wait_warp(dev::smem_u32(&xfull_bar[slot]), ph, abort_v, job.timeout_ns, job.err))
                 return false;
-            uint8_t *stage = smem + (size_t)slot * G_::kStageBytes;
+            uint8_t *stage = smem + (size_t)slot * job.slot_bytes;
             const int nchunks = nb * NCP * 8;
             for (int ci = lane; ci < nchunks; ci += 32) {
                 const int b = ci / (NCP * 8), c = (ci >> 3) % NCP, e8 = ci & 7;
-                const uint4 h = *reinterpret_cast<const uint4 *>(stage + G_::kX16Off + b * G_::kX16Slot + c * 128 +
+                const uint4 h = *reinterpret_cast<const uint4 *>(stage + job.x16_off + b * kX16Slot + c * 128 +
                                                                 ((e8 ^ (c & 7)) << 4));
                 float f[8];
                 widen8(f, h);
-                float4 *d = reinterpret_cast<float4 *>(stage + G_::kX32Off + b * G_::kX32Block + c * 256 + e8 * 32);
+                float4 *d = reinterpret_cast<float4 *>(stage + job.x32_off + b * kX32Block + c * 256 + e8 * 32);
                 d[0] = make_float4(f[0], f[1], f[2], f[3]);
                 d[1] = make_float4(f[4], f[5], f[6], f[7]);
             }
@@ -240,7 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_sgemm_stream(const __grid_const
     } else if (warp >= kIssueWarp0) {
         // ------------------------------------------------------------ weight and X boxes
         bool waited = false;
-        walk<NCP>(glo, ghi, k, [&](int t, int64_t g, int ng, int bps, int kc0, int nb, bool) {
+        walk(job, glo, ghi, [&](int t, int64_t g, int ng, int kc0, int nb, bool) {
             const int slot = t % S;
             const uint32_t ph = (uint32_t)(t / S) & 1u;
             if (!dev::mbar_wait_warp(dev::smem_u32(&empty_bar[slot]), ph ^ 1u, abort_v, job.timeout_ns, job.err))
@@ -248,9 +241,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_sgemm_stream(const __grid_const
             if (lane < kIssuersPerWarp) {
                 const int me = (warp - kIssueWarp0) * kIssuersPerWarp + lane;
                 const uint32_t fb = dev::smem_u32(&wfull_bar[slot]);
-                const uint32_t dst = ring_u + (uint32_t)slot * G_::kStageBytes;
-                const int nw = ng * nb;  // <= 32 boxes, two per issuer at most
-                const int mine = (me < nw ? 1 : 0) + (me + kIssuers < nw ? 1 : 0);
+                const uint32_t dst = ring_u + (uint32_t)slot * job.slot_bytes;
+                const int nw = ng * nb;  // <= 32 boxes: one per issuer at most
+                const int mine = me < nw ? 1 : 0;
                 dev::mbar_expect_tx(fb, (uint32_t)mine * kWBoxBytes);
                 const int32_t row0 = (int32_t)(g * kGroupRows);
                 for (int i = me; i < nw; i += kIssuers) {
@@ -258,18 +251,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_sgemm_stream(const __grid_const
                     tma_load_2d(dst + (uint32_t)(q * bps + b) * kWBoxBytes, &job.wmap, kc0 + b * kBoxCols,
                                 row0 + q * kGroupRows, fb);
                 }
-                if (me == 0) {
-                    // the X boxes of the slot, on their own barrier
+                if (me == kIssuers - 1) {
+                    // the X boxes of the slot, on their own barrier, by the last issuer (it
+                    // issues no more weight boxes than any other)
                     if (!waited) {
                         dev::pdl_wait();  // X is the previous kernel's output
                         waited = true;
                     }
                     const uint32_t xb = dev::smem_u32(&xfull_bar[slot]);
                     x_last[slot] = t;
-                    dev::mbar_expect_tx(xb, (uint32_t)nb * G_::kX16BoxBytes);
+                    dev::mbar_expect_tx(xb, (uint32_t)nb * kX16BoxBytes);
                     for (int b = 0; b < nb; b++)
-                        tma_load_2d(dst + G_::kX16Off + (uint32_t)b * G_::kX16Slot, &job.xmap, kc0 + b * kBoxCols, 0,
-                                    xb);
+                        tma_load_2d(dst + job.x16_off + (uint32_t)b * kX16Slot, &job.xmap, kc0 + b * kBoxCols, 0, xb);
                 }
             }
             if (warp == kIssueWarp0 && lane == 0) w_issued = t + 1;
@@ -279,63 +272,74 @@ __global__ void __launch_bounds__(kThreads, 1) k_sgemm_stream(const __grid_const
     } else {
         // ------------------------------------------------------------ consumers
         dev::pdl_wait();  // output writes follow the kernel ahead
-        const int h = lane & 1;          // lanes 4h..4h+3 of the eight chains
-        const int r16 = lane >> 1;       // row among the warp's 16
-        const int rho = r16 & 7;         // row in its group
-        const int mygrp = warp * kGroupsPerWarp + (r16 >> 3);
-        float acc[NCP][4];
-        walk<NCP>(glo, ghi, k, [&](int t, int64_t g, int ng, int bps, int kc0, int nb, bool last) {
+        const int lp = lane & 3;   // chains 2*lp and 2*lp + 1
+        const int rs = lane >> 2;  // row within each of the warp's R groups
+        float acc[R][NCP][2];
+        walk(job, glo, ghi, [&](int t, int64_t g, int ng, int kc0, int nb, bool last) {
             const int slot = t % S;
             const uint32_t ph = (uint32_t)(t / S) & 1u;
             if (kc0 == 0) {
 #pragma unroll
-                for (int c = 0; c < NCP; c++)
+                for (int j = 0; j < R; j++)
 #pragma unroll
-                    for (int e = 0; e < 4; e++) acc[c][e] = 0.0f;
+                    for (int c = 0; c < NCP; c++) acc[j][c][0] = acc[j][c][1] = 0.0f;
             }
             if (!dev::mbar_wait_warp(dev::smem_u32(&wfull_bar[slot]), ph, abort_v, job.timeout_ns, job.err) ||
                 !dev::mbar_wait_warp(dev::smem_u32(&xready_bar[slot]), ph, abort_v, job.timeout_ns, job.err))
                 return false;
-            const uint8_t *stage = smem + (size_t)slot * G_::kStageBytes;
-            const bool active = mygrp < ng;
-            if (active) {
-                const uint8_t *wrow = stage + (size_t)(mygrp * bps) * kWBoxBytes + rho * 128 + 8 * h;
-                const uint8_t *x32 = stage + G_::kX32Off + 16 * h;
-                const int nst = min(8 * bps, (k - kc0) >> 3);  // 8-element steps in this slice
+            const uint8_t *stage = smem + (size_t)slot * job.slot_bytes;
+            const int nact = min(R, ng - warp * R);  // groups of this warp in the sub-block (warp-uniform)
+            if (nact > 0) {
+                // row rs of group warp*R + j: box (warp*R + j)*bps + b, 128-byte row rs, word lp of a chunk
+                const uint8_t *wrow = stage + (size_t)(warp * R * bps) * kWBoxBytes + rs * 128 + 4 * lp;
+                const uint8_t *x32 = stage + job.x32_off + 8 * lp;
+                const int nst = min(8 * bps, (job.k - kc0) >> 3);  // 8-element steps in this slice
                 for (int b = 0; b * 8 < nst; b++) {
                     const uint8_t *wb = wrow + b * kWBoxBytes;
-                    const uint8_t *xb = x32 + b * G_::kX32Block;
-                    const int n8 = min(8, nst - 8 * b);
-#pragma unroll(NCP >= 12 ? 1 : 2)
-                    for (int c8 = 0; c8 < n8; c8++) {
-                        float w[4];
-                        widen4(w, *reinterpret_cast<const uint2 *>(wb + ((c8 ^ rho) << 4)));
+                    const uint8_t *xb = x32 + b * kX32Block;
+                    // one 8-element step: R weight words, NCP widened X pairs, R * NCP paired FMAs
+                    auto step = [&](int c8) {
+                        float w[R][2];
+#pragma unroll
+                        for (int j = 0; j < R; j++) {
+                            uint32_t h = 0;  // rows of groups past the sub-block are never stored
+                            if (j < nact)
+                                h = *reinterpret_cast<const uint32_t *>(wb + (size_t)(j * bps) * kWBoxBytes +
+                                                                        ((c8 ^ rs) << 4));
+                            widen2(w[j][0], w[j][1], h);
+                        }
 #pragma unroll
                         for (int c = 0; c < NCP; c++) {
-                            const float4 x = *reinterpret_cast<const float4 *>(xb + c * 256 + c8 * 32);
-                            fma_x2(acc[c][0], acc[c][1], w[0], w[1], x.x, x.y);
-                            fma_x2(acc[c][2], acc[c][3], w[2], w[3], x.z, x.w);
+                            const float2 x = *reinterpret_cast<const float2 *>(xb + c * 256 + c8 * 32);
+#pragma unroll
+                            for (int j = 0; j < R; j++) fma_x2(acc[j][c][0], acc[j][c][1], w[j][0], w[j][1], x.x, x.y);
                         }
+                    };
+                    if (nst - 8 * b >= 8) {
+#pragma unroll
+                        for (int c8 = 0; c8 < 8; c8++) step(c8);
+                    } else {
+                        for (int c8 = 0; c8 < nst - 8 * b; c8++) step(c8);
                     }
                 }
             }
             if (last) {
-                // lanes 0..7 of column c are split over this thread and its partner (lane ^ 1):
-                // ((l0+l4)+(l2+l6))+((l1+l5)+(l3+l7)); the thread with h == c % 2 stores it
-                const int64_t row = (g + mygrp) * kGroupRows + rho;
+                // column c of row r: chains 2lp, 2lp+1 sit in lane pair lp of the row's four lanes.
+                // xor 2 pairs lp 0<->2 and 1<->3: (l0+l4, l1+l5) and (l2+l6, l3+l7); xor 1 then
+                // brings the other pair: ((l0+l4)+(l2+l6))+((l1+l5)+(l3+l7)) in every lane of the row.
 #pragma unroll
-                for (int c = 0; c < NCP; c++) {
-                    float p[4];
+                for (int j = 0; j < R; j++) {
+                    const int64_t row = (g + warp * R + j) * kGroupRows + rs;
+                    const bool mine = j < nact && row < job.rows;
 #pragma unroll
-                    for (int e = 0; e < 4; e++) p[e] = __shfl_xor_sync(0xffffffffu, acc[c][e], 1);
-                    float lo[4], hi[4];
-#pragma unroll
-                    for (int e = 0; e < 4; e++) {
-                        lo[e] = h ? p[e] : acc[c][e];
-                        hi[e] = h ? acc[c][e] : p[e];
+                    for (int c = 0; c < NCP; c++) {
+                        const float s0 = acc[j][c][0] + __shfl_xor_sync(0xffffffffu, acc[j][c][0], 2);
+                        const float s1 = acc[j][c][1] + __shfl_xor_sync(0xffffffffu, acc[j][c][1], 2);
+                        const float o0 = __shfl_xor_sync(0xffffffffu, s0, 1);
+                        const float o1 = __shfl_xor_sync(0xffffffffu, s1, 1);
+                        const float y = (lp & 1) ? (o0 + s0) + (o1 + s1) : (s0 + o0) + (s1 + o1);
+                        if (mine && lp == (c & 3) && c < job.ncols) job.Y[(int64_t)c * job.rows + row] = y;
                     }
-                    const float y = ((lo[0] + hi[0]) + (lo[2] + hi[2])) + ((lo[1] + hi[1]) + (lo[3] + hi[3]));
-                    if (active && (c & 1) == h && c < job.ncols && row < job.rows) job.Y[(int64_t)c * job.rows + row] = y;
                 }
             }
             __syncwarp();
@@ -350,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_sgemm_stream(const __grid_const
         // every copy issued must land before this CTA's shared memory is released
         const int issued = w_issued;
         for (int s = 0; s < S && s < issued; s++) {
-            const int lastw = issued - 1 - ((issued - 1 - s) % S);  // last stage whose weights went to slot s
+            const int lastw = issued - 1 - ((issued - 1 - s) % S);  // last step whose weights went to slot s
             dev::mbar_drain(dev::smem_u32(&wfull_bar[s]), (uint32_t)(lastw / S) & 1u, job.timeout_ns);
         }
         for (int s = 0; s < S; s++)
@@ -389,24 +393,31 @@ bool make_map(CUtensorMap *map, const uint16_t *base, int64_t outer, int64_t k, 
 }
 
 constexpr int kMaxDevices = 64;
-std::once_flag g_attr_once[kMaxDevices][9];
+std::once_flag g_attr_once[kMaxDevices][5];
 
 template <int NCP>
 int launch_ncp(SgemmJob &job, cudaStream_t s, const DeviceInfo &dev)
 {
-    using G_ = Geo<NCP>;
-    auto kern = k_sgemm_stream<NCP>;
-    // One CTA per SM, with a ring as deep as its share of the work needs.
+    constexpr int R = kRowsPerThread;
+    auto kern = k_sgemm_stream<NCP, R>;
+    // One CTA per SM.  The slot layout follows the groups a CTA owns: a sub-block of
+    // up to 8*R groups, and as many 64-element blocks per slot as keep its weight boxes
+    // within 32; then as many slots as shared memory holds, so that the most weight
+    // bytes are in flight.
     const int64_t G = job.groups;
     const int64_t grid = std::min<int64_t>((int64_t)dev.sm_count, G);
     const int64_t groups_per_cta = (G + grid - 1) / grid;
-    const int64_t boxes_per_cta = groups_per_cta * ((job.k + kBoxCols - 1) / kBoxCols);
-    const int64_t stages_needed = (boxes_per_cta + kWBoxesPerStage - 1) / kWBoxesPerStage + 1;
-    const int64_t want = std::max<int64_t>(2, std::min<int64_t>(kMaxStages, stages_needed));
-    const int64_t room = ((int64_t)dev.max_smem_optin - 2048 - 1024) / G_::kStageBytes;
+    job.sub = (int)std::min<int64_t>(kConsumerWarps * R, groups_per_cta);
+    job.bps = std::max(1, std::min(kMaxBlocks, kMaxWBoxes / job.sub));
+    job.x16_off = (uint32_t)(job.sub * job.bps) * kWBoxBytes;
+    job.x32_off = job.x16_off + (uint32_t)job.bps * x16_slot(NCP);
+    job.slot_bytes = (job.x32_off + (uint32_t)job.bps * NCP * 256u + 1023u) / 1024u * 1024u;
+    const int64_t slots_per_sub = (job.k + job.bps * kBoxCols - 1) / (job.bps * kBoxCols);
+    const int64_t steps = (groups_per_cta + job.sub - 1) / job.sub * slots_per_sub;
+    const int64_t room = ((int64_t)dev.max_smem_optin - 2048 - 1024) / job.slot_bytes;
     if (room < 2) return fail(BM_ERR_UNSUPPORTED_DEVICE, "sgemm stream: too little shared memory");
-    job.stages = (int)std::min<int64_t>(want, room);
-    const size_t smem = (size_t)job.stages * G_::kStageBytes + 1024;
+    job.stages = (int)std::max<int64_t>(2, std::min<int64_t>({(int64_t)kMaxStages, room, steps}));
+    const size_t smem = (size_t)job.stages * job.slot_bytes + 1024;
 
     int dev_id = 0;
     cudaGetDevice(&dev_id);
@@ -435,7 +446,7 @@ int launch_sgemm_stream(const uint16_t *W, int64_t rows, int64_t k, const uint16
                         cudaStream_t s, const DeviceInfo &dev)
 {
     if (ncols < 2 || ncols > kSgemmStreamMaxCols || rows % 4 != 0 || k % 8 != 0)
-        return fail(BM_ERR_INVALID_ARG, "sgemm stream: shape outside 2..16 columns, rows %% 4 == 0, k %% 8 == 0");
+        return fail(BM_ERR_INVALID_ARG, "sgemm stream: shape outside 2..8 columns, rows %% 4 == 0, k %% 8 == 0");
     if (rows == 0) return BM_OK;
     if (rows > 0x7fffffffLL || k > 0x7fffffffLL) return fail(BM_ERR_INVALID_ARG, "sgemm stream: size too large");
     if (!encoder()) return fail(BM_ERR_CUDA, "sgemm stream: cuTensorMapEncodeTiled unavailable");
@@ -455,11 +466,7 @@ int launch_sgemm_stream(const uint16_t *W, int64_t rows, int64_t k, const uint16
     case 2: return launch_ncp<2>(job, s, dev);
     case 4: return launch_ncp<4>(job, s, dev);
     case 6: return launch_ncp<6>(job, s, dev);
-    case 8: return launch_ncp<8>(job, s, dev);
-    case 10: return launch_ncp<10>(job, s, dev);
-    case 12: return launch_ncp<12>(job, s, dev);
-    case 14: return launch_ncp<14>(job, s, dev);
-    default: return launch_ncp<16>(job, s, dev);
+    default: return launch_ncp<8>(job, s, dev);
     }
 }
 

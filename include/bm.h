@@ -11,7 +11,7 @@
  *     weight has a multiple of 4 rows and the row a multiple of 8 elements, and
  *     falls back to vec_dot otherwise (sections "Summary", "Technical usage",
  *     "Design notes", bullet "sgemm_dot").  Here that tinyBLAS path gives
- *     tinyBLAS's bits for 2..16 columns (CUDA cores, the same chain order) and,
+ *     tinyBLAS's bits for 2..8 columns (CUDA cores, the same chain order) and,
  *     for more columns, runs on tcgen05 tensor cores accurate to
  *     4e-6 * sum|w_i * a_i| of tinyBLAS's result; the fallback is bit-exact.
  *
@@ -108,11 +108,11 @@ int bm_f16_matvec_act(int nmat, const uint16_t *const *W, const int64_t *rows, i
 /*
  * Y[c*rows + r] = W[r] . X[c] for every row r and column c
  * (f16.md, "Matrix products", mat_mul_par), with the path ggml takes:
- *   - bm_takes_sgemm(rows, k, ncols) and ncols <= 16: tinyBLAS's sgemm_dot per
+ *   - bm_takes_sgemm(rows, k, ncols) and ncols <= 8: tinyBLAS's sgemm_dot per
  *     element, bit for bit (eight f32 lane chains, lane l taking elements 8t + l in
  *     increasing t, folded ((l0+l4)+(l2+l6))+((l1+l5)+(l3+l7)); "Design notes",
  *     "sgemm_dot");
- *   - bm_takes_sgemm(rows, k, ncols) and ncols > 16: tcgen05 tensor cores, f32
+ *   - bm_takes_sgemm(rows, k, ncols) and ncols > 8: tcgen05 tensor cores, f32
  *     accumulation, |Y - sgemm_dot(W[r], X[c])| <= 4e-6 * sum_i |W[r][i] * X[c][i]|;
  *   - otherwise: vec_dot per element, bit-exact (ncols == 1 is bm_f16_matvec).
  *   W : device, f16[rows][k].   X : device, f16[ncols][k].   Y : device, f32[ncols*rows].
@@ -167,7 +167,7 @@ int bm_takes_sgemm(int64_t rows, int64_t k, int64_t ncols);
 /*
  * Programmatic dependent launch for the products (default off; process-wide).
  * When on, a product of one column with k % 8 == 0, or a bm_takes_sgemm product
- * of up to 16 columns, is launched so that it may start before the kernel ahead
+ * of up to 8 columns, is launched so that it may start before the kernel ahead
  * of it on the stream has finished: it begins copying its weight matrix into
  * shared memory at once and waits for that kernel only before it reads its
  * activation and writes its output.  Precondition while on: the

@@ -1,4 +1,4 @@
-"""GPU parity of the CUDA-core tinyBLAS kernel (bm_takes_sgemm shapes of 2..16
+"""GPU parity of the CUDA-core tinyBLAS kernel (bm_takes_sgemm shapes of 2..8
 columns) against the oracle, bit for bit.
 
 Each output of these products is tinyBLAS's sgemm_dot (page f16.md, "Design
@@ -18,7 +18,7 @@ from conftest import GOLDEN, bits32, to_dev
 
 pytestmark = pytest.mark.gpu
 
-MAX_STREAM_COLS = 16
+MAX_STREAM_COLS = 8
 
 
 def rnd_f16(tid, shape, sigma=0.02, seed=0):
@@ -46,9 +46,9 @@ def exact_or_sampled(Y, W, X, limit=3e8, nsample=4000):
 # every column count of the kernel; rows with and without a half group (rows % 8 == 4);
 # k with a ragged last 64-element block, a single step, several stages, the maximum
 STREAM_SHAPES = [(12, 1000, n) for n in range(2, MAX_STREAM_COLS + 1)] + [
-    (4, 8, 2), (12, 8, 3), (4, 16, 16), (20, 72, 5), (1536, 576, 4), (1536, 576, 2), (4100, 1536, 3),
-    (4096, 4104, 8), (4096, 4096, 16), (1024, 14336, 7), (576, 1536, 9), (2048, 1024, 12), (8, 65536, 13),
-    (65532, 64, 2), (300, 8200, 11),
+    (4, 8, 2), (12, 8, 3), (4, 16, 8), (20, 72, 5), (1536, 576, 4), (1536, 576, 2), (4100, 1536, 3),
+    (4096, 4104, 8), (4096, 4096, 6), (1024, 14336, 7), (576, 1536, 8), (2048, 1024, 6), (8, 65536, 5),
+    (65532, 64, 2), (300, 8200, 7), (128256, 64, 3), (14336, 4096, 8),
 ]
 
 
@@ -67,7 +67,7 @@ def golden_sgemm_examples():
 
 
 @pytest.mark.parametrize("ex", golden_sgemm_examples(), ids=lambda e: e["name"])
-@pytest.mark.parametrize("ncols", [2, 5, 16])
+@pytest.mark.parametrize("ncols", [2, 5, 8])
 def test_gpu_reproduces_sgemm_worked_examples(bm, ex, ncols):
     """The hand-derived sgemm_dot bits, on the GPU: the example row repeated over 12
     rows (bm_takes_sgemm), inside a larger product of random rows."""
@@ -94,7 +94,7 @@ def test_columns_are_independent(bm):
     W = to_dev(rnd_f16(104, (rows, k)))
     X = act(105, (MAX_STREAM_COLS, k))
     full = bits32(bm.bm_f16_matmul(W, to_dev(X))).reshape(MAX_STREAM_COLS, rows)
-    for n in (2, 3, 4, 5, 8, 9, 13):
+    for n in (2, 3, 4, 5, 6, 7):
         part = bits32(bm.bm_f16_matmul(W, to_dev(X[:n]))).reshape(n, rows)
         assert np.array_equal(part, full[:n])
 
