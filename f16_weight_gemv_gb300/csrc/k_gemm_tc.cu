@@ -410,12 +410,15 @@ int pow2_at_least(int v)
     return p;
 }
 
-// Split count minimising waves x (k-blocks per unit + the partial tile's write and
-// read, counted in k-blocks: about 0.5 + 10 * BN/256 of them -- a wide partial tile
-// costs as much as several k-blocks of operand traffic, a narrow one almost nothing).
+// Split count minimising waves x (k-blocks per unit + the cost of splitting, counted
+// in k-blocks).  Splitting costs the partial tile's write and ordered re-read, the
+// serial reduction by the last unit of each tile and the counter reset: measured on
+// the Llama shapes at 512 columns (gate: 2 waves unsplit beat 3 waves of half-k units
+// by 20 %; down: one wave of half-k units beat 42 % of the SMs unsplit by 28 %), about
+// 8 + 30 * BN/256 k-blocks.
 int choose_splits(int tiles, int num_kb, int bn, int ctas)
 {
-    const double partial = 0.5 + 10.0 * bn / 256.0;
+    const double partial = 8.0 + 30.0 * bn / 256.0;
     int best = 1;
     double best_cost = 1e300;
     for (int s = 1; s <= kMaxSplits && s <= num_kb; s++) {
