@@ -382,9 +382,11 @@ def bench_products(bm, dev, stream, torch):
         gbs = algorithmic_bytes(rows, k) / ms / 1e6
         out.append({"product": name, "rows": rows, "k": k, "ncols": 1, "ms": round(ms, 5), "GB_s": round(gbs, 1),
                     "how": "%d back-to-back launches over %d weight replicas, PDL" % (launches, nrep)})
-        for nc in ([2, 3, 5, 8, 16, 17, 64] if name in ("llama3_8b.q", "llama3_8b.gate") else []):
-            # few columns: HBM-bound, timed like the one-column products (2..8 columns on
-            # the CUDA-core tinyBLAS kernel, 16, 17 and 64 on the tensor cores)
+        few = [(nc, None) for nc in (2, 3, 5, 8, 16, 17, 64)] + [(nc, 8) for nc in (3, 5, 8)]
+        for nc, exact_cols in (few if name in ("llama3_8b.q", "llama3_8b.gate") else []):
+            # few columns: HBM-bound, timed like the one-column products.  The library's
+            # default takes the bit-exact CUDA-core kernel for 2 columns and the tensor
+            # cores for more; the (nc, 8) entries time the bit-exact kernel at 3..8 too.
             Yn = torch.empty((nc, rows), dtype=torch.float32, device=dev)
             xn = x[:nc].contiguous()
 
@@ -392,10 +394,19 @@ def bench_products(bm, dev, stream, torch):
                 for i in range(launches):
                     bm.bm_f16_matmul(reps[i % nrep], xn, Yn, stream=stream)
 
-            ms = graph_time(torch, stream, chain_n) / launches
+            old_cols = bm.bm_set_exact_sgemm_cols(exact_cols) if exact_cols is not None else None
+            try:
+                ms = graph_time(torch, stream, chain_n) / launches
+                cur = bm.bm_set_exact_sgemm_cols(0)  # read the setting in force (and put it back)
+                bm.bm_set_exact_sgemm_cols(cur)
+                exact = nc <= cur
+            finally:
+                if old_cols is not None:
+                    bm.bm_set_exact_sgemm_cols(old_cols)
             out.append({"product": name, "rows": rows, "k": k, "ncols": nc, "ms": round(ms, 5),
                         "GB_s": round(algorithmic_bytes(rows, k, nc) / ms / 1e6, 1),
-                        "TFLOP_s": round(2.0 * rows * k * nc / ms / 1e9, 2)})
+                        "TFLOP_s": round(2.0 * rows * k * nc / ms / 1e9, 2),
+                        "path": "tinyBLAS bit-exact (CUDA cores)" if exact else "tensor cores"})
         Y = torch.empty((512, rows), dtype=torch.float32, device=dev)
         ms = graph_time(torch, stream, lambda: bm.bm_f16_matmul(W, x, Y, stream=stream), reps=5, pre=flush)
         tf = 2.0 * rows * k * 512 / ms / 1e9

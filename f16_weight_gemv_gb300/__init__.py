@@ -19,7 +19,7 @@ from . import _build
 __all__ = [
     "BmError", "lib", "bm_to_f16", "bm_f16_matvec", "bm_f16_matvec_multi", "bm_f16_matvec_act", "bm_f16_matmul", "bm_f16_matmul_noalloc",
     "bm_f16_logits", "bm_takes_sgemm", "bm_device_status", "bm_status_string", "bm_last_error",
-    "bm_selftest_wait_timeout", "bm_set_pdl", "EXPORTS", "BM_MAX_K",
+    "bm_selftest_wait_timeout", "bm_set_pdl", "bm_set_exact_sgemm_cols", "EXPORTS", "BM_MAX_K",
 ]
 
 BM_OK, BM_ERR_INVALID_ARG, BM_ERR_ALIGNMENT, BM_ERR_UNSUPPORTED_DEVICE, BM_ERR_CUDA, BM_ERR_TIMEOUT = range(6)
@@ -38,6 +38,7 @@ EXPORTS = {
     "bm_takes_sgemm": (_i, [_i64, _i64, _i64]),
     "bm_device_status": (_i, [_vp]),
     "bm_set_pdl": (_i, [_i]),
+    "bm_set_exact_sgemm_cols": (_i, [_i]),
     "bm_selftest_wait_timeout": (_i, [_vp, _vp, _vp, _vp]),
     "bm_status_string": (C.c_char_p, [_i]),
     "bm_last_error": (C.c_char_p, []),
@@ -221,6 +222,12 @@ def bm_selftest_wait_timeout(W, X, Y, stream=None) -> int:
 def bm_set_pdl(enable: bool) -> bool:
     """Turn programmatic dependent launch of the products on or off; returns the old setting."""
     return bool(lib().bm_set_pdl(1 if enable else 0))
+
+
+def bm_set_exact_sgemm_cols(ncols: int) -> int:
+    """tinyBLAS-path products of at most `ncols` columns (0..8) take the bit-exact
+    CUDA-core kernel, wider ones the tensor cores; returns the old setting."""
+    return int(lib().bm_set_exact_sgemm_cols(int(ncols)))
 
 
 def bm_status_string(status: int) -> str:

@@ -7,6 +7,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <algorithm>
 #include <atomic>
 #include <mutex>
 
@@ -31,6 +32,7 @@ DeviceInfo g_dev[kMaxDevices];
 std::once_flag g_once[kMaxDevices];
 int g_dev_status[kMaxDevices];
 std::atomic<int> g_pdl{0};
+std::atomic<int> g_exact_cols{2};  // bm_set_exact_sgemm_cols
 unsigned int *g_err_addr[kMaxDevices];
 std::once_flag g_err_once[kMaxDevices];
 }  // namespace
@@ -144,8 +146,9 @@ int product(const char *fn, const uint16_t *W, int64_t rows, int64_t k, const ui
     if (!current_device(&dev, &st)) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (bm_takes_sgemm(rows, k, ncols))
-        return ncols <= kSgemmStreamMaxCols ? launch_sgemm_stream(W, rows, k, X, ncols, Y, s, dev)
-                                            : launch_gemm_tc(W, rows, k, X, ncols, Y, s, dev);
+        return ncols <= g_exact_cols.load(std::memory_order_relaxed)
+                   ? launch_sgemm_stream(W, rows, k, X, ncols, Y, s, dev)
+                   : launch_gemm_tc(W, rows, k, X, ncols, Y, s, dev);
     VecdotJob job{};
     job.W[0] = W;
     job.y[0] = Y;
@@ -293,8 +296,9 @@ int bm_f16_matmul_noalloc(const uint16_t *W, int64_t rows, int64_t k, const uint
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     // the CUDA-core kernels use no scratch memory
     if (bm_takes_sgemm(rows, k, ncols))
-        return ncols <= kSgemmStreamMaxCols ? launch_sgemm_stream(W, rows, k, X, ncols, Y, s, dev)
-                                            : launch_gemm_tc_noalloc(W, rows, k, X, ncols, Y, s, dev);
+        return ncols <= g_exact_cols.load(std::memory_order_relaxed)
+                   ? launch_sgemm_stream(W, rows, k, X, ncols, Y, s, dev)
+                   : launch_gemm_tc_noalloc(W, rows, k, X, ncols, Y, s, dev);
     VecdotJob job{};
     job.W[0] = W;
     job.y[0] = Y;
@@ -317,6 +321,12 @@ int bm_set_pdl(int enable)
 {
     clear_error();
     return g_pdl.exchange(enable ? 1 : 0);
+}
+
+int bm_set_exact_sgemm_cols(int ncols)
+{
+    clear_error();
+    return g_exact_cols.exchange(std::max(0, std::min(ncols, kSgemmStreamMaxCols)));
 }
 
 int bm_device_status(bm_stream_t stream)

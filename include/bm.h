@@ -10,10 +10,11 @@
  *   - a product of two or more columns takes tinyBLAS's 8-lane chain when the
  *     weight has a multiple of 4 rows and the row a multiple of 8 elements, and
  *     falls back to vec_dot otherwise (sections "Summary", "Technical usage",
- *     "Design notes", bullet "sgemm_dot").  Here that tinyBLAS path gives
- *     tinyBLAS's bits for 2..8 columns (CUDA cores, the same chain order) and,
- *     for more columns, runs on tcgen05 tensor cores accurate to
- *     4e-6 * sum|w_i * a_i| of tinyBLAS's result; the fallback is bit-exact.
+ *     "Design notes", bullet "sgemm_dot").  Here that tinyBLAS path runs on
+ *     tcgen05 tensor cores accurate to 4e-6 * sum|w_i * a_i| of tinyBLAS's
+ *     result, or -- for products of up to bm_set_exact_sgemm_cols columns
+ *     (default 2) -- on a CUDA-core kernel that gives tinyBLAS's bits; the
+ *     fallback is bit-exact.
  *
  * Conventions shared by every call:
  *   - f16 values are passed as their IEEE binary16 bit patterns (uint16_t),
@@ -108,12 +109,12 @@ int bm_f16_matvec_act(int nmat, const uint16_t *const *W, const int64_t *rows, i
 /*
  * Y[c*rows + r] = W[r] . X[c] for every row r and column c
  * (f16.md, "Matrix products", mat_mul_par), with the path ggml takes:
- *   - bm_takes_sgemm(rows, k, ncols) and ncols <= 8: tinyBLAS's sgemm_dot per
- *     element, bit for bit (eight f32 lane chains, lane l taking elements 8t + l in
- *     increasing t, folded ((l0+l4)+(l2+l6))+((l1+l5)+(l3+l7)); "Design notes",
- *     "sgemm_dot");
- *   - bm_takes_sgemm(rows, k, ncols) and ncols > 8: tcgen05 tensor cores, f32
- *     accumulation, |Y - sgemm_dot(W[r], X[c])| <= 4e-6 * sum_i |W[r][i] * X[c][i]|;
+ *   - bm_takes_sgemm(rows, k, ncols): tcgen05 tensor cores, f32 accumulation,
+ *     |Y - sgemm_dot(W[r], X[c])| <= 4e-6 * sum_i |W[r][i] * X[c][i]|; except
+ *     that a product of at most bm_set_exact_sgemm_cols columns gives tinyBLAS's
+ *     sgemm_dot per element, bit for bit (eight f32 lane chains, lane l taking
+ *     elements 8t + l in increasing t, folded ((l0+l4)+(l2+l6))+((l1+l5)+(l3+l7));
+ *     "Design notes", "sgemm_dot");
  *   - otherwise: vec_dot per element, bit-exact (ncols == 1 is bm_f16_matvec).
  *   W : device, f16[rows][k].   X : device, f16[ncols][k].   Y : device, f32[ncols*rows].
  *   rows, ncols >= 0, 1 <= k <= BM_MAX_K.
@@ -167,7 +168,7 @@ int bm_takes_sgemm(int64_t rows, int64_t k, int64_t ncols);
 /*
  * Programmatic dependent launch for the products (default off; process-wide).
  * When on, a product of one column with k % 8 == 0, or a bm_takes_sgemm product
- * of up to 8 columns, is launched so that it may start before the kernel ahead
+ * on the bit-exact kernel (bm_set_exact_sgemm_cols), is launched so that it may start before the kernel ahead
  * of it on the stream has finished: it begins copying its weight matrix into
  * shared memory at once and waits for that kernel only before it reads its
  * activation and writes its output.  Precondition while on: the
@@ -176,6 +177,17 @@ int bm_takes_sgemm(int64_t rows, int64_t k, int64_t ncols);
  * are identical either way.  Returns the previous setting.
  */
 int bm_set_pdl(int enable);
+
+/*
+ * Bit-exact tinyBLAS products (process-wide; no counterpart on the pages: a choice
+ * between two implementations of the same contract).  A bm_takes_sgemm product of
+ * at most `ncols` columns runs on a CUDA-core kernel that keeps tinyBLAS's chain
+ * order and returns its bits; wider ones run on the tensor cores within the bound.
+ * `ncols` is clamped to 0..8 (0 or 1: always the tensor cores).  The default, 2, is
+ * where the exact kernel is as fast as the tensor cores on GB300; larger values buy
+ * tinyBLAS's bits at some speed.  Returns the previous setting.
+ */
+int bm_set_exact_sgemm_cols(int ncols);
 
 /* Waits for `stream`, then reads and clears this library's device error word
  * on the current device: BM_OK, BM_ERR_TIMEOUT (a kernel gave up a bounded

@@ -109,6 +109,15 @@ def test_matmul_host_checks(L):
         assert st(L, f, A, 2 ** 40, 64, A + 2 ** 20, 2 ** 30, A + 2 ** 21, None) == 1
 
 
+def test_exact_sgemm_cols_setting(L):
+    """bm_set_exact_sgemm_cols clamps to 0..8 and returns the previous value (host only)."""
+    old = L.bm_set_exact_sgemm_cols(5)
+    assert 0 <= old <= 8
+    assert L.bm_set_exact_sgemm_cols(100) == 5
+    assert L.bm_set_exact_sgemm_cols(-3) == 8
+    assert L.bm_set_exact_sgemm_cols(old) == 0
+
+
 def test_product_path_is_cuda_only():
     """The binding has no CPU fallback: it loads libbm.so or fails, and never imports the oracle."""
     import f16_weight_gemv_gb300 as bm

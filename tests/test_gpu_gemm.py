@@ -1,11 +1,12 @@
 """GPU parity of the takes_sgemm products against the oracle's tinyBLAS element:
 |Y - sgemm_dot| <= 4e-6 * sum_i |w_i * a_i| per element.
 
-The bound is the one the product's contract states for the tensor-core path (more
-than 8 columns); tinyBLAS's own result is one rounding order among many, so the
-tensor-core sum is compared to it within that bound rather than bit for bit.  The
-shapes of 2..8 columns run on the CUDA-core kernel, which gives tinyBLAS's bits
-(test_gpu_sgemm_exact.py checks them exactly); they must meet the bound here too."""
+The bound is the one the product's contract states for the tensor-core path;
+tinyBLAS's own result is one rounding order among many, so the tensor-core sum is
+compared to it within that bound rather than bit for bit.  Products of at most
+bm_set_exact_sgemm_cols columns (default 2) run on the CUDA-core kernel, which gives
+tinyBLAS's bits (test_gpu_sgemm_exact.py checks them exactly); they must meet the
+bound here too."""
 import numpy as np
 import pytest
 

@@ -1,5 +1,5 @@
 """GPU parity of the CUDA-core tinyBLAS kernel (bm_takes_sgemm shapes of 2..8
-columns) against the oracle, bit for bit.
+columns, with bm_set_exact_sgemm_cols(8)) against the oracle, bit for bit.
 
 Each output of these products is tinyBLAS's sgemm_dot (page f16.md, "Design
 notes", "sgemm_dot"): eight lane chains in increasing t, folded
@@ -19,6 +19,14 @@ from conftest import GOLDEN, bits32, to_dev
 pytestmark = pytest.mark.gpu
 
 MAX_STREAM_COLS = 8
+
+
+@pytest.fixture(autouse=True)
+def exact_up_to_eight(bm):
+    """Every takes_sgemm product of up to 8 columns on the bit-exact kernel."""
+    old = bm.bm_set_exact_sgemm_cols(MAX_STREAM_COLS)
+    yield
+    bm.bm_set_exact_sgemm_cols(old)
 
 
 def rnd_f16(tid, shape, sigma=0.02, seed=0):
