@@ -18,7 +18,7 @@ from . import _build
 
 __all__ = [
     "BmError", "lib", "bm_to_f16", "bm_f16_matvec", "bm_f16_matvec_multi", "bm_f16_matvec_act", "bm_f16_matmul", "bm_f16_matmul_noalloc",
-    "bm_f16_logits", "bm_takes_sgemm", "bm_device_status", "bm_status_string", "bm_last_error",
+    "bm_f16_logits", "bm_f16_get_rows", "bm_takes_sgemm", "bm_device_status", "bm_status_string", "bm_last_error",
     "bm_selftest_wait_timeout", "bm_set_pdl", "bm_set_exact_sgemm_cols", "EXPORTS", "BM_MAX_K",
 ]
 
@@ -35,6 +35,7 @@ EXPORTS = {
     "bm_f16_matmul": (_i, [_vp, _i64, _i64, _vp, _i64, _vp, _vp]),
     "bm_f16_logits": (_i, [_vp, _i64, _i64, _vp, _i64, _vp, _vp]),
     "bm_f16_matmul_noalloc": (_i, [_vp, _i64, _i64, _vp, _i64, _vp, _vp]),
+    "bm_f16_get_rows": (_i, [_vp, _i64, _i64, _vp, _i64, _vp, _vp]),
     "bm_takes_sgemm": (_i, [_i64, _i64, _i64]),
     "bm_device_status": (_i, [_vp]),
     "bm_set_pdl": (_i, [_i]),
@@ -208,6 +209,22 @@ def bm_f16_matmul_noalloc(W, X, Y, stream=None):
 def bm_f16_logits(E, X, Y=None, stream=None):
     """Logits over a tied embedding E [vocab][hidden]; Y[c][v]."""
     return _product("bm_f16_logits", E, X, Y, stream)
+
+
+def bm_f16_get_rows(E, ids, out=None, stream=None):
+    """out[i] = E[ids[i]] widened to f32 exactly; E [vocab][hidden] f16, ids int32 [n].
+    Ids out of range are reported by bm_device_status (their rows are left untouched)."""
+    vocab, hidden = _wk(E)
+    if ids.dtype != torch.int32 or ids.dim() != 1:
+        raise ValueError("ids must be a 1-D int32 tensor")
+    n = ids.numel()
+    if out is None:
+        out = torch.empty((n, hidden), dtype=torch.float32, device=E.device)
+    if out.numel() != n * hidden:
+        raise ValueError("out must have n*hidden elements")
+    _check(lib().bm_f16_get_rows(_dev(E, "E", _F16_LIKE), vocab, hidden, _dev(ids, "ids", (torch.int32,)), n,
+                                 _dev(out, "out", (torch.float32,)), _stream(stream)), "bm_f16_get_rows")
+    return out
 
 
 def bm_device_status(stream=None) -> int:

@@ -5,6 +5,7 @@
 #include "bm_internal.h"
 
 #include <cstdarg>
+#include <cstdint>
 #include <cstdio>
 #include <cstring>
 #include <algorithm>
@@ -63,6 +64,7 @@ int read_device_error(cudaStream_t s)
     e = cudaMemcpy(&v, w, sizeof v, cudaMemcpyDeviceToHost);
     if (e == cudaSuccess) e = cudaMemcpy(w, &zero, sizeof zero, cudaMemcpyHostToDevice);
     if (e != cudaSuccess) return fail(BM_ERR_CUDA, "reading the device error word failed: %s", cudaGetErrorString(e));
+    if (v == BM_ERR_INVALID_ARG) return fail((int)v, "a kernel met an invalid argument on the device (an id out of range)");
     if (v != 0) return fail((int)v, "a kernel gave up a bounded wait");
     return BM_OK;
 }
@@ -163,6 +165,27 @@ int product(const char *fn, const uint16_t *W, int64_t rows, int64_t k, const ui
 }  // namespace
 
 extern "C" {
+
+int bm_f16_get_rows(const uint16_t *E, int64_t vocab, int64_t hidden, const int32_t *ids, int64_t n, float *out,
+                    bm_stream_t stream)
+{
+    clear_error();
+    if (n < 0 || vocab < 0 || hidden < 0) return fail(BM_ERR_INVALID_ARG, "bm_f16_get_rows: negative size");
+    if (n == 0) return BM_OK;
+    if (vocab < 1 || hidden < 1) return fail(BM_ERR_INVALID_ARG, "bm_f16_get_rows: empty table");
+    if (vocab > INT32_MAX || hidden > INT64_MAX / 8 / vocab || n > INT64_MAX / 8 / hidden)
+        return fail(BM_ERR_INVALID_ARG, "bm_f16_get_rows: sizes overflow");
+    if (!E || !ids || !out) return fail(BM_ERR_INVALID_ARG, "bm_f16_get_rows: null pointer");
+    if (!aligned(E, 16) || !aligned(ids, 16))
+        return fail(BM_ERR_ALIGNMENT, "bm_f16_get_rows: the table and the ids must be 16-byte aligned");
+    if (!aligned(out, 4)) return fail(BM_ERR_ALIGNMENT, "bm_f16_get_rows: the output must be 4-byte aligned");
+    if (overlap(out, n * hidden * 4, E, vocab * hidden * 2) || overlap(out, n * hidden * 4, ids, n * 4))
+        return fail(BM_ERR_INVALID_ARG, "bm_f16_get_rows: the output overlaps an input");
+    DeviceInfo dev;
+    int st = BM_OK;
+    if (!current_device(&dev, &st)) return st;
+    return launch_get_rows(E, vocab, hidden, ids, n, out, reinterpret_cast<cudaStream_t>(stream), dev);
+}
 
 int bm_takes_sgemm(int64_t rows, int64_t k, int64_t ncols)
 {

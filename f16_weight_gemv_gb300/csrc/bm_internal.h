@@ -69,6 +69,9 @@ int launch_gemm_tc_noalloc(const uint16_t *W, int64_t rows, int64_t k, const uin
 // fills its only stage, so the MMA issuer gives up after `timeout_ns`.
 int launch_gemm_tc_withheld(const uint16_t *W, int64_t rows, int64_t k, const uint16_t *X, int64_t ncols,
                             float *Y, cudaStream_t s, const DeviceInfo &dev, unsigned long long timeout_ns);
+// Rows of an f16 table widened to f32 (ids checked on the device).
+int launch_get_rows(const uint16_t *E, int64_t vocab, int64_t hidden, const int32_t *ids, int64_t n, float *out,
+                    cudaStream_t s, const DeviceInfo &dev);
 // Waits for `s` and reads/clears the device error word of the tensor-core kernels.
 int read_device_error(cudaStream_t s);
 

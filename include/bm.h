@@ -161,6 +161,18 @@ int bm_f16_matmul_noalloc(const uint16_t *W, int64_t rows, int64_t k, const uint
 int bm_f16_logits(const uint16_t *E, int64_t vocab, int64_t hidden, const uint16_t *X,
                   int64_t ncols, float *Y, bm_stream_t stream);
 
+/*
+ * Rows of an f16 table widened to f32, exactly: the token-embedding lookup
+ * (f16.md, "Technical usage", dequantize_row -- F16 bytes widened to f32, as
+ * get_rows does; widen is exact).  out[i*hidden + j] = (float) E[ids[i]*hidden + j].
+ *   E : device, f16[vocab][hidden].   ids : device, int32[n].
+ *   out : device, f32[n][hidden] (16-byte aligned output takes the fast path).
+ *   vocab, hidden >= 1 unless n == 0; n >= 0.  An id outside [0, vocab) leaves its
+ *   output row untouched and makes bm_device_status return BM_ERR_INVALID_ARG.
+ */
+int bm_f16_get_rows(const uint16_t *E, int64_t vocab, int64_t hidden, const int32_t *ids, int64_t n,
+                    float *out, bm_stream_t stream);
+
 /* ggml's path selector (f16.md, "Technical usage"): 1 when
  * ncols >= 2 && rows % 4 == 0 && k % 8 == 0, else 0.  Pure; never fails. */
 int bm_takes_sgemm(int64_t rows, int64_t k, int64_t ncols);
@@ -191,7 +203,8 @@ int bm_set_exact_sgemm_cols(int ncols);
 
 /* Waits for `stream`, then reads and clears this library's device error word
  * on the current device: BM_OK, BM_ERR_TIMEOUT (a kernel gave up a bounded
- * wait and wrote nothing trustworthy), or BM_ERR_CUDA (the wait failed). */
+ * wait and wrote nothing trustworthy), BM_ERR_INVALID_ARG (bm_f16_get_rows met
+ * an id out of range), or BM_ERR_CUDA (the wait failed). */
 int bm_device_status(bm_stream_t stream);
 
 /* Self-test of the bounded device waits (no counterpart on the pages; it

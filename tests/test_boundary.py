@@ -109,6 +109,18 @@ def test_matmul_host_checks(L):
         assert st(L, f, A, 2 ** 40, 64, A + 2 ** 20, 2 ** 30, A + 2 ** 21, None) == 1
 
 
+def test_get_rows_host_checks(L):
+    f = L.bm_f16_get_rows
+    assert f(A, 16, 64, A + 2 ** 20, 0, A + 2 ** 21, None) == 0                 # n = 0: nothing to do
+    assert f(A, 16, 64, A + 2 ** 20, -1, A + 2 ** 21, None) == 1
+    assert f(A, 0, 64, A + 2 ** 20, 3, A + 2 ** 21, None) == 1                  # empty table
+    assert f(None, 16, 64, A + 2 ** 20, 3, A + 2 ** 21, None) == 1
+    assert f(A + 2, 16, 64, A + 2 ** 20, 3, A + 2 ** 21, None) == 2             # table misaligned
+    assert f(A, 16, 64, A + 2 ** 20 + 4, 3, A + 2 ** 21, None) == 2             # ids misaligned
+    assert f(A, 16, 64, A + 2 ** 20, 3, A + 2 ** 21 + 2, None) == 2             # output misaligned
+    assert f(A, 16, 64, A + 2 ** 20, 3, A + 64, None) == 1                      # output overlaps the table
+
+
 def test_exact_sgemm_cols_setting(L):
     """bm_set_exact_sgemm_cols clamps to 0..8 and returns the previous value (host only)."""
     old = L.bm_set_exact_sgemm_cols(5)
