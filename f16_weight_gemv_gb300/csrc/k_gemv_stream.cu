@@ -153,8 +153,10 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv_stream(const __grid_consta
     const int k = job.k;
     const int S = job.stages;
     const uint32_t xbytes = (uint32_t)((2 * k + 1023) / 1024 * 1024);
-    // 1024-byte alignment: the swizzle pattern of the TMA boxes repeats every 1024 bytes
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // 1024-byte alignment: the swizzle pattern of the TMA boxes repeats every 1024 bytes.
+    // (Offsetting the __shared__ array itself keeps the pointer in the shared window, so
+    // the reads below compile to shared-memory loads, not generic ones.)
+    uint8_t *smem = smem_raw + ((1024u - (dev::smem_u32(smem_raw) & 1023u)) & 1023u);
     uint16_t *xs = reinterpret_cast<uint16_t *>(smem);  // the f16 activation
     const uint32_t ring_u = dev::smem_u32(smem) + xbytes;
     volatile int *abort_v = &abort_flag;
