@@ -8,24 +8,28 @@
 // tinyBLAS's bit pattern; it is within 4e-6 * sum_i |W[r][i] * X[c][i]| of it.
 //
 // Persistent, warp-specialised kernel (cta_group::1, one CTA per SM):
-//   warp 0, one lane : TMA producer.  For each k-block a W tile (128 rows x 64)
-//                      and an X tile (BN columns x 64), K-major with the
+//   warp 0, one lane : TMA producer.  For each k-block a W tile (128 * MT rows x
+//                      64) and an X tile (BN columns x 64), K-major with the
 //                      128-byte swizzle, into a ring of shared-memory stages.
-//   warp 1, one lane : MMA issuer.  Four tcgen05.mma (K = 16) per k-block into
-//                      one of two TMEM accumulators; tcgen05.commit frees the
-//                      stage, and after a unit's last k-block signals the
-//                      epilogue.  Warp 1 also owns the TMEM allocation.
+//   warp 1, one lane : MMA issuer.  4 * MT tcgen05.mma (M = 128, K = 16) per
+//                      k-block into the unit's MT accumulators; tcgen05.commit
+//                      frees the stage, and after a unit's last k-block signals
+//                      the epilogue.  Warp 1 also owns the TMEM allocation.
 //   warps 2..5       : epilogue.  tcgen05.ld (32 lanes x 32 columns per trip)
 //                      then coalesced f32 stores: a column of a tile is a
-//                      contiguous run of rows in Y.  The accumulator is handed
-//                      back to the MMA warp as soon as it has been read, so the
-//                      epilogue of one unit overlaps the MMAs of the next.
-// Work units are (row tile, column tile, k-split).  With S > 1 splits each unit
-// writes its partial tile to a workspace, and for every 32-row quarter of the
-// tile the last of the S units to finish (an atomic counter per quarter) sums
-// the S partials in split order 0..S-1 and writes Y -- so the result does not
-// depend on which unit finishes last.  The split count comes from a cost model
-// of waves x (k-blocks per unit + partial traffic).
+//                      contiguous run of rows in Y.  The accumulators are handed
+//                      back to the MMA warp as soon as they have been read; when
+//                      TMEM holds two sets (MT * BN <= 256) the epilogue of one
+//                      unit overlaps the MMAs of the next.
+// Work units are (row unit of MT tiles of 128 rows, column tile, k-split).  MT = 2
+// lets two MMAs share each X tile, so a k-block moves 64 KB of operands for the
+// work that takes 96 KB with MT = 1 -- the operand feed, not the tensor pipe, is
+// what limits this kernel (the MMA sequence alone runs at full rate).  With S > 1
+// splits each unit writes its partial tiles to a workspace, and for every 32-row
+// quarter of a 128-row tile the last of the S units to finish (an atomic counter
+// per quarter) sums the S partials in split order 0..S-1 and writes Y -- so the
+// result does not depend on which unit finishes last.  MT and S come from a model
+// of the predicted time (waves x per-unit time, fitted to measurements).
 //
 // Out-of-range rows, columns and the k % 64 end are zero-filled by TMA and add
 // +0 exactly.  Every mbarrier wait is bounded by the global timer; on a
@@ -65,7 +69,9 @@ struct GemmParams {
     int num_kb;               // ceil(k / 64)
     int bn;                   // tile columns (MMA N), multiple of 16, <= 256
     int bn_alloc;             // TMEM columns per accumulator: power of two >= max(32, bn)
-    int mt, nt;               // row tiles, column tiles
+    int mt, nt;               // row tiles (128 rows), column tiles
+    int mtu;                  // row units: MT row tiles each (one work unit's rows)
+    int nbuf;                 // TMEM accumulator sets: 2 (double-buffered) or 1
     int splits;
     int stages;
     unsigned long long timeout_ns;
@@ -147,26 +153,36 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32])
 }
 
 struct Unit {
-    int m0, n0, s, tile, kb0, kb1;
+    int m0;     // first row of the unit: MT row tiles of 128 rows
+    int n0, s, kb0, kb1;
+    int tile0;  // split-k bookkeeping index of the unit's first row tile (row tile t: tile0 + t * nt)
 };
 
-// Units are ordered column tile fastest, then split, then row tile: CTAs that
-// run side by side share a W block (the column tiles) through L2.
+// Units are (row unit, column tile, k-split), ordered column tile fastest, then split,
+// then row unit: CTAs that run side by side share a W block (the column tiles)
+// through L2.
+template <int MT>
 __device__ __forceinline__ Unit unit_of(const GemmParams &p, int u)
 {
     Unit x;
     const int nt = u % p.nt;
     const int rest = u / p.nt;
     x.s = rest % p.splits;
-    const int mt = rest / p.splits;
-    x.m0 = mt * kBM;
+    const int mu = rest / p.splits;
+    x.m0 = mu * MT * kBM;
     x.n0 = nt * p.bn;
-    x.tile = mt * p.nt + nt;
+    x.tile0 = mu * MT * p.nt + nt;
     x.kb0 = (int)((int64_t)p.num_kb * x.s / p.splits);
     x.kb1 = (int)((int64_t)p.num_kb * (x.s + 1) / p.splits);
     return x;
 }
 
+// MT = 1: a unit is 128 rows x BN columns.  MT = 2: 256 rows x BN columns, two
+// M = 128 MMAs per k-step sharing the X tile, so each k-block moves 64 KB of operands
+// for twice the work (32 KB per 128 x 256 x 64 block instead of 48 KB).  The
+// accumulators of a unit take MT * BN TMEM columns; with room for two sets
+// (p.nbuf == 2) the epilogue of one unit overlaps the MMAs of the next.
+template <int MT>
 __global__ void __launch_bounds__(kThreads, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_x,
               const GemmParams p)
@@ -183,18 +199,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // 1024-byte alignment of the stage ring (the swizzle pattern repeats every 1024 bytes)
-    uint8_t *ring = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const uint32_t ring_u32 = smem_u32(ring);
-    const uint32_t stage_bytes = kTileABytes + (uint32_t)p.bn * kBK * 2;
+    const uint32_t ring_u32 = (smem_u32(smem_raw) + 1023u) & ~1023u;
+    const uint32_t stage_bytes = MT * kTileABytes + (uint32_t)p.bn * kBK * 2;
+    const uint32_t tmem_cols = (uint32_t)(p.nbuf * MT * p.bn_alloc);
     volatile int *abort_v = &abort_flag;
-    const int units = p.mt * p.nt * p.splits;
+    const int units = p.mtu * p.nt * p.splits;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.stages; s++) {
             mbar_init(smem_u32(&full_bar[s]), 1);
             mbar_init(smem_u32(&empty_bar[s]), 1);
         }
-        for (int b = 0; b < 2; b++) {
+        for (int b = 0; b < p.nbuf; b++) {
             mbar_init(smem_u32(&acc_full[b]), 1);
             mbar_init(smem_u32(&acc_empty[b]), kEpiWarps);
         }
@@ -206,7 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          smem_u32(&tmem_base_slot)),
-                     "r"(2 * p.bn_alloc)
+                     "r"(tmem_cols)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
@@ -221,7 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int t = 0;
             bool ok = true;
             for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-                const Unit x = unit_of(p, u);
+                const Unit x = unit_of<MT>(p, u);
                 for (int kb = x.kb0; kb < x.kb1; kb++, t++) {
                     const int s = t % p.stages;
                     const uint32_t ph = (uint32_t)(t / p.stages) & 1u;
@@ -233,8 +249,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t a_dst = ring_u32 + (uint32_t)s * stage_bytes;
                     const uint32_t fb = smem_u32(&full_bar[s]);
                     mbar_expect_tx(fb, stage_bytes);
-                    tma_load_2d(a_dst, &map_w, kb * kBK, x.m0, fb);
-                    tma_load_2d(a_dst + kTileABytes, &map_x, kb * kBK, x.n0, fb);
+                    tma_load_2d(a_dst, &map_w, kb * kBK, x.m0, fb);  // MT * 128 rows in one box
+                    tma_load_2d(a_dst + MT * kTileABytes, &map_x, kb * kBK, x.n0, fb);
                     issued_slot = t + 1;
                 }
             }
@@ -247,13 +263,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             int t = 0, i = 0;
             bool ok = true;
             for (int u = blockIdx.x; u < units && ok; u += gridDim.x, i++) {
-                const Unit x = unit_of(p, u);
-                const int b = i & 1;
-                if (!dev::mbar_wait(smem_u32(&acc_empty[b]), (((uint32_t)i >> 1) & 1u) ^ 1u, abort_v, p.timeout_ns,
-                                    p.err))
-                    break;
+                const Unit x = unit_of<MT>(p, u);
+                const int b = i % p.nbuf;
+                const uint32_t use = (uint32_t)(i / p.nbuf);  // how many times set b was used before
+                if (!dev::mbar_wait(smem_u32(&acc_empty[b]), (use & 1u) ^ 1u, abort_v, p.timeout_ns, p.err)) break;
                 tc_fence_after();
-                const uint32_t d = tmem_base + (uint32_t)(b * p.bn_alloc);
+                const uint32_t d = tmem_base + (uint32_t)(b * MT * p.bn_alloc);
                 for (int kb = x.kb0; kb < x.kb1; kb++, t++) {
                     const int s = t % p.stages;
                     const uint32_t ph = (uint32_t)(t / p.stages) & 1u;
@@ -263,15 +278,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tc_fence_after();
                     const uint32_t a_addr = ring_u32 + (uint32_t)s * stage_bytes;
-                    const uint32_t b_addr = a_addr + kTileABytes;
+                    const uint32_t b_addr = a_addr + MT * kTileABytes;
 #pragma unroll
                     for (int kk = 0; kk < kBK / kUmmaK; kk++)
-                        mma_f16(d, smem_desc_sw128(a_addr + kk * kUmmaK * 2), smem_desc_sw128(b_addr + kk * kUmmaK * 2),
-                                idesc, (kb > x.kb0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+                        for (int m = 0; m < MT; m++)
+                            mma_f16(d + (uint32_t)(m * p.bn_alloc), smem_desc_sw128(a_addr + m * kTileABytes + kk * kUmmaK * 2),
+                                    smem_desc_sw128(b_addr + kk * kUmmaK * 2), idesc, (kb > x.kb0 || kk > 0) ? 1u : 0u);
                     mma_commit(smem_u32(&empty_bar[s]));  // the stage is free once these MMAs have read it
                 }
                 if (!ok) break;
-                mma_commit(smem_u32(&acc_full[b]));  // the accumulator is complete
+                mma_commit(smem_u32(&acc_full[b]));  // the accumulators are complete
             }
             mma_commit(smem_u32(&done_bar));  // always: completes when every issued MMA has finished
         }
@@ -279,47 +296,54 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ---------------------------------------------------------------- epilogue
         const int quarter = warp & 3;                 // TMEM lanes 32*quarter .. +31 (warp % 4 rule)
-        const int rloc = quarter * 32 + lane;         // row inside the tile
+        const int rloc = quarter * 32 + lane;         // row inside a 128-row tile
         int i = 0;
         for (int u = blockIdx.x; u < units; u += gridDim.x, i++) {
-            const Unit x = unit_of(p, u);
-            const int b = i & 1;
-            if (!dev::mbar_wait_warp(smem_u32(&acc_full[b]), ((uint32_t)i >> 1) & 1u, abort_v, p.timeout_ns, p.err))
-                break;
+            const Unit x = unit_of<MT>(p, u);
+            const int b = i % p.nbuf;
+            const uint32_t use = (uint32_t)(i / p.nbuf);
+            if (!dev::mbar_wait_warp(smem_u32(&acc_full[b]), use & 1u, abort_v, p.timeout_ns, p.err)) break;
             tc_fence_after();
-            const uint32_t taddr = tmem_base + (uint32_t)(b * p.bn_alloc) + ((uint32_t)(quarter * 32) << 16);
-            const int row = x.m0 + rloc;
-            float *ws_unit = p.splits > 1 ? p.ws + ((size_t)x.tile * p.splits + x.s) * (size_t)p.bn * kBM : nullptr;
-            for (int c = 0; c < p.bn; c += 32) {
-                uint32_t v[32];
-                tmem_ld32(taddr + (uint32_t)c, v);
-                if (p.splits > 1) {
+            for (int m = 0; m < MT; m++) {
+                const uint32_t taddr =
+                    tmem_base + (uint32_t)((b * MT + m) * p.bn_alloc) + ((uint32_t)(quarter * 32) << 16);
+                const int row = x.m0 + m * kBM + rloc;
+                const int tile = x.tile0 + m * p.nt;
+                float *ws_unit = p.splits > 1 ? p.ws + ((size_t)tile * p.splits + x.s) * (size_t)p.bn * kBM : nullptr;
+                for (int c = 0; c < p.bn; c += 32) {
+                    uint32_t v[32];
+                    tmem_ld32(taddr + (uint32_t)c, v);
+                    if (p.splits > 1) {
 #pragma unroll
-                    for (int q = 0; q < 32; q++)
-                        if (c + q < p.bn) ws_unit[(size_t)(c + q) * kBM + rloc] = __uint_as_float(v[q]);
-                } else if (row < p.rows) {
+                        for (int q = 0; q < 32; q++)
+                            if (c + q < p.bn) ws_unit[(size_t)(c + q) * kBM + rloc] = __uint_as_float(v[q]);
+                    } else if (row < p.rows) {
 #pragma unroll
-                    for (int q = 0; q < 32; q++) {
-                        const int col = x.n0 + c + q;
-                        if (c + q < p.bn && col < p.ncols) p.Y[(size_t)col * p.rows + row] = __uint_as_float(v[q]);
+                        for (int q = 0; q < 32; q++) {
+                            const int col = x.n0 + c + q;
+                            if (c + q < p.bn && col < p.ncols) p.Y[(size_t)col * p.rows + row] = __uint_as_float(v[q]);
+                        }
                     }
                 }
             }
-            // hand the accumulator back to the MMA warp
+            // hand the accumulators back to the MMA warp
             tc_fence_before();
             __syncwarp();
             if (lane == 0) dev::mbar_arrive(smem_u32(&acc_empty[b]));
 
             if (p.splits > 1) {
-                // the last of the S units of this tile quarter sums the partials in split order
+                // the last of the S units of each tile quarter sums the partials in split order
                 __threadfence();
                 __syncwarp();
-                unsigned old = 0;
-                if (lane == 0) old = atomicAdd(&p.counters[x.tile * 4 + quarter], 1u);
-                old = __shfl_sync(0xffffffffu, old, 0);
-                if (old == (unsigned)(p.splits - 1)) {
+                for (int m = 0; m < MT; m++) {
+                    const int row = x.m0 + m * kBM + rloc;
+                    const int tile = x.tile0 + m * p.nt;
+                    unsigned old = 0;
+                    if (lane == 0) old = atomicAdd(&p.counters[tile * 4 + quarter], 1u);
+                    old = __shfl_sync(0xffffffffu, old, 0);
+                    if (old != (unsigned)(p.splits - 1)) continue;
                     __threadfence();
-                    const float *ws_row = p.ws + (size_t)x.tile * p.splits * (size_t)p.bn * kBM + rloc;
+                    const float *ws_row = p.ws + (size_t)tile * p.splits * (size_t)p.bn * kBM + rloc;
                     if (row < p.rows) {
                         // 32 columns per trip, all of a split's loads in flight at once;
                         // the sum starts from split 0 and adds the others in order
@@ -343,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             }
                         }
                     }
-                    if (lane == 0) p.counters[x.tile * 4 + quarter] = 0;  // ready for the next launch
+                    if (lane == 0) p.counters[tile * 4 + quarter] = 0;  // ready for the next launch
                 }
             }
         }
@@ -367,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(2 * p.bn_alloc)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(tmem_cols)
                      : "memory");
     }
 }
@@ -410,30 +434,22 @@ int pow2_at_least(int v)
     return p;
 }
 
-// Split count minimising waves x (k-blocks per unit + the cost of splitting, counted
-// in k-blocks).  Splitting costs the partial tile's write and ordered re-read, the
-// serial reduction by the last unit of each tile and the counter reset: measured on
-// the Llama shapes at 512 columns (gate: 2 waves unsplit beat 3 waves of half-k units
-// by 20 %; down: one wave of half-k units beat 42 % of the SMs unsplit by 28 %), about
-// 8 + 30 * BN/256 k-blocks.
-int choose_splits(int tiles, int num_kb, int bn, int ctas)
+// Predicted time (us) of a plan on this GPU, fitted to this kernel's measured times
+// on the Llama shapes at 512 columns: a k-block costs about 0.003125 us per KB of
+// operands it moves plus 0.3 us per 128 x 256 x 64 block of MMA work (so 0.45 us for a
+// 128-row unit, 0.80 us for a 256-row one); a k-split costs the partial tiles' write
+// and ordered re-read, the serial reduction of the last unit and the counter reset,
+// about (8 + 30 * MT * BN / 256) k-blocks of 0.45 us.
+double plan_cost(int64_t tiles, int num_kb, int bn, int mt, int s, int ctas)
 {
-    const double partial = 8.0 + 30.0 * bn / 256.0;
-    int best = 1;
-    double best_cost = 1e300;
-    for (int s = 1; s <= kMaxSplits && s <= num_kb; s++) {
-        const double waves = std::ceil((double)tiles * s / ctas);
-        const double cost = waves * ((double)num_kb / s + (s > 1 ? partial : 0.0));
-        if (cost < best_cost - 1e-9) {
-            best_cost = cost;
-            best = s;
-        }
-    }
-    return best;
+    const double kblock = 0.003125 * (16.0 * mt + bn / 8.0) + 0.3 * mt * bn / 256.0;
+    const double split = (8.0 + 30.0 * mt * bn / 256.0) * 0.45;
+    const double waves = std::ceil((double)tiles * s / ctas);
+    return waves * ((double)num_kb / s * kblock + (s > 1 ? split : 0.0));
 }
 
 constexpr int kMaxDevices = 64;
-std::once_flag g_attr_once[kMaxDevices];
+std::once_flag g_attr_once[kMaxDevices][2];
 std::once_flag g_pool_once[kMaxDevices];
 cudaMemPool_t g_pool[kMaxDevices];
 
@@ -459,12 +475,14 @@ cudaMemPool_t workspace_pool(int dev_id)
 
 struct Plan {
     GemmParams p;
+    int mt_per_unit;  // MT: 128-row tiles per work unit (1 or 2)
     int grid;
     size_t smem;
     size_t ws_bytes, counter_bytes;
 };
 
-int plan_gemm(Plan *pl, int64_t rows, int64_t k, int64_t ncols, const DeviceInfo &dev, bool allow_split)
+int plan_gemm(Plan *pl, int64_t rows, int64_t k, int64_t ncols, const DeviceInfo &dev, bool allow_split,
+              bool allow_mt2)
 {
     if (rows > 0x7fffffffLL || ncols > 0x7fffffffLL || k > 0x7fffffffLL)
         return fail(BM_ERR_INVALID_ARG, "tensor-core product: rows, k and ncols must be below 2^31");
@@ -479,22 +497,58 @@ int plan_gemm(Plan *pl, int64_t rows, int64_t k, int64_t ncols, const DeviceInfo
     p.bn_alloc = pow2_at_least(p.bn);
     p.mt = (int)((rows + kBM - 1) / kBM);
     p.nt = (int)((ncols + p.bn - 1) / p.bn);
-    const int64_t tiles = (int64_t)p.mt * p.nt;
-    if (tiles * kMaxSplits > 0x7fffffffLL) return fail(BM_ERR_INVALID_ARG, "tensor-core product: too many tiles");
-    p.splits = allow_split ? choose_splits((int)tiles, p.num_kb, p.bn, dev.sm_count) : 1;
-    const int stage_bytes = kTileABytes + p.bn * kBK * 2;
+    if ((int64_t)p.mt * p.nt * kMaxSplits > 0x7fffffffLL)
+        return fail(BM_ERR_INVALID_ARG, "tensor-core product: too many tiles");
+    // Row tiles per unit (MT) and k-splits with the least predicted time.  256-row units
+    // (two MMAs sharing the X tile: fewer operand bytes per unit of work) are taken only
+    // with full 256-column tiles, where they were measured.
+    int mt_unit = 1, splits = 1;
+    double best = 1e300;
+    for (int mt = 1; mt <= (allow_mt2 && p.mt >= 2 && p.bn == 256 ? 2 : 1); mt++) {
+        const int64_t tiles = (int64_t)((p.mt + mt - 1) / mt) * p.nt;
+        for (int sp = 1; sp <= (allow_split ? std::min(kMaxSplits, p.num_kb) : 1); sp++) {
+            const double c = plan_cost(tiles, p.num_kb, p.bn, mt, sp, dev.sm_count);
+            if (c < best - 1e-9) {
+                best = c;
+                mt_unit = mt;
+                splits = sp;
+            }
+        }
+    }
+    pl->mt_per_unit = mt_unit;
+    p.mtu = (p.mt + mt_unit - 1) / mt_unit;
+    p.nbuf = 2 * mt_unit * p.bn_alloc <= 512 ? 2 : 1;  // TMEM holds 512 columns
+    const int64_t tiles = (int64_t)p.mtu * p.nt;       // work tiles of 128 * MT rows
+    p.splits = splits;
+    const int stage_bytes = mt_unit * kTileABytes + p.bn * kBK * 2;
     const int budget = dev.max_smem_optin - 1024 - 1024;  // alignment slack and static shared memory
     p.stages = std::min(kMaxStages, budget / stage_bytes);
     if (p.stages < 2) return fail(BM_ERR_CUDA, "tensor-core product: not enough shared memory");
     const int64_t units = tiles * p.splits;
     pl->grid = (int)std::min<int64_t>(units, dev.sm_count);
     // One CTA per SM (this request is more than half of the SM's shared memory), so the
-    // two accumulators of up to 256 columns each never exceed the SM's 512 TMEM columns.
+    // accumulators (up to 512 columns) never exceed the SM's TMEM.
     const size_t smem = (size_t)p.stages * stage_bytes + 1024;
     const size_t one_per_sm = (size_t)dev.max_smem_optin / 2 + 4096;
     pl->smem = std::max(smem, one_per_sm);
-    pl->ws_bytes = p.splits > 1 ? (size_t)tiles * p.splits * p.bn * kBM * sizeof(float) : 0;
-    pl->counter_bytes = p.splits > 1 ? (size_t)tiles * 4 * sizeof(unsigned int) : 0;
+    // split-k bookkeeping is per 128-row tile
+    const size_t tiles128 = (size_t)tiles * mt_unit;
+    pl->ws_bytes = p.splits > 1 ? tiles128 * p.splits * p.bn * kBM * sizeof(float) : 0;
+    pl->counter_bytes = p.splits > 1 ? tiles128 * 4 * sizeof(unsigned int) : 0;
+    return BM_OK;
+}
+
+template <int MT>
+int launch_mt(const Plan &pl, const CUtensorMap &mw, const CUtensorMap &mx, cudaStream_t s, const DeviceInfo &dev)
+{
+    int dev_id = 0;
+    cudaGetDevice(&dev_id);
+    std::call_once(g_attr_once[dev_id & (kMaxDevices - 1)][MT - 1], [&] {
+        cudaFuncSetAttribute(k_gemm_tc<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, dev.max_smem_optin - 1024);
+    });
+    k_gemm_tc<MT><<<pl.grid, kThreads, pl.smem, s>>>(mw, mx, pl.p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(BM_ERR_CUDA, "tensor-core product: launch failed: %s", cudaGetErrorString(e));
     return BM_OK;
 }
 
@@ -502,17 +556,9 @@ int launch_plan(const Plan &pl, const uint16_t *W, const uint16_t *X, cudaStream
 {
     if (!get_encoder()) return fail(BM_ERR_CUDA, "tensor-core product: cuTensorMapEncodeTiled unavailable");
     CUtensorMap mw, mx;
-    if (!make_map(&mw, W, pl.p.rows, pl.p.k, kBM) || !make_map(&mx, X, pl.p.ncols, pl.p.k, pl.p.bn))
+    if (!make_map(&mw, W, pl.p.rows, pl.p.k, kBM * pl.mt_per_unit) || !make_map(&mx, X, pl.p.ncols, pl.p.k, pl.p.bn))
         return fail(BM_ERR_CUDA, "tensor-core product: tensor map encoding failed");
-    int dev_id = 0;
-    cudaGetDevice(&dev_id);
-    std::call_once(g_attr_once[dev_id & (kMaxDevices - 1)], [&] {
-        cudaFuncSetAttribute(k_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, dev.max_smem_optin - 1024);
-    });
-    k_gemm_tc<<<pl.grid, kThreads, pl.smem, s>>>(mw, mx, pl.p);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return fail(BM_ERR_CUDA, "tensor-core product: launch failed: %s", cudaGetErrorString(e));
-    return BM_OK;
+    return pl.mt_per_unit == 2 ? launch_mt<2>(pl, mw, mx, s, dev) : launch_mt<1>(pl, mw, mx, s, dev);
 }
 
 }  // namespace
@@ -523,7 +569,7 @@ int launch_gemm_tc(const uint16_t *W, int64_t rows, int64_t k, const uint16_t *X
     unsigned int *err = device_error_word();
     if (!err) return fail(BM_ERR_CUDA, "tensor-core product: device error word unavailable");
     Plan pl;
-    int st = plan_gemm(&pl, rows, k, ncols, dev, true);
+    int st = plan_gemm(&pl, rows, k, ncols, dev, true, true);
     if (st != BM_OK) return st;
     pl.p.Y = Y;
     pl.p.err = err;
@@ -574,7 +620,7 @@ int launch_gemm_tc_noalloc(const uint16_t *W, int64_t rows, int64_t k, const uin
     unsigned int *err = device_error_word();
     if (!err) return fail(BM_ERR_CUDA, "no-allocation product: device error word unavailable");
     Plan pl;
-    int st = plan_gemm(&pl, rows, k, ncols, dev, true);
+    int st = plan_gemm(&pl, rows, k, ncols, dev, true, true);
     if (st != BM_OK) return st;
     const size_t need = pl.ws_bytes + pl.counter_bytes;
     if (need > kNoAllocScratchBytes)
@@ -616,7 +662,7 @@ int launch_gemm_tc_withheld(const uint16_t *W, int64_t rows, int64_t k, const ui
     unsigned int *err = device_error_word();
     if (!err) return fail(BM_ERR_CUDA, "tensor-core product: device error word unavailable");
     Plan pl;
-    int st = plan_gemm(&pl, rows, k, ncols, dev, false);
+    int st = plan_gemm(&pl, rows, k, ncols, dev, false, false);
     if (st != BM_OK) return st;
     pl.p.Y = Y;
     pl.p.err = err;
