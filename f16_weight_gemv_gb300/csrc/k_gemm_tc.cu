@@ -29,7 +29,7 @@
 // quarter of a 128-row tile the last of the S units to finish (an atomic counter
 // per quarter) sums the S partials in split order 0..S-1 and writes Y -- so the
 // result does not depend on which unit finishes last.  MT and S come from a model
-// of the predicted time (waves x per-unit time, fitted to measurements).
+// of the predicted time (waves x per-unit time, calibrated by measurements).
 //
 // Out-of-range rows, columns and the k % 64 end are zero-filled by TMA and add
 // +0 exactly.  Every mbarrier wait is bounded by the global timer; on a
@@ -434,19 +434,23 @@ int pow2_at_least(int v)
     return p;
 }
 
-// Predicted time (us) of a plan on this GPU, fitted to this kernel's measured times
-// on the Llama shapes at 512 columns: a k-block costs about 0.003125 us per KB of
-// operands it moves plus 0.3 us per 128 x 256 x 64 block of MMA work (so 0.45 us for a
-// 128-row unit, 0.80 us for a 256-row one); a k-split costs the partial tiles' write
-// and ordered re-read, the serial reduction of the last unit and the counter reset,
-// about (8 + 30 * MT * BN / 256) k-blocks of 0.45 us.
-double plan_cost(int64_t tiles, int num_kb, int bn, int mt, int s, int ctas)
+// Cost of a plan in k-blocks of its own unit height: waves x (k-blocks per unit + the
+// cost of splitting).  A k-split costs the partial tiles' write and ordered re-read,
+// the serial reduction by the last unit of each tile and the counter reset: measured
+// on the Llama shapes at 512 columns (gate: 2 waves unsplit beat 3 waves of half-k
+// units by 20 %; down: one wave of half-k units beat 42 % of the SMs unsplit by 28 %),
+// about 8 + 30 * MT * BN/256 k-blocks.
+double plan_kblocks(int64_t tiles, int num_kb, int bn, int mt, int s, int ctas)
 {
-    const double kblock = 0.003125 * (16.0 * mt + bn / 8.0) + 0.3 * mt * bn / 256.0;
-    const double split = (8.0 + 30.0 * mt * bn / 256.0) * 0.45;
+    const double split = 8.0 + 30.0 * mt * bn / 256.0;
     const double waves = std::ceil((double)tiles * s / ctas);
-    return waves * ((double)num_kb / s * kblock + (s > 1 ? split : 0.0));
+    return waves * ((double)num_kb / s + (s > 1 ? split : 0.0));
 }
+
+// Measured time of one k-block with 256-column tiles: 0.45 us for a 128-row unit,
+// 0.80 us for a 256-row unit (twice the work, two thirds of the operand bytes per
+// unit of work).
+constexpr double kKblockUs[3] = {0.0, 0.45, 0.80};
 
 constexpr int kMaxDevices = 64;
 std::once_flag g_attr_once[kMaxDevices][2];
@@ -503,16 +507,23 @@ int plan_gemm(Plan *pl, int64_t rows, int64_t k, int64_t ncols, const DeviceInfo
     // (two MMAs sharing the X tile: fewer operand bytes per unit of work) are taken only
     // with full 256-column tiles, where they were measured.
     int mt_unit = 1, splits = 1;
-    double best = 1e300;
+    double best_us = 1e300;
     for (int mt = 1; mt <= (allow_mt2 && p.mt >= 2 && p.bn == 256 ? 2 : 1); mt++) {
         const int64_t tiles = (int64_t)((p.mt + mt - 1) / mt) * p.nt;
+        int best_s = 1;
+        double best_kb = 1e300;
         for (int sp = 1; sp <= (allow_split ? std::min(kMaxSplits, p.num_kb) : 1); sp++) {
-            const double c = plan_cost(tiles, p.num_kb, p.bn, mt, sp, dev.sm_count);
-            if (c < best - 1e-9) {
-                best = c;
-                mt_unit = mt;
-                splits = sp;
+            const double c = plan_kblocks(tiles, p.num_kb, p.bn, mt, sp, dev.sm_count);
+            if (c < best_kb - 1e-9) {
+                best_kb = c;
+                best_s = sp;
             }
+        }
+        const double us = best_kb * kKblockUs[mt];
+        if (us < best_us - 1e-9) {
+            best_us = us;
+            mt_unit = mt;
+            splits = best_s;
         }
     }
     pl->mt_per_unit = mt_unit;
