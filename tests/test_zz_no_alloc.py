@@ -58,7 +58,7 @@ def test_noalloc_matches_matmul_twice(bm, rows, k, ncols):
 
 def test_noalloc_refuses_products_beyond_its_scratch(bm):
     import torch
-    rows, k, ncols = 4096, 14336, 512  # split along k: 16 MiB of partial tiles, more than the scratch
+    rows, k, ncols = 1024, 65536, 512  # 16 tiles, 8 k-splits: 16 MiB of partial tiles, more than the scratch
     dW = to_dev(rnd_f16(202, (rows, k)))
     dX = to_dev(act(203, (ncols, k)))
     Y = torch.zeros((ncols, rows), dtype=torch.float32, device="cuda")
