@@ -68,6 +68,8 @@ def lib():
             L.or_check_to_f16_vs_compiler.argtypes = [C.c_uint64, C.c_uint64, C.POINTER(C.c_uint32)]
             L.or_check_to_f16_vs_compiler.restype = C.c_int64
             L.or_threads.argtypes = []; L.or_threads.restype = C.c_int
+            L.or_rms_norm_mul_rows.argtypes = [f32p, f32p, C.c_int64, C.c_int64, C.c_float, f32p]
+            L.or_rms_norm_mul_rows.restype = None
             _lib = L
     return _lib
 
@@ -180,6 +182,19 @@ def abs_matmul(W, X) -> np.ndarray:
     ncols = X.shape[0]
     out = np.empty((ncols, rows), dtype=np.float64)
     lib().or_abs_matmul(_p(W, C.c_uint16), rows, k, _p(X, C.c_uint16), ncols, _p(out, C.c_double))
+    return out
+
+
+def rms_norm_mul(x, w, eps: float) -> np.ndarray:
+    """rms_norm then mul of each row of x (1-D, or rows x n) by the weight w (n)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    n = x.shape[-1]
+    assert w.shape == (n,) and n >= 1
+    rows = x.size // n
+    out = np.empty(x.shape, dtype=np.float32)
+    lib().or_rms_norm_mul_rows(_p(x, C.c_float), _p(w, C.c_float), rows, n, float(np.float32(eps)),
+                               _p(out, C.c_float))
     return out
 
 

@@ -219,6 +219,40 @@ int64_t or_check_to_f16_vs_compiler(uint64_t lo, uint64_t hi, uint32_t *first_ba
     return bad;
 }
 
+/*
+ * rms_norm then mul of one row of n f32 values by an f32 weight (page
+ * "docs/modules/forward.md", Technical usage, "Other public pieces": the sum of
+ * squares in double, no FMA; Design notes, step three: the first RMS norm with its
+ * weight gives attn_norm-0).  Readings where the page is silent:
+ *   - each square is one f32 multiply (the row's own type), widened to double and
+ *     added in index order to a double sum that starts at +0;
+ *   - the mean is sum / n divided in double, then rounded to f32;
+ *   - scale = 1 / sqrt(mean + eps): an f32 add, a correctly rounded f32 square root
+ *     and an f32 division;
+ *   - out[i] = (x[i] * scale) * w[i]: two f32 multiplies, each rounded.
+ * A zero row with eps == 0 gives 0 * inf = NaN, as the formula does.
+ */
+void or_rms_norm_mul(const float *x, const float *w, int64_t n, float eps, float *out)
+{
+    double sum = 0.0;
+    for (int64_t i = 0; i < n; i++) {
+        float sq = x[i] * x[i];
+        sum += (double)sq;
+    }
+    float mean = (float)(sum / (double)n);
+    float scale = 1.0f / sqrtf(mean + eps);
+    for (int64_t i = 0; i < n; i++) {
+        float y = x[i] * scale;
+        out[i] = y * w[i];
+    }
+}
+
+void or_rms_norm_mul_rows(const float *X, const float *w, int64_t rows, int64_t n, float eps, float *out)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; r++) or_rms_norm_mul(X + r * n, w, n, eps, out + r * n);
+}
+
 int or_threads(void)
 {
 #ifdef _OPENMP

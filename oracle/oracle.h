@@ -19,6 +19,11 @@
  *   - matvec, matvec_multi, matmul : section "Matrix products"
  *                     (out[c*rows + r]; sgemm_dot when takes_sgemm, else vec_dot).
  *
+ * and (page "docs/modules/forward.md", bankML):
+ *   - rms_norm_mul  : section "Technical usage", "Other public pieces" -- rms_norm
+ *                     then mul, the sum of squares in double, no FMA (the readings
+ *                     of the steps the page leaves open are listed in oracle.c).
+ *
  * Every f16 x f16 product is exact in f32 (11-bit significands, exponents well
  * inside the f32 normal range), so an FMA and a multiply-then-add give the same
  * bits; this file uses plain '*' and '+' and is built with -ffp-contract=off.
@@ -59,6 +64,12 @@ void or_matmul_sample(const uint16_t *W, int64_t rows, int64_t k, const uint16_t
 /* Sum |w.a| in double for every element, laid out as out[c*rows + r]. */
 void or_abs_matmul(const uint16_t *W, int64_t rows, int64_t k, const uint16_t *X,
                    int64_t ncols, double *out);
+
+/* rms_norm then mul: out = (x * (1 / sqrt(mean(x^2) + eps))) * w, one row of n
+ * values, or `rows` rows of n values laid out one after another. */
+void or_rms_norm_mul(const float *x, const float *w, int64_t n, float eps, float *out);
+void or_rms_norm_mul_rows(const float *X, const float *w, int64_t rows, int64_t n, float eps,
+                          float *out);
 
 /* Exhaustive self-checks over every f32 bit pattern in [lo, hi): returns the
  * number of non-NaN inputs whose or_to_f16 differs from the C compiler's own

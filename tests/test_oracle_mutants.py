@@ -1,7 +1,8 @@
 """Mistakes planted in a copy of the oracle (on the CPU) must be caught by the pins.
 
 Each mutant is oracle.c with one plausible slip -- a transposed pairing, a dropped
-term, a wrong sign or index, a float tail, a wrong rounding rule -- compiled into
+term, a wrong sign or index, a float tail, a wrong rounding rule, a norm summed in
+float or with eps in the wrong place -- compiled into
 a temporary library and run through the same page-derived checks the pin tests
 use.  The unmutated source passes every check; each mutant must fail at least one.
 """
@@ -14,6 +15,7 @@ import tempfile
 import numpy as np
 import pytest
 
+import norm_cases
 from conftest import GOLDEN, ROOT
 
 SRC = os.path.join(ROOT, "oracle", "oracle.c")
@@ -48,6 +50,18 @@ MUTANTS = {
     "to_f16_subnormal_shift": ("uint32_t shift = 126 - e;", "uint32_t shift = 125 - e;"),
     "widen_subnormal_scale": ("float v = (float)m * 0x1p-24f;", "float v = (float)m * 0x1p-25f;"),
     "matmul_layout_transposed": ("int64_t c = e / rows, r = e % rows;", "int64_t r = e / ncols, c = e % ncols;"),
+    "norm_sum_in_float": ("    double sum = 0.0;\n    for (int64_t i = 0; i < n; i++) {\n        float sq = x[i] * x[i];\n"
+                          "        sum += (double)sq;",
+                          "    float sum = 0.0f;\n    for (int64_t i = 0; i < n; i++) {\n        float sq = x[i] * x[i];\n"
+                          "        sum += sq;"),
+    "norm_dropped_first_square": ("for (int64_t i = 0; i < n; i++) {\n        float sq",
+                                  "for (int64_t i = 1; i < n; i++) {\n        float sq"),
+    "norm_mean_over_n_minus_1": ("(float)(sum / (double)n)", "(float)(sum / (double)(n > 1 ? n - 1 : 1))"),
+    "norm_eps_outside_root": ("1.0f / sqrtf(mean + eps)", "1.0f / sqrtf(mean) + eps"),
+    "norm_no_root": ("1.0f / sqrtf(mean + eps)", "1.0f / (mean + eps)"),
+    "norm_sign_lost": ("float y = x[i] * scale;", "float y = fabsf(x[i]) * scale;"),
+    "norm_weight_reversed": ("out[i] = y * w[i];", "out[i] = y * w[n - 1 - i];"),
+    "norm_weight_dropped": ("out[i] = y * w[i];", "out[i] = y;"),
 }
 
 
@@ -66,6 +80,7 @@ def build(src_text, d, name):
     L.or_to_f16.argtypes = [C.c_float]; L.or_to_f16.restype = C.c_uint16
     L.or_widen.argtypes = [C.c_uint16]; L.or_widen.restype = C.c_float
     L.or_matmul.argtypes = [u16p, C.c_int64, C.c_int64, u16p, C.c_int64, f32p]; L.or_matmul.restype = None
+    L.or_rms_norm_mul.argtypes = [f32p, f32p, C.c_int64, C.c_float, f32p]; L.or_rms_norm_mul.restype = None
     return L
 
 
@@ -113,6 +128,15 @@ def failures(L):
         L.or_matmul(P(W), rows, k, P(X), ncols, Y.ctypes.data_as(C.POINTER(C.c_float)))
         if not np.array_equal(Y, (Xi @ Wi.T).astype(np.float32)):
             bad.append("matmul_layout")
+
+    def norm(x, w, eps):
+        x, w = np.ascontiguousarray(x, np.float32), np.ascontiguousarray(w, np.float32)
+        out = np.empty_like(x)
+        F = lambda a: a.ctypes.data_as(C.POINTER(C.c_float))
+        L.or_rms_norm_mul(F(x), F(w), x.size, float(np.float32(eps)), F(out))
+        return out
+
+    bad += ["norm:" + b for b in norm_cases.failures(norm)]
     return bad
 
 
