@@ -15,6 +15,8 @@ Extra objects in the same JSON line:
   roofline     -- the step's kernel (k_gemv_stream) against the measured HBM peak
   unfused      -- the same step as bm_to_f16 + bm_f16_matvec[_multi]/bm_f16_logits
                   (242 launches)
+  norm_front_end -- the step with the RMS norm ahead of Q/K/V, gate/up and the
+                  logits fused into those products (bm_f16_matvec_norm)
   products     -- single products of the Llama-3-8B / Qwen3-0.6B shapes:
                   decode GB/s and 512-column tensor-core TFLOP/s
   e2e          -- the same step through the Python binding, eagerly, with the
@@ -221,7 +223,10 @@ def run_gpu(args, rank, world, local_rank):
     # copying its weights while the kernel ahead of it is still running.
     bm.bm_set_pdl(not args.no_pdl)
 
-    def run_step(s, fused=True):
+    norm_w = {k: torch.from_numpy((1.0 + synth.normal_f32(SEED, "smollm2.norm%d" % k, 0.2, k))
+                                  .astype(np.float32)).to(dev) for k in (HIDDEN,)}
+
+    def run_step(s, fused=True, norm=False):
         for op in plan:
             if op[0] == "round":
                 if not fused:
@@ -229,6 +234,11 @@ def run_gpu(args, rank, world, local_rank):
                     bm.bm_to_f16(act_f32[offs[a]:offs[a] + op[1]], act_f16[offs[a]:offs[a] + op[1]], stream=s)
                 continue
             kind, mats, k, a = op
+            if norm and kind in ("multi", "logits"):
+                # the norm ahead of Q/K/V, of gate/up and of the logits, fused into the product
+                bm.bm_f16_matvec_norm([weights[n] for n, _ in mats], act_f32[offs[a]:offs[a] + k], norm_w[k], 1e-5,
+                                      [outs[n] for n, _ in mats], stream=s)
+                continue
             if fused:
                 bm.bm_f16_matvec_act([weights[n] for n, _ in mats], act_f32[offs[a]:offs[a] + k],
                                      [outs[n] for n, _ in mats], stream=s)
@@ -243,18 +253,19 @@ def run_gpu(args, rank, world, local_rank):
 
     launches_per_step = sum(1 for op in plan if op[0] != "round")
 
-    def capture(fused):
+    def capture(fused, norm=False):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.stream(stream):
-            run_step(stream, fused)  # warm (attribute setup happens outside capture)
+            run_step(stream, fused, norm)  # warm (attribute setup happens outside capture)
         torch.cuda.synchronize()
         with torch.cuda.graph(g, stream=stream):
-            run_step(stream, fused)
+            run_step(stream, fused, norm)
         torch.cuda.synchronize()
         return g
 
     g_step = capture(True)
     g_unfused = capture(False)
+    g_norm = capture(True, True)
 
     def timed(g, steps, warmup):
         for _ in range(warmup):
@@ -282,6 +293,7 @@ def run_gpu(args, rank, world, local_rank):
     ms = timed(g_step, args.steps, args.warmup)
     t_end = time.time()
     ms_unfused = timed(g_unfused, max(args.steps, 20), args.warmup)
+    ms_norm = timed(g_norm, max(args.steps, 20), args.warmup)
     clk = clocks.summary(t_begin, t_end)
     clocks.stop()
 
@@ -315,7 +327,7 @@ def run_gpu(args, rank, world, local_rank):
     ms_e2e = e0.elapsed_time(e1) / e2e_steps
 
     result = {
-        "ms": ms, "ms_unfused": ms_unfused, "ms_e2e": ms_e2e, "tot_bytes": tot_bytes,
+        "ms": ms, "ms_unfused": ms_unfused, "ms_norm": ms_norm, "ms_e2e": ms_e2e, "tot_bytes": tot_bytes,
         "unfused_bytes": unfused_bytes, "launches_per_step": launches_per_step, "clocks": clk,
         "h2d": int(act_host.nbytes), "d2h": int(VOCAB * 4),
     }
@@ -446,10 +458,30 @@ def bench_llama_decode(bm, dev, stream, torch, steps=10):
             bm.bm_f16_matvec_act([w["down"]], xf, [ys["down"]], stream=stream)
         bm.bm_f16_matvec_act([out_w], xa, [logits], stream=stream)
 
+    norms = [torch.from_numpy((1.0 + synth.normal_f32(SEED, "llama3_8b.norm%d" % i, 0.2, hid)).astype(np.float32))
+             .to(dev) for i in range(2 * layers + 1)]
+
+    def step_norm():
+        # the same step with the RMS norm ahead of Q/K/V, gate/up and the output product
+        # fused into those launches (each reads its norm weight, 4 * 4096 bytes, too)
+        for L in range(layers):
+            w = lw[L]
+            bm.bm_f16_matvec_norm([w["q"], w["k"], w["v"]], xa, norms[2 * L], 1e-5, [ys["q"], ys["k"], ys["v"]],
+                                  stream=stream)
+            bm.bm_f16_matvec_act([w["o"]], xa, [ys["o"]], stream=stream)
+            bm.bm_f16_matvec_norm([w["gate"], w["up"]], xa, norms[2 * L + 1], 1e-5, [ys["gate"], ys["up"]],
+                                  stream=stream)
+            bm.bm_f16_matvec_act([w["down"]], xf, [ys["down"]], stream=stream)
+        bm.bm_f16_matvec_norm([out_w], xa, norms[-1], 1e-5, [logits], stream=stream)
+
     ms = graph_time(torch, stream, step, reps=steps)
+    ms_norm = graph_time(torch, stream, step_norm, reps=steps)
     res = {"ms_per_step": round(ms, 4), "GB_s": round(nbytes / ms / 1e6, 1), "weight_GB": round(
-        (sum(t.numel() for t in base.values()) * layers + out_w.numel()) * 2 / 1e9, 3), "launches": 4 * layers + 1}
-    del lw, out_w, base
+        (sum(t.numel() for t in base.values()) * layers + out_w.numel()) * 2 / 1e9, 3), "launches": 4 * layers + 1,
+        "with_norm_front_end": {"ms_per_step": round(ms_norm, 4),
+                                "GB_s": round((nbytes + 4 * hid * (2 * layers + 1)) / ms_norm / 1e6, 1),
+                                "how": "bm_f16_matvec_norm for Q/K/V, gate/up and the output product"}}
+    del lw, out_w, base, norms
     return res
 
 
@@ -628,6 +660,11 @@ def main():
                     "value": round(r["unfused_bytes"] / (r["ms_unfused"] / 1e3) / 1e9, 2),
                     "launches_per_step": 2 * r["launches_per_step"],
                     "how": "bm_to_f16 then bm_f16_matvec[_multi] / bm_f16_logits per product"},
+        "norm_front_end": {"ms_per_step": round(r["ms_norm"], 5),
+                           "value": round((r["tot_bytes"] + 4 * HIDDEN * (2 * LAYERS + 1)) / (r["ms_norm"] / 1e3) / 1e9,
+                                          2),
+                           "how": "the step with the RMS norm (rms_norm then mul) ahead of Q/K/V, gate/up and the "
+                                  "logits fused into those launches (bm_f16_matvec_norm)"},
         "gpu_launches": r["launches_per_step"] * args.steps,
         "clocks": r["clocks"],
         "e2e": {"value": round(r["tot_bytes"] / (r["ms_e2e"] / 1e3) / 1e9, 2), "unit": "GB/s",

@@ -17,7 +17,7 @@ import torch
 from . import _build
 
 __all__ = [
-    "BmError", "lib", "bm_to_f16", "bm_f16_matvec", "bm_f16_matvec_multi", "bm_f16_matvec_act", "bm_f16_matmul", "bm_f16_matmul_noalloc",
+    "BmError", "lib", "bm_to_f16", "bm_f16_matvec", "bm_f16_matvec_multi", "bm_f16_matvec_act", "bm_f16_matvec_norm", "bm_rms_norm_mul", "bm_f16_matmul", "bm_f16_matmul_noalloc",
     "bm_f16_logits", "bm_f16_get_rows", "bm_takes_sgemm", "bm_device_status", "bm_status_string", "bm_last_error",
     "bm_selftest_wait_timeout", "bm_set_pdl", "bm_set_exact_sgemm_cols", "EXPORTS", "BM_MAX_K",
 ]
@@ -32,6 +32,9 @@ EXPORTS = {
     "bm_f16_matvec": (_i, [_vp, _i64, _i64, _vp, _vp, _vp]),
     "bm_f16_matvec_multi": (_i, [_i, C.POINTER(_vp), C.POINTER(_i64), _i64, _vp, C.POINTER(_vp), _vp]),
     "bm_f16_matvec_act": (_i, [_i, C.POINTER(_vp), C.POINTER(_i64), _i64, _vp, _vp, C.POINTER(_vp), _vp]),
+    "bm_f16_matvec_norm": (_i, [_i, C.POINTER(_vp), C.POINTER(_i64), _i64, _vp, _vp, C.c_float, _vp, _vp,
+                                C.POINTER(_vp), _vp]),
+    "bm_rms_norm_mul": (_i, [_vp, _vp, _i64, _i64, C.c_float, _vp, _vp, _vp]),
     "bm_f16_matmul": (_i, [_vp, _i64, _i64, _vp, _i64, _vp, _vp]),
     "bm_f16_logits": (_i, [_vp, _i64, _i64, _vp, _i64, _vp, _vp]),
     "bm_f16_matmul_noalloc": (_i, [_vp, _i64, _i64, _vp, _i64, _vp, _vp]),
@@ -173,6 +176,62 @@ def bm_f16_matvec_act(Ws, x: torch.Tensor, ys=None, h: torch.Tensor | None = Non
     _check(lib().bm_f16_matvec_act(n, wp, rows, k, _dev(x, "x", (torch.float32,)), hp, yp, _stream(stream)),
            "bm_f16_matvec_act")
     return ys
+
+
+def bm_f16_matvec_norm(Ws, x: torch.Tensor, g: torch.Tensor, eps: float, ys=None, n_out=None,
+                       h: torch.Tensor | None = None, stream=None):
+    """rms_norm then mul of the f32 row x by g, rounded to f16, multiplied by each
+    matrix in Ws -- one launch.  n_out / h (optional) receive the normed row and its
+    f16 rounding.  Returns ys."""
+    n = len(Ws)
+    k = x.numel()
+    if g.numel() != k:
+        raise ValueError("g must have k elements")
+    if ys is None:
+        ys = [torch.empty(W.shape[0], dtype=torch.float32, device=x.device) for W in Ws]
+    if len(ys) != n:
+        raise ValueError("one output per matrix")
+    for W, y in zip(Ws, ys):
+        r, kk = _wk(W)
+        if kk != k or y.numel() != r:
+            raise ValueError("shape mismatch in bm_f16_matvec_norm")
+    if h is not None and h.numel() != k:
+        raise ValueError("h must have k elements")
+    if n_out is not None and n_out.numel() != k:
+        raise ValueError("n_out must have k elements")
+    wp = (C.c_void_p * max(n, 1))(*[_dev(W, "W", _F16_LIKE) for W in Ws])
+    yp = (C.c_void_p * max(n, 1))(*[_dev(y, "y", (torch.float32,)) for y in ys])
+    rows = (C.c_int64 * max(n, 1))(*[W.shape[0] for W in Ws])
+    hp = _dev(h, "h", _F16_LIKE) if h is not None else None
+    np_ = _dev(n_out, "n_out", (torch.float32,)) if n_out is not None else None
+    _check(lib().bm_f16_matvec_norm(n, wp, rows, k, _dev(x, "x", (torch.float32,)), _dev(g, "g", (torch.float32,)),
+                                    float(eps), np_, hp, yp, _stream(stream)), "bm_f16_matvec_norm")
+    return ys
+
+
+def bm_rms_norm_mul(x: torch.Tensor, g: torch.Tensor, eps: float, out=None, h=None, want_out: bool = True,
+                    stream=None):
+    """rms_norm then mul of each row of x ([nrows][k] or [k], f32) by g (f32[k]).
+    out (f32, same shape; may be x itself) and/or h (f16 bits, same shape) receive the
+    result; with neither given, out is allocated (and h too when want_out is False).
+    Returns (out, h)."""
+    k = x.shape[-1] if x.dim() > 0 else 0
+    nrows = x.numel() // k if k else 0
+    if g.numel() != k:
+        raise ValueError("g must have k elements")
+    if out is None and h is None:
+        if want_out:
+            out = torch.empty_like(x)
+        else:
+            h = torch.empty(x.shape, dtype=torch.float16, device=x.device)
+    for t, name in ((out, "out"), (h, "h")):
+        if t is not None and t.numel() != x.numel():
+            raise ValueError(name + " must have as many elements as x")
+    op = _dev(out, "out", (torch.float32,)) if out is not None else None
+    hp = _dev(h, "h", _F16_LIKE) if h is not None else None
+    _check(lib().bm_rms_norm_mul(_dev(x, "x", (torch.float32,)), _dev(g, "g", (torch.float32,)), nrows, k,
+                                 float(eps), op, hp, _stream(stream)), "bm_rms_norm_mul")
+    return out, h
 
 
 def _product(fn_name: str, W, X, Y, stream):

@@ -256,49 +256,114 @@ int bm_f16_matvec_multi(int nmat, const uint16_t *const *W, const int64_t *rows,
     return launch_vecdot_1col(job, reinterpret_cast<cudaStream_t>(stream), dev);
 }
 
-int bm_f16_matvec_act(int nmat, const uint16_t *const *W, const int64_t *rows, int64_t k, const float *x,
-                      uint16_t *h, float *const *y, bm_stream_t stream)
+namespace {
+
+// bm_f16_matvec_act and bm_f16_matvec_norm: the f32 activation, optionally normalised
+// (nrm non-null), rounded to f16 and multiplied by up to four matrices.
+int act_products(const char *fn, int nmat, const uint16_t *const *W, const int64_t *rows, int64_t k, const float *x,
+                 const ActNorm *nrm, uint16_t *h, float *const *y, bm_stream_t stream)
 {
-    clear_error();
-    if (nmat < 1 || nmat > 4) return fail(BM_ERR_INVALID_ARG, "bm_f16_matvec_act: nmat = %d outside 1..4", nmat);
-    if (!W || !rows || !y) return fail(BM_ERR_INVALID_ARG, "bm_f16_matvec_act: null host array");
-    if (k < 1 || k > BM_MAX_K) return fail(BM_ERR_INVALID_ARG, "bm_f16_matvec_act: k = %lld outside 1..%d", (long long)k, BM_MAX_K);
-    if (!x) return fail(BM_ERR_INVALID_ARG, "bm_f16_matvec_act: null activation");
+    if (nmat < 1 || nmat > 4) return fail(BM_ERR_INVALID_ARG, "%s: nmat = %d outside 1..4", fn, nmat);
+    if (!W || !rows || !y) return fail(BM_ERR_INVALID_ARG, "%s: null host array", fn);
+    if (k < 1 || k > BM_MAX_K) return fail(BM_ERR_INVALID_ARG, "%s: k = %lld outside 1..%d", fn, (long long)k, BM_MAX_K);
+    if (!x) return fail(BM_ERR_INVALID_ARG, "%s: null activation", fn);
     if (!aligned(x, 16) || (h && !aligned(h, 16)))
-        return fail(BM_ERR_ALIGNMENT, "bm_f16_matvec_act: x and h must be 16-byte aligned");
-    if (h && overlap(h, k * 2, x, k * 4)) return fail(BM_ERR_INVALID_ARG, "bm_f16_matvec_act: h overlaps x");
+        return fail(BM_ERR_ALIGNMENT, "%s: x and h must be 16-byte aligned", fn);
+    if (h && overlap(h, k * 2, x, k * 4)) return fail(BM_ERR_INVALID_ARG, "%s: h overlaps x", fn);
+    float *n_out = nrm ? nrm->n_out : nullptr;
+    if (nrm) {
+        if (!nrm->g) return fail(BM_ERR_INVALID_ARG, "%s: null norm weight", fn);
+        if (!aligned(nrm->g, 16) || (n_out && !aligned(n_out, 16)))
+            return fail(BM_ERR_ALIGNMENT, "%s: g and n_out must be 16-byte aligned", fn);
+        if (n_out && (overlap(n_out, k * 4, x, k * 4) || overlap(n_out, k * 4, nrm->g, k * 4) ||
+                      (h && overlap(n_out, k * 4, h, k * 2))))
+            return fail(BM_ERR_INVALID_ARG, "%s: n_out overlaps x, g or h", fn);
+        if (h && overlap(h, k * 2, nrm->g, k * 4)) return fail(BM_ERR_INVALID_ARG, "%s: h overlaps g", fn);
+    }
     VecdotJob job{};
     job.k = k;
     job.ncols = 1;
     for (int m = 0; m < nmat; m++) {
         // the products' checks, with the activation standing in as X (same size in bytes or larger)
-        int st = check_matrix_args("bm_f16_matvec_act", W[m], rows[m], k, reinterpret_cast<const uint16_t *>(x), 1, y[m]);
+        int st = check_matrix_args(fn, W[m], rows[m], k, reinterpret_cast<const uint16_t *>(x), 1, y[m]);
         if (st != BM_OK) return st;
         if (overlap(y[m], rows[m] * 4, x, k * 4) || (h && (overlap(h, k * 2, y[m], rows[m] * 4) ||
                                                           overlap(h, k * 2, W[m], rows[m] * k * 2))))
-            return fail(BM_ERR_INVALID_ARG, "bm_f16_matvec_act: output %d overlaps an input or output", m);
+            return fail(BM_ERR_INVALID_ARG, "%s: output %d overlaps an input or output", fn, m);
+        if (nrm && (overlap(y[m], rows[m] * 4, nrm->g, k * 4) ||
+                    (n_out && (overlap(n_out, k * 4, y[m], rows[m] * 4) ||
+                               overlap(n_out, k * 4, W[m], rows[m] * k * 2)))))
+            return fail(BM_ERR_INVALID_ARG, "%s: output %d overlaps an input or output", fn, m);
         for (int q = 0; q < m; q++)
             if (overlap(y[m], rows[m] * 4, y[q], rows[q] * 4) || overlap(y[m], rows[m] * 4, W[q], rows[q] * k * 2) ||
                 overlap(y[q], rows[q] * 4, W[m], rows[m] * k * 2))
-                return fail(BM_ERR_INVALID_ARG, "bm_f16_matvec_act: output %d overlaps an input or output", m);
+                return fail(BM_ERR_INVALID_ARG, "%s: output %d overlaps an input or output", fn, m);
         if (rows[m] == 0) continue;
         job.W[job.nmat] = W[m];
         job.y[job.nmat] = y[m];
         job.rows[job.nmat] = rows[m];
         job.nmat++;
     }
+    if (job.nmat > 0 && k % 8 != 0 && !h) return fail(BM_ERR_INVALID_ARG, "%s: k %% 8 != 0 needs the h buffer", fn);
     int st;
     DeviceInfo dev;
     if (!current_device(&dev, &st)) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (job.nmat == 0) return h ? launch_to_f16(x, h, k, s, dev) : BM_OK;
-    if (k % 8 == 0) return launch_gemv_stream(job, x, h, s, dev);
+    if (job.nmat == 0) {
+        if (nrm) return (h || n_out) ? launch_rms_norm(x, nrm->g, 1, k, nrm->eps, n_out, h, s, dev) : BM_OK;
+        return h ? launch_to_f16(x, h, k, s, dev) : BM_OK;
+    }
+    if (k % 8 == 0) return launch_gemv_stream(job, x, h, s, dev, nrm);
     // rows that are not 16-byte aligned: round into h, then the lane-per-chain kernel
-    if (!h) return fail(BM_ERR_INVALID_ARG, "bm_f16_matvec_act: k %% 8 != 0 needs the h buffer");
-    st = launch_to_f16(x, h, k, s, dev);
+    st = nrm ? launch_rms_norm(x, nrm->g, 1, k, nrm->eps, n_out, h, s, dev) : launch_to_f16(x, h, k, s, dev);
     if (st != BM_OK) return st;
     job.X = h;
     return launch_vecdot_1col(job, s, dev);
+}
+
+}  // namespace
+
+int bm_f16_matvec_act(int nmat, const uint16_t *const *W, const int64_t *rows, int64_t k, const float *x,
+                      uint16_t *h, float *const *y, bm_stream_t stream)
+{
+    clear_error();
+    return act_products("bm_f16_matvec_act", nmat, W, rows, k, x, nullptr, h, y, stream);
+}
+
+int bm_f16_matvec_norm(int nmat, const uint16_t *const *W, const int64_t *rows, int64_t k, const float *x,
+                       const float *g, float eps, float *n_out, uint16_t *h, float *const *y, bm_stream_t stream)
+{
+    clear_error();
+    ActNorm nrm;
+    nrm.g = g;
+    nrm.eps = eps;
+    nrm.n_out = n_out;
+    return act_products("bm_f16_matvec_norm", nmat, W, rows, k, x, &nrm, h, y, stream);
+}
+
+int bm_rms_norm_mul(const float *x, const float *g, int64_t nrows, int64_t k, float eps, float *out, uint16_t *h,
+                    bm_stream_t stream)
+{
+    clear_error();
+    if (nrows < 0 || k < 1 || k > BM_MAX_K)
+        return fail(BM_ERR_INVALID_ARG, "bm_rms_norm_mul: nrows = %lld, k = %lld (need nrows >= 0, 1 <= k <= %d)",
+                    (long long)nrows, (long long)k, BM_MAX_K);
+    if (nrows > (INT64_MAX / 4) / k) return fail(BM_ERR_INVALID_ARG, "bm_rms_norm_mul: nrows * k too large");
+    if (!x || !g) return fail(BM_ERR_INVALID_ARG, "bm_rms_norm_mul: null x or g");
+    if (!out && !h) return fail(BM_ERR_INVALID_ARG, "bm_rms_norm_mul: neither out nor h given");
+    if (!aligned(x, 4) || !aligned(g, 4) || (out && !aligned(out, 4)) || (h && !aligned(h, 2)))
+        return fail(BM_ERR_ALIGNMENT, "bm_rms_norm_mul: x, g, out must be 4-byte aligned and h 2-byte aligned");
+    const int64_t n = nrows * k;
+    if (out && out != x && overlap(out, n * 4, x, n * 4))
+        return fail(BM_ERR_INVALID_ARG, "bm_rms_norm_mul: out overlaps x without being x");
+    if ((out && overlap(out, n * 4, g, k * 4)) || (h && (overlap(h, n * 2, x, n * 4) || overlap(h, n * 2, g, k * 4) ||
+                                                         (out && overlap(h, n * 2, out, n * 4)))))
+        return fail(BM_ERR_INVALID_ARG, "bm_rms_norm_mul: an output overlaps an input or the other output");
+    if (nrows == 0) return BM_OK;
+    int st;
+    DeviceInfo dev;
+    if (!current_device(&dev, &st)) return st;
+    return launch_rms_norm(x, g, nrows, k, eps, out, h, reinterpret_cast<cudaStream_t>(stream), dev);
 }
 
 int bm_f16_matmul(const uint16_t *W, int64_t rows, int64_t k, const uint16_t *X, int64_t ncols, float *Y,

@@ -44,11 +44,21 @@ struct VecdotJob {
 int launch_to_f16(const float *x, uint16_t *h, int64_t n, cudaStream_t s, const DeviceInfo &dev);
 // One column, any k; uses the 16-byte fast kernel when k % 8 == 0.
 int launch_vecdot_1col(const VecdotJob &job, cudaStream_t s, const DeviceInfo &dev);
+// The rms_norm then mul that may precede the rounding of an f32 activation.
+struct ActNorm {
+    const float *g = nullptr;  // norm weight, f32[k], 16-byte aligned
+    float eps = 0.0f;
+    float *n_out = nullptr;    // optional: the normalised row, f32[k], 16-byte aligned
+};
 // One column, k % 8 == 0: rows streamed through shared memory by TMA.  With
 // x_f32 non-null the activation is read in f32 and rounded in the kernel
-// (job.X is then unused); h_out, if non-null, receives the rounded activation.
+// (job.X is then unused), after rms_norm then mul when nrm is non-null; h_out, if
+// non-null, receives the rounded activation.
 int launch_gemv_stream(const VecdotJob &job, const float *x_f32, uint16_t *h_out, cudaStream_t s,
-                       const DeviceInfo &dev);
+                       const DeviceInfo &dev, const ActNorm *nrm = nullptr);
+// rms_norm then mul of nrows rows of k values (out and/or h; out may equal x).
+int launch_rms_norm(const float *x, const float *g, int64_t nrows, int64_t k, float eps, float *out, uint16_t *h,
+                    cudaStream_t s, const DeviceInfo &dev);
 // ncols >= 1 columns of one matrix, any k, Y[c*rows + r], bit-exact vec_dot.
 int launch_vecdot_ncol(const VecdotJob &job, cudaStream_t s, const DeviceInfo &dev);
 // Most columns taken by the CUDA-core tinyBLAS kernel (launch_sgemm_stream); wider

@@ -7,7 +7,12 @@
 // (a0+a2)+(a1+a3) lane-wise, low four lanes + high four lanes, two horizontal
 // adds, and the k%32 tail added in double in order.  Optionally the activation
 // arrives in f32 and is first rounded to f16, nearest-even (Design notes,
-// "Activation"), once per CTA -- the same bits bm_to_f16 gives.
+// "Activation"), once per CTA -- the same bits bm_to_f16 gives -- and, before
+// that, optionally normalised: rms_norm then mul by the norm weight (page
+// "docs/modules/forward.md", Technical usage, "Other public pieces"), with the
+// steps of bm_norm.cuh (an exact integer sum of the squares and an integer
+// mean), so every CTA reaches the same scale and the same bits as the
+// standalone norm kernel.
 //
 // Layout on the GPU.  Each matrix's rows are cut into groups of 8; the groups
 // of all (up to four) matrices are split evenly between the CTAs (CTA b owns
@@ -40,6 +45,7 @@
 #include "../../include/bm.h"
 #include "bm_device.cuh"
 #include "bm_internal.h"
+#include "bm_norm.cuh"
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -65,6 +71,9 @@ constexpr uint32_t kStageBytes = kBoxesPerStage * kBoxBytes;  // 32 KB
 constexpr int kMaxStages = 8;
 constexpr unsigned long long kTimeoutNs = 2000000000ull;
 constexpr unsigned kFull = 0xffffffffu;
+static_assert(kConsumerWarps == norm::kNormWarps, "the norm's reductions run over the eight consumer warps");
+constexpr int kNormThreadsC = norm::kNormThreads;
+constexpr int kHeldChunks = 4;  // rows of up to 4 * 4 * 256 = 4096 values keep x and g in registers
 
 // Boxes per group in one stage for a sub-block of ng groups: the stage always
 // holds up to 32 boxes, so a sub-block of few groups takes a wider k-slice.
@@ -76,10 +85,14 @@ __host__ __device__ __forceinline__ int boxes_per_group(int ng)
 struct StreamJob {
     CUtensorMap map[4];  // W[m] as [rows[m]][k] 16-bit elements, box 64 x 8, 128-byte swizzle
     float *y[4];
-    int64_t rows[4];
-    int64_t gbeg[5];     // first 8-row group of matrix m; gbeg[nmat] = total groups
+    int rows[4];         // each below 2^31 (checked on the host)
+    int gbeg[5];         // first 8-row group of matrix m; gbeg[nmat] = total groups (below 2^30)
     const void *x;       // activation: f16 bits, or f32 when x_is_f32
     uint16_t *h_out;     // optional: the rounded activation (written by CTA 0)
+    const float *g;      // with x_is_f32: rms_norm then mul by g first (null: no norm)
+    float *n_out;        // optional with g: the normalised f32 row (written by CTA 0)
+    norm::Recip rk;      // 1 / k in fixed point (the norm's mean)
+    float eps;
     int x_is_f32;
     int nmat;
     int k;
@@ -119,7 +132,7 @@ __device__ __forceinline__ uint32_t pack_rn(float lo, float hi)
     return *reinterpret_cast<uint32_t *>(&p);
 }
 
-__device__ __forceinline__ int matrix_of(const StreamJob &job, int64_t g)
+__device__ __forceinline__ int matrix_of(const StreamJob &job, int g)
 {
     int m = 0;
 #pragma unroll
@@ -148,6 +161,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv_stream(const __grid_consta
     __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
     __shared__ int abort_flag;
     __shared__ int issued_slot;
+    __shared__ norm::Scratch norm_sh;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int k = job.k;
@@ -173,17 +187,17 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv_stream(const __grid_consta
     __syncthreads();
     dev::pdl_trigger();  // the next kernel may start its own weight copies
 
-    const int64_t G = job.gbeg[job.nmat];
-    const int64_t glo = G * blockIdx.x / gridDim.x, ghi = G * (blockIdx.x + 1) / gridDim.x;
+    const int G = job.gbeg[job.nmat];
+    const int glo = (int)((int64_t)G * blockIdx.x / gridDim.x), ghi = (int)((int64_t)G * (blockIdx.x + 1) / gridDim.x);
     const int nsteps = k >> 5;
 
     if (warp >= kConsumerWarps) {
         // ------------------------------------------------------------ producers
         int t = 0;
         bool ok = true;
-        for (int64_t g = glo; g < ghi && ok;) {
+        for (int g = glo; g < ghi && ok;) {
             const int m = matrix_of(job, g);
-            const int ng = (int)min((int64_t)kGroupsPerBlock, min(ghi, job.gbeg[m + 1]) - g);
+            const int ng = min(kGroupsPerBlock, min(ghi, job.gbeg[m + 1]) - g);
             const int bpg = boxes_per_group(ng);
             const int sw = bpg * kBoxCols;  // slice width in elements
             const int nslices = (k + sw - 1) / sw;
@@ -218,12 +232,59 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv_stream(const __grid_consta
         __syncwarp();
     } else {
         // ------------------------------------------------------------ consumers
+        const bool held = job.g && k <= 4 * kHeldChunks * kNormThreadsC;
+        const int n4 = k >> 2;
+        float4 w[kHeldChunks];
+        if (held) {
+            // the norm weight is a constant, not the previous kernel's output: read this
+            // thread's chunks of it while that kernel finishes
+#pragma unroll
+            for (int i = 0; i < kHeldChunks; i++) {
+                const int c = threadIdx.x + i * kNormThreadsC;
+                w[i] = c < n4 ? __ldg(reinterpret_cast<const float4 *>(job.g) + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
         dev::pdl_wait();  // the activation is the previous kernel's output; outputs follow too
-        if (job.x_is_f32) {
+        if (held) {
+            // the norm with this thread's chunks of x held in registers: one read of x
+            const int t = threadIdx.x;
+            const float4 *xf = reinterpret_cast<const float4 *>(job.x);
+            float4 v[kHeldChunks];
+#pragma unroll
+            for (int i = 0; i < kHeldChunks; i++) {
+                const int c = t + i * kNormThreadsC;
+                v[i] = c < n4 ? __ldg(xf + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            const float scale = norm::row_scale_held(v, n4, job.rk, job.eps, t, norm_sh, [] { consumers_sync(); });
+            uint2 *xo = reinterpret_cast<uint2 *>(xs);
+#pragma unroll
+            for (int i = 0; i < kHeldChunks; i++) {
+                const int c = t + i * kNormThreadsC;
+                if (c < n4) {
+                    const float4 o = make_float4(norm::apply(v[i].x, scale, w[i].x), norm::apply(v[i].y, scale, w[i].y),
+                                                 norm::apply(v[i].z, scale, w[i].z), norm::apply(v[i].w, scale, w[i].w));
+                    if (job.n_out && blockIdx.x == 0) reinterpret_cast<float4 *>(job.n_out)[c] = o;
+                    const uint2 p = make_uint2(pack_rn(o.x, o.y), pack_rn(o.z, o.w));
+                    xo[c] = p;
+                    if (job.h_out && blockIdx.x == 0) reinterpret_cast<uint2 *>(job.h_out)[c] = p;
+                }
+            }
+        } else if (job.x_is_f32) {
             const float4 *xf = reinterpret_cast<const float4 *>(job.x);
             uint2 *xo = reinterpret_cast<uint2 *>(xs);
+            float scale = 1.0f;
+            if (job.g) {  // longer rows: x read once for the sum, once more for the values
+                scale = norm::row_scale(static_cast<const float *>(job.x), k, job.rk, job.eps, true, threadIdx.x,
+                                        norm_sh, [] { consumers_sync(); });
+            }
             for (int i = threadIdx.x; i < (k >> 2); i += 32 * kConsumerWarps) {
-                const float4 v = __ldg(xf + i);
+                float4 v = __ldg(xf + i);
+                if (job.g) {
+                    const float4 w = __ldg(reinterpret_cast<const float4 *>(job.g) + i);
+                    v = make_float4(norm::apply(v.x, scale, w.x), norm::apply(v.y, scale, w.y),
+                                    norm::apply(v.z, scale, w.z), norm::apply(v.w, scale, w.w));
+                    if (job.n_out && blockIdx.x == 0) reinterpret_cast<float4 *>(job.n_out)[i] = v;
+                }
                 const uint2 p = make_uint2(pack_rn(v.x, v.y), pack_rn(v.z, v.w));
                 xo[i] = p;
                 if (job.h_out && blockIdx.x == 0) reinterpret_cast<uint2 *>(job.h_out)[i] = p;
@@ -241,13 +302,13 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv_stream(const __grid_consta
         const uint4 *x4 = reinterpret_cast<const uint4 *>(xs) + j;  // x[32s + 8j] at x4[4s]
         bool ok = true;
         int t = 0;
-        for (int64_t g = glo; g < ghi && ok;) {
+        for (int g = glo; g < ghi && ok;) {
             const int m = matrix_of(job, g);
-            const int ng = (int)min((int64_t)kGroupsPerBlock, min(ghi, job.gbeg[m + 1]) - g);
+            const int ng = min(kGroupsPerBlock, min(ghi, job.gbeg[m + 1]) - g);
             const int bpg = boxes_per_group(ng);
             const int sw = bpg * kBoxCols;
             const int nslices = (k + sw - 1) / sw;
-            const int64_t row = (g - job.gbeg[m] + warp) * kGroupRows + rho;  // this thread's row
+            const int row = (g - job.gbeg[m] + warp) * kGroupRows + rho;  // this thread's row (< 2^31)
             const bool active = warp < ng;                                     // warp-uniform
             float acc[8];
 #pragma unroll
@@ -358,7 +419,7 @@ std::once_flag g_attr_once[kMaxDevices];
 }  // namespace
 
 int launch_gemv_stream(const VecdotJob &vj, const float *x_f32, uint16_t *h_out, cudaStream_t s,
-                       const DeviceInfo &dev)
+                       const DeviceInfo &dev, const ActNorm *nrm)
 {
     if (!encoder()) return fail(BM_ERR_CUDA, "vec_dot: cuTensorMapEncodeTiled unavailable");
     if (vj.k > 0x7fffffffLL) return fail(BM_ERR_INVALID_ARG, "vec_dot: k too large");
@@ -368,14 +429,21 @@ int launch_gemv_stream(const VecdotJob &vj, const float *x_f32, uint16_t *h_out,
     job.x = x_f32 ? static_cast<const void *>(x_f32) : static_cast<const void *>(vj.X);
     job.x_is_f32 = x_f32 != nullptr;
     job.h_out = h_out;
+    if (nrm) {
+        if (!x_f32) return fail(BM_ERR_INVALID_ARG, "vec_dot: the norm needs the f32 activation");
+        job.g = nrm->g;
+        job.eps = nrm->eps;
+        job.rk = norm::reciprocal_of(vj.k);
+        job.n_out = nrm->n_out;
+    }
     job.gbeg[0] = 0;
     for (int m = 0; m < vj.nmat; m++) {
         if (vj.rows[m] > 0x7fffffffLL) return fail(BM_ERR_INVALID_ARG, "vec_dot: rows must be below 2^31");
         if (!make_row_map(&job.map[m], vj.W[m], vj.rows[m], vj.k))
             return fail(BM_ERR_CUDA, "vec_dot: tensor map encoding failed");
         job.y[m] = vj.y[m];
-        job.rows[m] = vj.rows[m];
-        job.gbeg[m + 1] = job.gbeg[m] + (vj.rows[m] + kGroupRows - 1) / kGroupRows;
+        job.rows[m] = (int)vj.rows[m];
+        job.gbeg[m + 1] = job.gbeg[m] + (int)((vj.rows[m] + kGroupRows - 1) / kGroupRows);  // 4 x 2^28 at most
     }
     for (int m = vj.nmat; m < 4; m++) job.gbeg[m + 1] = job.gbeg[vj.nmat];
     const int64_t G = job.gbeg[vj.nmat];

@@ -107,6 +107,50 @@ int bm_f16_matvec_act(int nmat, const uint16_t *const *W, const int64_t *rows, i
                       const float *x, uint16_t *h, float *const *y, bm_stream_t stream);
 
 /*
+ * rms_norm then mul of f32 rows by an f32 norm weight (page forward.md,
+ * "Technical usage", "Other public pieces": the sum of squares in double, no
+ * FMA; "Design notes", step three: the first RMS norm with its weight gives
+ * attn_norm-0), optionally rounded to f16 (f16.md, "Activation") for the
+ * products that follow -- each row of a prefill micro-batch before bm_f16_matmul.
+ *     q_i = x_i * x_i (f32);  mean = mean of the q_i rounded once to f32;
+ *     scale = 1 / sqrtf(mean + eps) (f32 add, IEEE square root and divide);
+ *     out_i = (x_i * scale) * g_i (two f32 multiplies);  h_i = f16(out_i).
+ * The page takes the mean from a double sum of the squares, which lies within
+ * (k - 1) * 2^-53 (relative) of the exact sum.  Here the squares are summed
+ * exactly in 128-bit fixed point (squares more than 2^63 below the largest left
+ * out: together under k * 2^-63 of the sum) and the mean is divided out to 2^-62
+ * by integer steps, so it does not depend on any order and is the same in every
+ * call and in bm_f16_matvec_norm.  The f32 mean, and with it every output bit,
+ * equals the double-sum route's unless the exact mean lies within about
+ * (k + 4) * 2^-53 (relative) of an f32 rounding boundary.  A zero row with eps
+ * == 0 gives NaN, as the formula does; a NaN or infinite square makes the mean
+ * NaN or +inf.
+ *   x : device, f32[nrows][k].  g : device, f32[k].  out : device, f32[nrows][k],
+ *   or NULL; out == x (in place) is allowed, any other overlap is not.
+ *   h : device, uint16[nrows][k] (f16 bits), or NULL; at least one of out, h.
+ *   nrows >= 0, 1 <= k <= BM_MAX_K.  x, g, out 4-byte aligned, h 2-byte aligned
+ *   (16-byte aligned pointers and k % 4 == 0 take the vector loads).
+ */
+int bm_rms_norm_mul(const float *x, const float *g, int64_t nrows, int64_t k, float eps,
+                    float *out, uint16_t *h, bm_stream_t stream);
+
+/*
+ * The decode front end in one launch: n = rms_norm then mul of x by g (as
+ * bm_rms_norm_mul, same bits), h = f16(n), then y[m] = vec_dot(W[m][r], h) for
+ * up to four matrices (forward.md, "Design notes", steps three and four: the
+ * first RMS norm with its weight, then the Q, K and V projections of the normed
+ * row; the same for gate and up after the second norm).  Every bit equals
+ * bm_rms_norm_mul followed by bm_f16_matvec_multi.
+ *   x, g : device, f32[k], 16-byte aligned.  eps : the norm's epsilon.
+ *   n_out : device, f32[k], 16-byte aligned, or NULL (the normed row is then not
+ *   stored).  h : device, uint16[k], 16-byte aligned, or NULL (needed, and must
+ *   be given, when k % 8 != 0).  W, rows, y as for bm_f16_matvec_multi.
+ */
+int bm_f16_matvec_norm(int nmat, const uint16_t *const *W, const int64_t *rows, int64_t k,
+                       const float *x, const float *g, float eps, float *n_out, uint16_t *h,
+                       float *const *y, bm_stream_t stream);
+
+/*
  * Y[c*rows + r] = W[r] . X[c] for every row r and column c
  * (f16.md, "Matrix products", mat_mul_par), with the path ggml takes:
  *   - bm_takes_sgemm(rows, k, ncols): tcgen05 tensor cores, f32 accumulation,

@@ -162,3 +162,36 @@ def test_matmul_noalloc_host_checks(L):
     assert st(L, f, A, 16, 0, A + 2 ** 20, 2, A + 2 ** 21, None) == 1
     assert st(L, f, A + 2, 16, 64, A + 2 ** 20, 2, A + 2 ** 21, None) == 2
     assert st(L, f, A, 16, 64, A + 2 ** 20, 2, A + 2 ** 20 + 64, None) == 1
+
+
+def test_matvec_norm_host_checks(L):
+    f = L.bm_f16_matvec_norm
+    W = (C.c_void_p * 2)(A, A + 2 ** 20)
+    y = (C.c_void_p * 2)(A + 2 ** 24, A + 2 ** 24 + 4096)
+    rows = (C.c_int64 * 2)(16, 16)
+    x, g, n, h = A + 2 ** 26, A + 2 ** 26 + 2 ** 16, A + 2 ** 26 + 2 ** 17, A + 2 ** 27
+    assert f(0, W, rows, 64, x, g, 1e-5, n, h, y, None) == 1
+    assert f(2, W, rows, 64, x, None, 1e-5, n, h, y, None) == 1          # no norm weight
+    assert f(2, W, rows, 64, x, g + 4, 1e-5, n, h, y, None) == 2         # g misaligned
+    assert f(2, W, rows, 64, x, g, 1e-5, n + 8, h, y, None) == 2         # n_out misaligned
+    assert f(2, W, rows, 64, x, g, 1e-5, x + 16, h, y, None) == 1        # n_out overlaps x
+    assert f(2, W, rows, 64, x, g, 1e-5, g, h, y, None) == 1             # n_out overlaps g
+    assert f(2, W, rows, 64, x, g, 1e-5, n, g + 64, y, None) == 1        # h overlaps g
+    yo = (C.c_void_p * 2)(A + 2 ** 24, g + 32)                             # y overlaps g
+    assert f(2, W, rows, 64, x, g, 1e-5, n, h, yo, None) == 1
+    assert f(2, W, rows, 60, x, g, 1e-5, n, None, y, None) == 1          # k % 8 != 0 needs h
+
+
+def test_rms_norm_host_checks(L):
+    f = L.bm_rms_norm_mul
+    x, g, o, h = A, A + 2 ** 20, A + 2 ** 21, A + 2 ** 22
+    assert f(x, g, 0, 64, 1e-5, o, h, None) == 0                          # no rows: nothing to do
+    assert f(x, g, -1, 64, 1e-5, o, h, None) == 1
+    assert f(x, g, 4, 0, 1e-5, o, h, None) == 1
+    assert f(x, None, 4, 64, 1e-5, o, h, None) == 1
+    assert f(x, g, 4, 64, 1e-5, None, None, None) == 1                    # no output
+    assert f(x + 2, g, 4, 64, 1e-5, o, h, None) == 2
+    assert f(x, g, 4, 64, 1e-5, o, h + 1, None) == 2
+    assert f(x, g, 4, 64, 1e-5, x + 4, h, None) == 1                      # out overlaps x, not in place
+    assert f(x, g, 4, 64, 1e-5, o, x + 256, None) == 1                    # h overlaps x
+    assert f(x, g, 4, 64, 1e-5, g, None, None) == 1                       # out overlaps g
