@@ -25,11 +25,13 @@
 // lets two MMAs share each X tile, so a k-block moves 64 KB of operands for the
 // work that takes 96 KB with MT = 1 -- the operand feed, not the tensor pipe, is
 // what limits this kernel (the MMA sequence alone runs at full rate).  With S > 1
-// splits each unit writes its partial tiles to a workspace, and for every 32-row
-// quarter of a 128-row tile the last of the S units to finish (an atomic counter
-// per quarter) sums the S partials in split order 0..S-1 and writes Y -- so the
-// result does not depend on which unit finishes last.  MT and S come from a model
-// of the predicted time (waves x per-unit time, calibrated by measurements).
+// splits each unit writes its partial tiles to a workspace (small enough to stay in
+// L2 on the shapes that split), and k_splitk_reduce, launched right behind with
+// programmatic dependent launch, sums the S partials of every element in split
+// order 0..S-1 across the whole GPU -- so the result does not depend on which unit
+// finished last, and the reduction runs with every SM's memory parallelism instead
+// of in the tail of a few units.  MT and S come from a model of the predicted time
+// (waves x per-unit time + the reduction, calibrated by measurements).
 //
 // Out-of-range rows, columns and the k % 64 end are zero-filled by TMA and add
 // +0 exactly.  Every mbarrier wait is bounded by the global timer; on a
@@ -63,8 +65,7 @@ constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;  // 2 s
 
 struct GemmParams {
     float *Y;
-    float *ws;                // partial tiles, [unit][BN][128] (split count > 1 only)
-    unsigned int *counters;   // one per 32-row quarter of each output tile (split count > 1 only)
+    float *ws;                // partial tiles, [tile][split][BN][128] (split count > 1 only)
     int rows, ncols, k;
     int num_kb;               // ceil(k / 64)
     int bn;                   // tile columns (MMA N), multiple of 16, <= 256
@@ -330,46 +331,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) dev::mbar_arrive(smem_u32(&acc_empty[b]));
-
-            if (p.splits > 1) {
-                // the last of the S units of each tile quarter sums the partials in split order
-                __threadfence();
-                __syncwarp();
-                for (int m = 0; m < MT; m++) {
-                    const int row = x.m0 + m * kBM + rloc;
-                    const int tile = x.tile0 + m * p.nt;
-                    unsigned old = 0;
-                    if (lane == 0) old = atomicAdd(&p.counters[tile * 4 + quarter], 1u);
-                    old = __shfl_sync(0xffffffffu, old, 0);
-                    if (old != (unsigned)(p.splits - 1)) continue;
-                    __threadfence();
-                    const float *ws_row = p.ws + (size_t)tile * p.splits * (size_t)p.bn * kBM + rloc;
-                    if (row < p.rows) {
-                        // 32 columns per trip, all of a split's loads in flight at once;
-                        // the sum starts from split 0 and adds the others in order
-                        for (int c0 = 0; c0 < p.bn; c0 += 32) {
-                            float acc[32];
-#pragma unroll
-                            for (int q = 0; q < 32; q++)
-                                acc[q] = (c0 + q < p.bn) ? __ldcg(ws_row + (size_t)(c0 + q) * kBM) : 0.0f;
-                            for (int s = 1; s < p.splits; s++) {
-                                float v[32];
-#pragma unroll
-                                for (int q = 0; q < 32; q++)
-                                    v[q] = (c0 + q < p.bn) ? __ldcg(ws_row + ((size_t)s * p.bn + c0 + q) * kBM) : 0.0f;
-#pragma unroll
-                                for (int q = 0; q < 32; q++) acc[q] += v[q];
-                            }
-#pragma unroll
-                            for (int q = 0; q < 32; q++) {
-                                const int col = x.n0 + c0 + q;
-                                if (c0 + q < p.bn && col < p.ncols) p.Y[(size_t)col * p.rows + row] = acc[q];
-                            }
-                        }
-                    }
-                    if (lane == 0) p.counters[tile * 4 + quarter] = 0;  // ready for the next launch
-                }
-            }
         }
     }
 
@@ -393,6 +354,47 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(tmem_cols)
                      : "memory");
+    }
+}
+
+// Split-k reduction: Y[col * rows + row] = sum of the S partials in order 0..S-1,
+// where the partial of split s for (row, col) lies at
+// ws[((tile * S + s) * bn + col % bn) * 128 + row % 128], tile = (row / 128) * nt + col / bn.
+// Each thread takes four consecutive rows of one column (rows % 4 == 0 on this path),
+// 16-byte loads from every split in flight before the adds; vec4 says Y is 16-byte
+// aligned, else the four results are stored one by one.
+constexpr int kReduceThreads = 256;
+
+__global__ void __launch_bounds__(kReduceThreads) k_splitk_reduce(const float *__restrict__ ws, float *__restrict__ Y,
+                                                                  int rows, int ncols, int bn, int nt, int S, int vec4)
+{
+    dev::pdl_wait();  // the partials are the previous kernel's output
+    const int rows4 = rows >> 2;
+    const int64_t total = (int64_t)rows4 * ncols;
+    for (int64_t e = (int64_t)blockIdx.x * kReduceThreads + threadIdx.x; e < total;
+         e += (int64_t)gridDim.x * kReduceThreads) {
+        const int col = (int)(e / rows4), row = (int)(e - (int64_t)col * rows4) * 4;
+        const int tile = (row >> 7) * nt + col / bn;
+        const float4 *src =
+            reinterpret_cast<const float4 *>(ws + (((size_t)tile * S) * bn + col % bn) * kBM + (row & (kBM - 1)));
+        const size_t split_stride = (size_t)bn * kBM / 4;  // in float4
+        float4 acc = __ldcg(src);
+        for (int sp = 1; sp < S; sp++) {
+            const float4 v = __ldcg(src + sp * split_stride);
+            acc.x += v.x;
+            acc.y += v.y;
+            acc.z += v.z;
+            acc.w += v.w;
+        }
+        float *dst = Y + (size_t)col * rows + row;
+        if (vec4) {
+            *reinterpret_cast<float4 *>(dst) = acc;
+        } else {
+            dst[0] = acc.x;
+            dst[1] = acc.y;
+            dst[2] = acc.z;
+            dst[3] = acc.w;
+        }
     }
 }
 
@@ -434,23 +436,25 @@ int pow2_at_least(int v)
     return p;
 }
 
-// Cost of a plan in k-blocks of its own unit height: waves x (k-blocks per unit + the
-// cost of splitting).  A k-split costs the partial tiles' write and ordered re-read,
-// the serial reduction by the last unit of each tile and the counter reset: measured
-// on the Llama shapes at 512 columns (gate: 2 waves unsplit beat 3 waves of half-k
-// units by 20 %; down: one wave of half-k units beat 42 % of the SMs unsplit by 28 %),
-// about 8 + 30 * MT * BN/256 k-blocks.
-double plan_kblocks(int64_t tiles, int num_kb, int bn, int mt, int s, int ctas)
-{
-    const double split = 8.0 + 30.0 * mt * bn / 256.0;
-    const double waves = std::ceil((double)tiles * s / ctas);
-    return waves * ((double)num_kb / s + (s > 1 ? split : 0.0));
-}
-
 // Measured time of one k-block with 256-column tiles: 0.45 us for a 128-row unit,
 // 0.80 us for a 256-row unit (twice the work, two thirds of the operand bytes per
 // unit of work).
 constexpr double kKblockUs[3] = {0.0, 0.45, 0.80};
+// The split-k reduction: a dependent launch, then one pass over the partials and Y.
+constexpr double kReduceFixedUs = 2.0;
+constexpr double kReduceBytesPerUs = 6.0e6;
+
+// Predicted time of a plan in microseconds: waves x (k-blocks per unit x the time of
+// a k-block), plus, with S > 1, the reduction kernel.
+double plan_us(int64_t units_per_split, int64_t tiles128, int num_kb, int bn, int mt, int s, int ctas, int64_t rows,
+               int64_t ncols)
+{
+    const double waves = std::ceil((double)units_per_split * s / ctas);
+    double us = waves * std::ceil((double)num_kb / s) * kKblockUs[mt];
+    if (s > 1)
+        us += kReduceFixedUs + ((double)tiles128 * s * bn * kBM * 4.0 + (double)rows * ncols * 4.0) / kReduceBytesPerUs;
+    return us;
+}
 
 constexpr int kMaxDevices = 64;
 std::once_flag g_attr_once[kMaxDevices][2];
@@ -482,7 +486,7 @@ struct Plan {
     int mt_per_unit;  // MT: 128-row tiles per work unit (1 or 2)
     int grid;
     size_t smem;
-    size_t ws_bytes, counter_bytes;
+    size_t ws_bytes;
 };
 
 int plan_gemm(Plan *pl, int64_t rows, int64_t k, int64_t ncols, const DeviceInfo &dev, bool allow_split,
@@ -508,22 +512,16 @@ int plan_gemm(Plan *pl, int64_t rows, int64_t k, int64_t ncols, const DeviceInfo
     // with full 256-column tiles, where they were measured.
     int mt_unit = 1, splits = 1;
     double best_us = 1e300;
+    const int64_t tiles128 = (int64_t)p.mt * p.nt;
     for (int mt = 1; mt <= (allow_mt2 && p.mt >= 2 && p.bn == 256 ? 2 : 1); mt++) {
         const int64_t tiles = (int64_t)((p.mt + mt - 1) / mt) * p.nt;
-        int best_s = 1;
-        double best_kb = 1e300;
         for (int sp = 1; sp <= (allow_split ? std::min(kMaxSplits, p.num_kb) : 1); sp++) {
-            const double c = plan_kblocks(tiles, p.num_kb, p.bn, mt, sp, dev.sm_count);
-            if (c < best_kb - 1e-9) {
-                best_kb = c;
-                best_s = sp;
+            const double us = plan_us(tiles, tiles128, p.num_kb, p.bn, mt, sp, dev.sm_count, rows, ncols);
+            if (us < best_us - 1e-9) {
+                best_us = us;
+                mt_unit = mt;
+                splits = sp;
             }
-        }
-        const double us = best_kb * kKblockUs[mt];
-        if (us < best_us - 1e-9) {
-            best_us = us;
-            mt_unit = mt;
-            splits = best_s;
         }
     }
     pl->mt_per_unit = mt_unit;
@@ -542,10 +540,9 @@ int plan_gemm(Plan *pl, int64_t rows, int64_t k, int64_t ncols, const DeviceInfo
     const size_t smem = (size_t)p.stages * stage_bytes + 1024;
     const size_t one_per_sm = (size_t)dev.max_smem_optin / 2 + 4096;
     pl->smem = std::max(smem, one_per_sm);
-    // split-k bookkeeping is per 128-row tile
-    const size_t tiles128 = (size_t)tiles * mt_unit;
-    pl->ws_bytes = p.splits > 1 ? tiles128 * p.splits * p.bn * kBM * sizeof(float) : 0;
-    pl->counter_bytes = p.splits > 1 ? tiles128 * 4 * sizeof(unsigned int) : 0;
+    // partial tiles of 128 rows, including a unit's second tile past the last row
+    const size_t ws_tiles = (size_t)tiles * mt_unit;
+    pl->ws_bytes = p.splits > 1 ? ws_tiles * p.splits * p.bn * kBM * sizeof(float) : 0;
     return BM_OK;
 }
 
@@ -563,13 +560,40 @@ int launch_mt(const Plan &pl, const CUtensorMap &mw, const CUtensorMap &mx, cuda
     return BM_OK;
 }
 
+// The split-k reduction right behind the product on the same stream, with
+// programmatic dependent launch so its launch overlaps the product's tail; it waits
+// (griddepcontrol.wait) for the product before it reads the partials.
+int launch_reduce(const Plan &pl, cudaStream_t s, const DeviceInfo &dev)
+{
+    const int64_t total = (int64_t)(pl.p.rows / 4) * pl.p.ncols;
+    int64_t blocks = (total + kReduceThreads - 1) / kReduceThreads;
+    blocks = std::max<int64_t>(1, std::min<int64_t>(blocks, (int64_t)dev.sm_count * 8));
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(kReduceThreads);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const int vec4 = (reinterpret_cast<uintptr_t>(pl.p.Y) & 15) == 0 ? 1 : 0;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, k_splitk_reduce, (const float *)pl.p.ws, pl.p.Y, pl.p.rows, pl.p.ncols,
+                                       pl.p.bn, pl.p.nt, pl.p.splits, vec4);
+    if (e != cudaSuccess)
+        return fail(BM_ERR_CUDA, "tensor-core product: reduction launch failed: %s", cudaGetErrorString(e));
+    return BM_OK;
+}
+
 int launch_plan(const Plan &pl, const uint16_t *W, const uint16_t *X, cudaStream_t s, const DeviceInfo &dev)
 {
     if (!get_encoder()) return fail(BM_ERR_CUDA, "tensor-core product: cuTensorMapEncodeTiled unavailable");
     CUtensorMap mw, mx;
     if (!make_map(&mw, W, pl.p.rows, pl.p.k, kBM * pl.mt_per_unit) || !make_map(&mx, X, pl.p.ncols, pl.p.k, pl.p.bn))
         return fail(BM_ERR_CUDA, "tensor-core product: tensor map encoding failed");
-    return pl.mt_per_unit == 2 ? launch_mt<2>(pl, mw, mx, s, dev) : launch_mt<1>(pl, mw, mx, s, dev);
+    const int st = pl.mt_per_unit == 2 ? launch_mt<2>(pl, mw, mx, s, dev) : launch_mt<1>(pl, mw, mx, s, dev);
+    if (st != BM_OK || pl.p.splits == 1) return st;
+    return launch_reduce(pl, s, dev);
 }
 
 }  // namespace
@@ -587,22 +611,19 @@ int launch_gemm_tc(const uint16_t *W, int64_t rows, int64_t k, const uint16_t *X
     pl.p.timeout_ns = kDefaultTimeoutNs;
     if (pl.p.splits == 1) return launch_plan(pl, W, X, s, dev);
 
-    // Split-k workspace: partial tiles and per-quarter counters, stream-ordered (so
-    // concurrent products on other streams never share it, and graph capture
-    // records it as an allocation node).  The counters start at zero.
+    // Split-k workspace for the partial tiles, stream-ordered (so concurrent products
+    // on other streams never share it, and graph capture records it as an allocation
+    // node).
     int dev_id = 0;
     cudaGetDevice(&dev_id);
     cudaMemPool_t pool = workspace_pool(dev_id & (kMaxDevices - 1));
     if (!pool) return fail(BM_ERR_CUDA, "tensor-core product: workspace pool unavailable");
     void *ws = nullptr;
-    cudaError_t e = cudaMallocFromPoolAsync(&ws, pl.ws_bytes + pl.counter_bytes, pool, s);
+    cudaError_t e = cudaMallocFromPoolAsync(&ws, pl.ws_bytes, pool, s);
     if (e != cudaSuccess)
         return fail(BM_ERR_CUDA, "tensor-core product: workspace allocation failed: %s", cudaGetErrorString(e));
     pl.p.ws = static_cast<float *>(ws);
-    pl.p.counters = reinterpret_cast<unsigned int *>(static_cast<char *>(ws) + pl.ws_bytes);
-    e = cudaMemsetAsync(pl.p.counters, 0, pl.counter_bytes, s);
-    st = e == cudaSuccess ? launch_plan(pl, W, X, s, dev)
-                          : fail(BM_ERR_CUDA, "tensor-core product: counter reset failed: %s", cudaGetErrorString(e));
+    st = launch_plan(pl, W, X, s, dev);
     cudaError_t e2 = cudaFreeAsync(ws, s);
     if (st == BM_OK && e2 != cudaSuccess)
         return fail(BM_ERR_CUDA, "tensor-core product: workspace release failed: %s", cudaGetErrorString(e2));
@@ -633,7 +654,7 @@ int launch_gemm_tc_noalloc(const uint16_t *W, int64_t rows, int64_t k, const uin
     Plan pl;
     int st = plan_gemm(&pl, rows, k, ncols, dev, true, true);
     if (st != BM_OK) return st;
-    const size_t need = pl.ws_bytes + pl.counter_bytes;
+    const size_t need = pl.ws_bytes;
     if (need > kNoAllocScratchBytes)
         return fail(BM_ERR_INVALID_ARG,
                     "bm_f16_matmul_noalloc: this product needs %zu bytes of split-k scratch; the static scratch "
@@ -658,11 +679,6 @@ int launch_gemm_tc_noalloc(const uint16_t *W, int64_t rows, int64_t k, const uin
             return fail(BM_ERR_CUDA, "bm_f16_matmul_noalloc: scratch address lookup failed: %s",
                         cudaGetErrorString(g_scratch_status[d]));
         pl.p.ws = reinterpret_cast<float *>(g_scratch_ptr[d]);
-        pl.p.counters = reinterpret_cast<unsigned int *>(g_scratch_ptr[d] + pl.ws_bytes);
-        // the previous call leaves its contents behind: the counters must start at zero
-        cudaError_t e = cudaMemsetAsync(pl.p.counters, 0, pl.counter_bytes, s);
-        if (e != cudaSuccess)
-            return fail(BM_ERR_CUDA, "bm_f16_matmul_noalloc: counter reset failed: %s", cudaGetErrorString(e));
     }
     return launch_plan(pl, W, X, s, dev);
 }

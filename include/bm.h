@@ -201,6 +201,14 @@ int bm_f16_matmul_noalloc(const uint16_t *W, int64_t rows, int64_t k, const uint
  * E (f16[vocab][hidden]) with ncols normalised activations X (f16[ncols][hidden]),
  * Y[c*vocab + v].  It is one product over all columns, so its path follows
  * bm_takes_sgemm(vocab, hidden, ncols) exactly as bm_f16_matmul's does.
+ *
+ * Which rows to pass is the caller's rule (forward.md, "Why only the output rows
+ * leave the last layer"): on the last layer only the rows the engine outputs (its
+ * inp_out_ids: none, the last one, or all) go through the feed-forward products and
+ * the logits.  Pass exactly those rows, gathered into X, and nothing else: the
+ * column count picks the path, so the last row alone (one column, vec_dot) and the
+ * same row inside a product over all rows (tinyBLAS) give different bits, each
+ * matching the engine that makes the same choice.
  */
 int bm_f16_logits(const uint16_t *E, int64_t vocab, int64_t hidden, const uint16_t *X,
                   int64_t ncols, float *Y, bm_stream_t stream);

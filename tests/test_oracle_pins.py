@@ -279,3 +279,22 @@ def test_thread_count_does_not_change_bits():
                            cwd=os.path.dirname(os.path.dirname(GOLDEN)), check=True)
         outs.add(r.stdout.strip())
     assert len(outs) == 1
+
+
+def test_output_rows_choose_the_path():
+    """forward.md, "Why only the output rows leave the last layer": the last layer's
+    products see only the output rows, so their count picks the path.  Over an FFN
+    shape (1536 x 576), the last row alone takes vec_dot and the same row among 7
+    takes sgemm_dot -- each element checked against the per-element reference of
+    its path, and the two differ in some elements."""
+    rows, k, n = 1536, 576, 7
+    W = synth.normal_f16(0, "outids.gate", 0.02, (rows, k))
+    X = oracle.to_f16(synth.normal_f32(0, "outids.x", 1.0, (n, k)))
+    assert oracle.takes_sgemm(rows, k, n) and not oracle.takes_sgemm(rows, k, 1)
+    all_rows = oracle.matmul(W, X)[n - 1]
+    last_only = oracle.matmul(W, X[n - 1:])[0]
+    for r in range(0, rows, 97):
+        assert f32_bits(all_rows[r]) == f32_bits(oracle.sgemm_dot_ref(W[r], X[n - 1]))
+        assert f32_bits(last_only[r]) == f32_bits(oracle.vec_dot_ref(W[r], X[n - 1]))
+    differ = np.count_nonzero(all_rows.view(np.uint32) != last_only.view(np.uint32))
+    assert 0 < differ < rows
