@@ -15,12 +15,17 @@
 //                      k-block into the unit's MT accumulators; tcgen05.commit
 //                      frees the stage, and after a unit's last k-block signals
 //                      the epilogue.  Warp 1 also owns the TMEM allocation.
-//   warps 2..5       : epilogue.  tcgen05.ld (32 lanes x 32 columns per trip)
-//                      then coalesced f32 stores: a column of a tile is a
-//                      contiguous run of rows in Y.  The accumulators are handed
-//                      back to the MMA warp as soon as they have been read; when
-//                      TMEM holds two sets (MT * BN <= 256) the epilogue of one
-//                      unit overlaps the MMAs of the next.
+//   warps 2..9       : epilogue, two warps per TMEM lane quarter (warp % 4),
+//                      each taking every other 32-column chunk.  tcgen05.ld of
+//                      the next chunk is in flight while the current chunk's
+//                      coalesced f32 stores go out (a column of a tile is a
+//                      contiguous run of rows in Y).  A 256 x 256 unit's
+//                      epilogue takes about 6 us either way: when every CTA
+//                      writes its tiles at once the stores run at HBM write
+//                      speed.  The accumulators are handed back to the MMA warp
+//                      once they have been read; when TMEM holds two sets
+//                      (MT * BN <= 256) the epilogue of one unit overlaps the
+//                      MMAs of the next.
 // Work units are (row unit of MT tiles of 128 rows, column tile, k-split).  MT = 2
 // lets two MMAs share each X tile, so a k-block moves 64 KB of operands for the
 // work that takes 96 KB with MT = 1 -- the operand feed, not the tensor pipe, is
@@ -56,7 +61,7 @@ namespace {
 constexpr int kBM = 128;          // tile rows (MMA M)
 constexpr int kBK = 64;           // k per stage: one 128-byte swizzle row of f16
 constexpr int kUmmaK = 16;        // k per tcgen05.mma of kind::f16
-constexpr int kEpiWarps = 4;
+constexpr int kEpiWarps = 8;  // two per TMEM lane quarter, splitting the columns
 constexpr int kThreads = 32 * (2 + kEpiWarps);
 constexpr int kTileABytes = kBM * kBK * 2;  // 16 KB
 constexpr int kMaxStages = 8;
@@ -140,6 +145,7 @@ __device__ __forceinline__ void mma_commit(uint32_t bar)
 }
 
 // 32 consecutive accumulator columns of this thread's TMEM lane.
+// 32 lanes x 32 columns of TMEM into v; the values may be used only after tmem_wait_ld.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32])
 {
     asm volatile(
@@ -150,7 +156,19 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32])
           "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]),
           "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
         : "r"(taddr));
+}
+
+// Waits for this thread's TMEM loads; the empty asm makes every later use of v depend
+// on the wait, so no read of v is scheduled before the data has arrived.
+__device__ __forceinline__ void tmem_wait_ld(uint32_t (&v)[32])
+{
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+    asm volatile(""
+                 : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]), "+r"(v[6]), "+r"(v[7]),
+                   "+r"(v[8]), "+r"(v[9]), "+r"(v[10]), "+r"(v[11]), "+r"(v[12]), "+r"(v[13]), "+r"(v[14]),
+                   "+r"(v[15]), "+r"(v[16]), "+r"(v[17]), "+r"(v[18]), "+r"(v[19]), "+r"(v[20]), "+r"(v[21]),
+                   "+r"(v[22]), "+r"(v[23]), "+r"(v[24]), "+r"(v[25]), "+r"(v[26]), "+r"(v[27]), "+r"(v[28]),
+                   "+r"(v[29]), "+r"(v[30]), "+r"(v[31]));
 }
 
 struct Unit {
@@ -297,6 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ---------------------------------------------------------------- epilogue
         const int quarter = warp & 3;                 // TMEM lanes 32*quarter .. +31 (warp % 4 rule)
+        const int half = (warp - 2) >> 2;             // this warp's 32-column chunks: 32 * (2j + half)
         const int rloc = quarter * 32 + lane;         // row inside a 128-row tile
         int i = 0;
         for (int u = blockIdx.x; u < units; u += gridDim.x, i++) {
@@ -311,9 +330,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int row = x.m0 + m * kBM + rloc;
                 const int tile = x.tile0 + m * p.nt;
                 float *ws_unit = p.splits > 1 ? p.ws + ((size_t)tile * p.splits + x.s) * (size_t)p.bn * kBM : nullptr;
-                for (int c = 0; c < p.bn; c += 32) {
-                    uint32_t v[32];
-                    tmem_ld32(taddr + (uint32_t)c, v);
+                // one chunk's 32 values of this row: to the split's partial tile, or to Y
+                auto store = [&](const uint32_t(&v)[32], int c) {
                     if (p.splits > 1) {
 #pragma unroll
                         for (int q = 0; q < 32; q++)
@@ -324,6 +342,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const int col = x.n0 + c + q;
                             if (c + q < p.bn && col < p.ncols) p.Y[(size_t)col * p.rows + row] = __uint_as_float(v[q]);
                         }
+                    }
+                };
+                // two chunks in flight: the next chunk's TMEM load overlaps this chunk's stores
+                const int nch = (p.bn / 32 - half + 1) / 2 + ((p.bn % 32) && (p.bn / 32) % 2 == half ? 1 : 0);
+                uint32_t va[32], vb[32];
+                if (nch > 0) {
+                    tmem_ld32(taddr + (uint32_t)(32 * half), va);
+                    tmem_wait_ld(va);
+                }
+                for (int j = 0; j < nch; j += 2) {
+                    const int ca = 32 * (2 * j + half), cb = ca + 64;
+                    if (j + 1 < nch) tmem_ld32(taddr + (uint32_t)cb, vb);
+                    store(va, ca);
+                    if (j + 1 < nch) {
+                        tmem_wait_ld(vb);
+                        if (j + 2 < nch) tmem_ld32(taddr + (uint32_t)(cb + 64), va);
+                        store(vb, cb);
+                        if (j + 2 < nch) tmem_wait_ld(va);
                     }
                 }
             }
