@@ -19,6 +19,9 @@ Extra objects in the same JSON line:
                   logits fused into those products (bm_f16_matvec_norm)
   products     -- single products of the Llama-3-8B / Qwen3-0.6B shapes:
                   decode GB/s and 512-column tensor-core TFLOP/s
+  llama3_8b_decode_step / llama3_8b_prefill_layer -- a whole Llama-3-8B-shaped
+                  decode step (129 products), and one layer's 7 products for a
+                  512-token prefill micro-batch (with and without PDL)
   e2e          -- the same step through the Python binding, eagerly, with the
                   step's activations copied from pinned host memory and the logits
                   copied back every step
@@ -334,6 +337,7 @@ def run_gpu(args, rank, world, local_rank):
     if rank == 0 and not args.no_products:
         result["products"] = bench_products(bm, dev, stream, torch)
         result["llama3_8b_decode_step"] = bench_llama_decode(bm, dev, stream, torch)
+        result["llama3_8b_prefill_layer"] = bench_llama_prefill(bm, dev, stream, torch)
     return result
 
 
@@ -482,6 +486,45 @@ def bench_llama_decode(bm, dev, stream, torch, steps=10):
                                 "GB_s": round((nbytes + 4 * hid * (2 * layers + 1)) / ms_norm / 1e6, 1),
                                 "how": "bm_f16_matvec_norm for Q/K/V, gate/up and the output product"}}
     del lw, out_w, base, norms
+    return res
+
+
+def bench_llama_prefill(bm, dev, stream, torch, reps=10):
+    """A Llama-3-8B-shaped prefill micro-batch of 512 tokens through one layer's products:
+    the rounding of the normed activations, Q/K/V/O (4096, 1024, 1024, 4096 rows x 4096),
+    gate and up (14336 x 4096), the rounding of the FFN activation and down (4096 x 14336):
+    7 tensor-core products and 2 rounding kernels per step (plus a reduction after each
+    product that splits k), one CUDA graph, with and without programmatic dependent launch.
+    The layer's 436 MB of weights exceed L2, so replays stream them from HBM."""
+    hid, ffn, kv, n = 4096, 14336, 1024, 512
+    shapes = [("q", hid, hid), ("k", kv, hid), ("v", kv, hid), ("o", hid, hid), ("gate", ffn, hid),
+              ("up", ffn, hid), ("down", hid, ffn)]
+    W = {nm: torch.from_numpy(synth.normal_f16(SEED, "llama3_8b." + nm, 0.01, (r, c)).view(np.float16)).to(dev)
+         for nm, r, c in shapes}
+    x = torch.from_numpy(synth.normal_f32(SEED, "llama3_8b.prefill_x", 1.0, (n, hid))).to(dev)
+    h = torch.empty((n, hid), dtype=torch.float16, device=dev)
+    Y = {nm: torch.empty((n, r), dtype=torch.float32, device=dev) for nm, r, _ in shapes}
+    hd = torch.empty((n, ffn), dtype=torch.float16, device=dev)
+    flops = 2.0 * n * sum(r * c for _, r, c in shapes)
+
+    def step():
+        bm.bm_to_f16(x, h, stream=stream)
+        for nm in ("q", "k", "v", "o", "gate", "up"):
+            bm.bm_f16_matmul(W[nm], h, Y=Y[nm], stream=stream)
+        bm.bm_to_f16(Y["gate"], hd, stream=stream)
+        bm.bm_f16_matmul(W["down"], hd, Y=Y["down"], stream=stream)
+
+    old = bm.bm_set_pdl(False)
+    try:
+        ms_plain = graph_time(torch, stream, step, reps=reps)
+        bm.bm_set_pdl(True)
+        ms_pdl = graph_time(torch, stream, step, reps=reps)
+    finally:
+        bm.bm_set_pdl(old)
+    res = {"tokens": n, "ms_per_step": round(ms_pdl, 4), "TFLOP_s": round(flops / ms_pdl / 1e9, 1),
+           "ms_per_step_without_pdl": round(ms_plain, 4), "TFLOP_s_without_pdl": round(flops / ms_plain / 1e9, 1),
+           "how": "one layer's 7 products at 512 columns plus 2 rounding kernels, CUDA graph, PDL on / off"}
+    del W, Y
     return res
 
 
@@ -675,6 +718,10 @@ def main():
     if "llama3_8b_decode_step" in r:
         r["llama3_8b_decode_step"]["pct_hbm"] = round(100.0 * r["llama3_8b_decode_step"]["GB_s"] / hbm_peak, 1)
         line["llama3_8b_decode_step"] = r["llama3_8b_decode_step"]
+    if "llama3_8b_prefill_layer" in r:
+        pf = r["llama3_8b_prefill_layer"]
+        pf["pct_bf16_dense_peak"] = round(100.0 * pf["TFLOP_s"] / float(peaks.get("bf16_tflops", 1900.0)), 1)
+        line["llama3_8b_prefill_layer"] = pf
     if "products" in r:
         line["products"] = r["products"]
         for p in r["products"]:

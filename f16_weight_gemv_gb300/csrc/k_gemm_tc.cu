@@ -249,12 +249,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = tmem_base_slot;
+    dev::pdl_trigger();  // the next kernel may start its own set-up and weight loads
 
     if (warp == 0) {
         // ---------------------------------------------------------------- TMA producer
         if (lane == 0) {
+            // Under programmatic dependent launch the weights (constants) of the first
+            // ring's worth of stages are requested before griddepcontrol.wait; the
+            // activation tiles (the previous kernel's output) only after it.
             int t = 0;
-            bool ok = true;
+            bool ok = true, waited = false;
+            int pend = 0;  // stages that hold their W copy, X still to come
+            int pend_s[kMaxStages], pend_kb[kMaxStages], pend_n0[kMaxStages];
+            auto issue_pending_x = [&]() {
+                dev::pdl_wait();
+                waited = true;
+                for (int q = 0; q < pend; q++)
+                    tma_load_2d(ring_u32 + (uint32_t)pend_s[q] * stage_bytes + MT * kTileABytes, &map_x,
+                                pend_kb[q] * kBK, pend_n0[q], smem_u32(&full_bar[pend_s[q]]));
+                pend = 0;
+            };
             for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
                 const Unit x = unit_of<MT>(p, u);
                 for (int kb = x.kb0; kb < x.kb1; kb++, t++) {
@@ -269,10 +283,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t fb = smem_u32(&full_bar[s]);
                     mbar_expect_tx(fb, stage_bytes);
                     tma_load_2d(a_dst, &map_w, kb * kBK, x.m0, fb);  // MT * 128 rows in one box
-                    tma_load_2d(a_dst + MT * kTileABytes, &map_x, kb * kBK, x.n0, fb);
+                    if (waited) {
+                        tma_load_2d(a_dst + MT * kTileABytes, &map_x, kb * kBK, x.n0, fb);
+                    } else {  // t < stages here, so at most kMaxStages stages wait for X
+                        pend_s[pend] = s;
+                        pend_kb[pend] = kb;
+                        pend_n0[pend] = x.n0;
+                        pend++;
+                        if (t + 1 == p.stages) issue_pending_x();
+                    }
                     issued_slot = t + 1;
                 }
             }
+            if (!waited) issue_pending_x();  // fewer k-blocks than stages, or a give-up: complete every stage
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -590,8 +613,17 @@ int launch_mt(const Plan &pl, const CUtensorMap &mw, const CUtensorMap &mx, cuda
     std::call_once(g_attr_once[dev_id & (kMaxDevices - 1)][MT - 1], [&] {
         cudaFuncSetAttribute(k_gemm_tc<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, dev.max_smem_optin - 1024);
     });
-    k_gemm_tc<MT><<<pl.grid, kThreads, pl.smem, s>>>(mw, mx, pl.p);
-    cudaError_t e = cudaGetLastError();
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)pl.grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = pl.smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_enabled() ? 1 : 0;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, k_gemm_tc<MT>, mw, mx, pl.p);
     if (e != cudaSuccess) return fail(BM_ERR_CUDA, "tensor-core product: launch failed: %s", cudaGetErrorString(e));
     return BM_OK;
 }

@@ -231,14 +231,16 @@ int bm_takes_sgemm(int64_t rows, int64_t k, int64_t ncols);
 
 /*
  * Programmatic dependent launch for the products (default off; process-wide).
- * When on, a product of one column with k % 8 == 0, or a bm_takes_sgemm product
- * on the bit-exact kernel (bm_set_exact_sgemm_cols), is launched so that it may start before the kernel ahead
- * of it on the stream has finished: it begins copying its weight matrix into
- * shared memory at once and waits for that kernel only before it reads its
- * activation and writes its output.  Precondition while on: the
- * kernel immediately ahead of a product on its stream must not write that
- * product's weight matrix (weights are constants in a forward pass).  Results
- * are identical either way.  Returns the previous setting.
+ * When on, a product of one column with k % 8 == 0, a bm_takes_sgemm product on
+ * the bit-exact kernel (bm_set_exact_sgemm_cols) or on the tensor cores, and the
+ * norm and embedding kernels are launched so that they may start before the
+ * kernel ahead of them on the stream has finished: a product sets up and begins
+ * copying its weight matrix (and bm_f16_matvec_norm its norm weight) into the
+ * chip at once, and waits for that kernel only before it reads its activation
+ * and writes its output.  Precondition while on: the kernel immediately ahead of
+ * a product on its stream must not write that product's weight matrix or norm
+ * weight (they are constants in a forward pass).  Results are identical either
+ * way.  Returns the previous setting.
  */
 int bm_set_pdl(int enable);
 

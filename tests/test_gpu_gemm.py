@@ -184,3 +184,57 @@ def test_split_k_in_a_cuda_graph_and_concurrent_streams(bm):
     torch.cuda.synchronize()
     assert np.array_equal(bits32(Ya), ref_a)
     assert bm.bm_device_status() == 0
+
+
+@pytest.mark.parametrize("rows,k,ncols", [(4096, 4096, 512), (1536, 576, 64), (14336, 1024, 512), (1000, 8192, 40)])
+def test_pdl_prefill_chain_matches_plain_launches(bm, rows, k, ncols):
+    """A prefill-like chain -- rounding kernel, tensor-core product (split or not),
+    rounding of that product's output, a second product -- under programmatic
+    dependent launch, eagerly and replayed from a CUDA graph: the same bits as with
+    plain launches, and within the bound."""
+    import torch
+    W1 = to_dev(rnd_f16(130, (rows, k)))
+    W2 = to_dev(rnd_f16(131, (k, rows)))
+    xf = to_dev(synth.normal_f32(0, 132, 1.0, (ncols, k)))
+    h1 = torch.empty((ncols, k), dtype=torch.float16, device="cuda")
+    Y1 = torch.empty((ncols, rows), dtype=torch.float32, device="cuda")
+    h2 = torch.empty((ncols, rows), dtype=torch.float16, device="cuda")
+    Y2 = torch.empty((ncols, k), dtype=torch.float32, device="cuda")
+    s = torch.cuda.Stream()
+
+    def chain():
+        bm.bm_to_f16(xf, h1, stream=s)
+        bm.bm_f16_matmul(W1, h1, Y=Y1, stream=s)
+        bm.bm_to_f16(Y1, h2, stream=s)
+        bm.bm_f16_matmul(W2, h2, Y=Y2, stream=s)
+
+    old = bm.bm_set_pdl(False)
+    try:
+        with torch.cuda.stream(s):
+            chain()
+        torch.cuda.synchronize()
+        want1, want2 = bits32(Y1).copy(), bits32(Y2).copy()
+        bm.bm_set_pdl(True)
+        for Y in (Y1, Y2):
+            Y.fill_(float("nan"))
+        with torch.cuda.stream(s):
+            chain()
+        torch.cuda.synchronize()
+        assert np.array_equal(bits32(Y1), want1) and np.array_equal(bits32(Y2), want2)
+        for Y in (Y1, Y2):
+            Y.fill_(float("nan"))
+        g = torch.cuda.CUDAGraph()
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=s):
+            chain()
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(bits32(Y1), want1) and np.array_equal(bits32(Y2), want2)
+    finally:
+        bm.bm_set_pdl(old)
+    assert bm.bm_device_status() == 0
+    rng = np.random.default_rng(rows + ncols)
+    ri = rng.integers(0, rows, 2000)
+    ci = rng.integers(0, ncols, 2000)
+    check_within(Y1.cpu().numpy(), rnd_f16(130, (rows, k)), h1.cpu().numpy().view(np.uint16), sample=(ri, ci))
