@@ -514,17 +514,37 @@ def bench_llama_prefill(bm, dev, stream, torch, reps=10):
         bm.bm_to_f16(Y["gate"], hd, stream=stream)
         bm.bm_f16_matmul(W["down"], hd, Y=Y["down"], stream=stream)
 
+    # The same layer with Q/K/V and gate/up stored as one matrix each ([6144][4096] and
+    # [28672][4096]): two products instead of five.  Every element is still its own row's
+    # product (the path follows the concatenated shape, which takes_sgemm the same way),
+    # and a caller reads Q, K, V (or gate, up) as row ranges of each output column.
+    Wqkv = torch.cat([W["q"], W["k"], W["v"]], 0)
+    Wgu = torch.cat([W["gate"], W["up"]], 0)
+    Yqkv = torch.empty((n, Wqkv.shape[0]), dtype=torch.float32, device=dev)
+    Ygu = torch.empty((n, Wgu.shape[0]), dtype=torch.float32, device=dev)
+
+    def step_fused():
+        bm.bm_to_f16(x, h, stream=stream)
+        bm.bm_f16_matmul(Wqkv, h, Y=Yqkv, stream=stream)
+        bm.bm_f16_matmul(W["o"], h, Y=Y["o"], stream=stream)
+        bm.bm_f16_matmul(Wgu, h, Y=Ygu, stream=stream)
+        bm.bm_to_f16(Y["gate"], hd, stream=stream)  # stand-in FFN activation, same shape as in step()
+        bm.bm_f16_matmul(W["down"], hd, Y=Y["down"], stream=stream)
+
     old = bm.bm_set_pdl(False)
     try:
         ms_plain = graph_time(torch, stream, step, reps=reps)
         bm.bm_set_pdl(True)
         ms_pdl = graph_time(torch, stream, step, reps=reps)
+        ms_fused = graph_time(torch, stream, step_fused, reps=reps)
     finally:
         bm.bm_set_pdl(old)
     res = {"tokens": n, "ms_per_step": round(ms_pdl, 4), "TFLOP_s": round(flops / ms_pdl / 1e9, 1),
            "ms_per_step_without_pdl": round(ms_plain, 4), "TFLOP_s_without_pdl": round(flops / ms_plain / 1e9, 1),
-           "how": "one layer's 7 products at 512 columns plus 2 rounding kernels, CUDA graph, PDL on / off"}
-    del W, Y
+           "how": "one layer's 7 products at 512 columns plus 2 rounding kernels, CUDA graph, PDL on / off",
+           "concatenated_weights": {"ms_per_step": round(ms_fused, 4), "TFLOP_s": round(flops / ms_fused / 1e9, 1),
+                                    "how": "Q/K/V and gate/up each stored as one matrix: 4 products, PDL on"}}
+    del W, Y, Wqkv, Wgu, Yqkv, Ygu
     return res
 
 
@@ -629,10 +649,42 @@ def run_single(spec: str, reps: int):
     return 0
 
 
+def run_prefill(reps: int):
+    """The Llama-3-8B-shaped prefill layer (bench_llama_prefill), eagerly, `reps` times with
+    programmatic dependent launch on (for profilers; prints nothing timed)."""
+    import torch
+
+    import __graft_entry__
+    import f16_weight_gemv_gb300 as bm
+
+    __graft_entry__.build()
+    dev = torch.device("cuda", 0)
+    hid, ffn, kv, n = 4096, 14336, 1024, 512
+    shapes = [("q", hid, hid), ("k", kv, hid), ("v", kv, hid), ("o", hid, hid), ("gate", ffn, hid),
+              ("up", ffn, hid), ("down", hid, ffn)]
+    W = {nm: torch.from_numpy(synth.normal_f16(SEED, "llama3_8b." + nm, 0.01, (r, c)).view(np.float16)).to(dev)
+         for nm, r, c in shapes}
+    x = torch.from_numpy(synth.normal_f32(SEED, "llama3_8b.prefill_x", 1.0, (n, hid))).to(dev)
+    h = torch.empty((n, hid), dtype=torch.float16, device=dev)
+    Y = {nm: torch.empty((n, r), dtype=torch.float32, device=dev) for nm, r, _ in shapes}
+    hd = torch.empty((n, ffn), dtype=torch.float16, device=dev)
+    bm.bm_set_pdl(True)
+    for _ in range(reps):
+        bm.bm_to_f16(x, h)
+        for nm in ("q", "k", "v", "o", "gate", "up"):
+            bm.bm_f16_matmul(W[nm], h, Y=Y[nm])
+        bm.bm_to_f16(Y["gate"], hd)
+        bm.bm_f16_matmul(W["down"], hd, Y=Y["down"])
+    torch.cuda.synchronize()
+    print(json.dumps({"prefill": "llama3_8b layer, 512 tokens", "reps": reps, "status": bm.bm_device_status()}))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--single", default=None, help="profile mode: run one product ROWSxKxNCOLS --reps times")
     ap.add_argument("--reps", type=int, default=3)
+    ap.add_argument("--prefill", action="store_true", help="profile mode: run the Llama-3-8B prefill layer --reps times")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=20)
@@ -647,6 +699,8 @@ def main():
         return run_reference(args)
     if args.single:
         return run_single(args.single, args.reps)
+    if args.prefill:
+        return run_prefill(args.reps)
 
     import torch
 

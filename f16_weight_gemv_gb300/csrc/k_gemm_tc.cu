@@ -419,9 +419,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 // Split-k reduction: Y[col * rows + row] = sum of the S partials in order 0..S-1,
 // where the partial of split s for (row, col) lies at
 // ws[((tile * S + s) * bn + col % bn) * 128 + row % 128], tile = (row / 128) * nt + col / bn.
-// Each thread takes four consecutive rows of one column (rows % 4 == 0 on this path),
-// 16-byte loads from every split in flight before the adds; vec4 says Y is 16-byte
-// aligned, else the four results are stored one by one.
+// Each thread takes four consecutive rows of one column (rows % 4 == 0 on this path)
+// and issues the 16-byte loads of every split before the first add (a loop bounded
+// only at run time left one round trip per split: 8 us for eight splits); vec4 says
+// Y is 16-byte aligned, else the four results are stored one by one.
 constexpr int kReduceThreads = 256;
 
 __global__ void __launch_bounds__(kReduceThreads) k_splitk_reduce(const float *__restrict__ ws, float *__restrict__ Y,
@@ -437,13 +438,19 @@ __global__ void __launch_bounds__(kReduceThreads) k_splitk_reduce(const float *_
         const float4 *src =
             reinterpret_cast<const float4 *>(ws + (((size_t)tile * S) * bn + col % bn) * kBM + (row & (kBM - 1)));
         const size_t split_stride = (size_t)bn * kBM / 4;  // in float4
-        float4 acc = __ldcg(src);
-        for (int sp = 1; sp < S; sp++) {
-            const float4 v = __ldcg(src + sp * split_stride);
-            acc.x += v.x;
-            acc.y += v.y;
-            acc.z += v.z;
-            acc.w += v.w;
+        float4 v[kMaxSplits];
+#pragma unroll
+        for (int sp = 0; sp < kMaxSplits; sp++)  // every split's load in flight before the first add
+            if (sp < S) v[sp] = __ldcg(src + sp * split_stride);
+        float4 acc = v[0];
+#pragma unroll
+        for (int sp = 1; sp < kMaxSplits; sp++) {
+            if (sp < S) {
+                acc.x += v[sp].x;
+                acc.y += v[sp].y;
+                acc.z += v[sp].z;
+                acc.w += v[sp].w;
+            }
         }
         float *dst = Y + (size_t)col * rows + row;
         if (vec4) {
