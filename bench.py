@@ -595,6 +595,17 @@ def cpu_baseline(budget_s=10.0):
                       "in %.1f s on the host" % (n, dt)}
 
 
+def step_config(world, no_pdl):
+    """The workload description both arms print (the reference arm runs it on the host)."""
+    return {"workload": "smollm2_135m_decode_step", "layers": LAYERS, "hidden": HIDDEN, "ffn": FFN,
+            "q_rows": Q_ROWS, "kv_rows": KV_ROWS, "vocab": VOCAB, "ncols": 1, "seed": SEED,
+            "weight_bytes": int(sum(2 * rows * op[2] for op in step_plan() if op[0] != "round"
+                                    for _, rows in op[1])),
+            "l2": "inputs larger than L2 (269 MB of weights per step, cyclic)",
+            "parallelism": "replicas" if world > 1 else "single GPU", "graph": "CUDA graph of the step",
+            "pdl": not no_pdl}
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -613,8 +624,7 @@ def run_reference(args):
         "value": round(value, 4), "unit": "GB/s", "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f16 weights, f32 accumulate", "data": "synthetic",
-        "config": {"workload": "smollm2_135m_decode_step", "layers": LAYERS, "hidden": HIDDEN, "ffn": FFN,
-                   "vocab": VOCAB, "ncols": 1, "seed": SEED, "l2": "inputs larger than L2 (269 MB)"},
+        "config": step_config(1, False),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
                          "sample": "%d full decode steps after %d warm-up" % (args.steps, args.warmup)},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -737,13 +747,7 @@ def main():
         "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(r["ms"], 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f16 weights and activations, f32 accumulate (vec_dot bits)", "data": "synthetic",
-        "config": {"workload": "smollm2_135m_decode_step", "layers": LAYERS, "hidden": HIDDEN, "ffn": FFN,
-                   "q_rows": Q_ROWS, "kv_rows": KV_ROWS, "vocab": VOCAB, "ncols": 1, "seed": SEED,
-                   "weight_bytes": int(sum(2 * rows * op[2] for op in step_plan() if op[0] != "round"
-                                           for _, rows in op[1])),
-                   "l2": "inputs larger than L2 (269 MB of weights per step, cyclic)",
-                   "parallelism": "replicas" if world > 1 else "single GPU", "graph": "CUDA graph of the step",
-                   "pdl": not args.no_pdl},
+        "config": step_config(world, args.no_pdl),
         "pct_of_hbm_peak": round(100.0 * value / world / hbm_peak, 2),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(achieved / hbm_peak, 4), "traffic": ncu_traffic(),
