@@ -338,6 +338,8 @@ def run_gpu(args, rank, world, local_rank):
         result["products"] = bench_products(bm, dev, stream, torch)
         result["llama3_8b_decode_step"] = bench_llama_decode(bm, dev, stream, torch)
         result["llama3_8b_prefill_layer"] = bench_llama_prefill(bm, dev, stream, torch)
+        result["qwen3_0.6b_decode_step"] = bench_qwen3_decode(bm, dev, stream, torch)
+        result["qwen3_0.6b_prefill_layer"] = bench_qwen3_prefill(bm, dev, stream, torch)
     return result
 
 
@@ -487,6 +489,81 @@ def bench_llama_decode(bm, dev, stream, torch, steps=10):
                                 "how": "bm_f16_matvec_norm for Q/K/V, gate/up and the output product"}}
     del lw, out_w, base, norms
     return res
+
+
+def bench_qwen3_decode(bm, dev, stream, torch, steps=10):
+    """A Qwen3-0.6B-shaped decode step: 28 layers of [fused Q/K/V (2048+1024+1024 x 1024),
+    O (1024 x 2048), fused gate/up (2 x 3072 x 1024), down (1024 x 3072)] then the tied
+    logits (151936 x 1024): 113 bm_f16_matvec_act calls over 1.19 GB of f16 weights
+    N(0, 0.02), one layer drawn and copied to 28 distinct buffers."""
+    hid, q, kv, ffn, vocab, layers = 1024, 2048, 1024, 3072, 151936, 28
+    base = {n: torch.from_numpy(synth.normal_f16(SEED, "qwen3." + n, 0.02, (r, c)).view(np.float16)).to(dev)
+            for n, r, c in [("q", q, hid), ("k", kv, hid), ("v", kv, hid), ("o", hid, q), ("gate", ffn, hid),
+                            ("up", ffn, hid), ("down", hid, ffn)]}
+    lw = [{n: (t if L == 0 else t.clone()) for n, t in base.items()} for L in range(layers)]
+    emb = torch.from_numpy(synth.normal_f16(SEED, "qwen3.embd", 0.02, (vocab, hid)).view(np.float16)).to(dev)
+    xa = torch.from_numpy(synth.normal_f32(SEED, "qwen3.act", 1.0, hid)).to(dev)
+    xo = torch.from_numpy(synth.normal_f32(SEED, "qwen3.act_o", 1.0, q)).to(dev)
+    xf = torch.from_numpy(synth.normal_f32(SEED, "qwen3.act_ffn", 1.0, ffn)).to(dev)
+    ys = {n: torch.empty(t.shape[0], dtype=torch.float32, device=dev) for n, t in base.items()}
+    logits = torch.empty(vocab, dtype=torch.float32, device=dev)
+    nbytes = 0
+    for n, t in base.items():
+        nbytes += layers * (2 * t.numel() + 4 * t.shape[0])
+    nbytes += layers * 4 * (hid + q + hid + ffn) + 2 * vocab * hid + 4 * vocab + 4 * hid
+
+    def step():
+        for L in range(layers):
+            w = lw[L]
+            bm.bm_f16_matvec_act([w["q"], w["k"], w["v"]], xa, [ys["q"], ys["k"], ys["v"]], stream=stream)
+            bm.bm_f16_matvec_act([w["o"]], xo, [ys["o"]], stream=stream)
+            bm.bm_f16_matvec_act([w["gate"], w["up"]], xa, [ys["gate"], ys["up"]], stream=stream)
+            bm.bm_f16_matvec_act([w["down"]], xf, [ys["down"]], stream=stream)
+        bm.bm_f16_matvec_act([emb], xa, [logits], stream=stream)
+
+    ms = graph_time(torch, stream, step, reps=steps)
+    res = {"ms_per_step": round(ms, 4), "GB_s": round(nbytes / ms / 1e6, 1), "weight_GB": round(
+        (sum(t.numel() for t in base.values()) * layers + emb.numel()) * 2 / 1e9, 3), "launches": 4 * layers + 1}
+    del lw, emb, base
+    return res
+
+
+def bench_qwen3_prefill(bm, dev, stream, torch, reps=10):
+    """A Qwen3-0.6B-shaped prefill micro-batch of 512 tokens through one layer's products,
+    with Q/K/V and gate/up stored as one matrix each ([4096][1024] and [6144][1024]), then
+    O (1024 x 2048) and down (1024 x 3072), plus the two roundings: one CUDA graph, PDL on.
+    One layer's weights (31 MB) sit in L2, so this measures the tensor path with hot weights."""
+    hid, q, kv, ffn, n = 1024, 2048, 1024, 3072, 512
+    Wqkv = torch.from_numpy(synth.normal_f16(SEED, "qwen3.qkv", 0.02, (q + 2 * kv, hid)).view(np.float16)).to(dev)
+    Wo = torch.from_numpy(synth.normal_f16(SEED, "qwen3.o", 0.02, (hid, q)).view(np.float16)).to(dev)
+    Wgu = torch.from_numpy(synth.normal_f16(SEED, "qwen3.gu", 0.02, (2 * ffn, hid)).view(np.float16)).to(dev)
+    Wd = torch.from_numpy(synth.normal_f16(SEED, "qwen3.down", 0.02, (hid, ffn)).view(np.float16)).to(dev)
+    x = torch.from_numpy(synth.normal_f32(SEED, "qwen3.prefill_x", 1.0, (n, hid))).to(dev)
+    xo = torch.from_numpy(synth.normal_f16(SEED, "qwen3.prefill_o", 1.0, (n, q)).view(np.float16)).to(dev)
+    xf = torch.from_numpy(synth.normal_f32(SEED, "qwen3.prefill_f", 1.0, (n, ffn))).to(dev)
+    h = torch.empty((n, hid), dtype=torch.float16, device=dev)
+    hf = torch.empty((n, ffn), dtype=torch.float16, device=dev)
+    Yqkv = torch.empty((n, q + 2 * kv), dtype=torch.float32, device=dev)
+    Yo = torch.empty((n, hid), dtype=torch.float32, device=dev)
+    Ygu = torch.empty((n, 2 * ffn), dtype=torch.float32, device=dev)
+    Yd = torch.empty((n, hid), dtype=torch.float32, device=dev)
+    flops = 2.0 * n * hid * (q + 2 * kv + q + 2 * ffn + ffn)
+
+    def step():
+        bm.bm_to_f16(x, h, stream=stream)
+        bm.bm_f16_matmul(Wqkv, h, Y=Yqkv, stream=stream)
+        bm.bm_f16_matmul(Wo, xo, Y=Yo, stream=stream)
+        bm.bm_f16_matmul(Wgu, h, Y=Ygu, stream=stream)
+        bm.bm_to_f16(xf, hf, stream=stream)
+        bm.bm_f16_matmul(Wd, hf, Y=Yd, stream=stream)
+
+    old = bm.bm_set_pdl(True)
+    try:
+        ms = graph_time(torch, stream, step, reps=reps)
+    finally:
+        bm.bm_set_pdl(old)
+    return {"tokens": n, "ms_per_step": round(ms, 4), "TFLOP_s": round(flops / ms / 1e9, 1),
+            "how": "one layer: Q/K/V and gate/up as one matrix each, O, down, 2 roundings; CUDA graph, PDL on"}
 
 
 def bench_llama_prefill(bm, dev, stream, torch, reps=10):
@@ -776,6 +853,13 @@ def main():
     if "llama3_8b_decode_step" in r:
         r["llama3_8b_decode_step"]["pct_hbm"] = round(100.0 * r["llama3_8b_decode_step"]["GB_s"] / hbm_peak, 1)
         line["llama3_8b_decode_step"] = r["llama3_8b_decode_step"]
+    if "qwen3_0.6b_decode_step" in r:
+        r["qwen3_0.6b_decode_step"]["pct_hbm"] = round(100.0 * r["qwen3_0.6b_decode_step"]["GB_s"] / hbm_peak, 1)
+        line["qwen3_0.6b_decode_step"] = r["qwen3_0.6b_decode_step"]
+    if "qwen3_0.6b_prefill_layer" in r:
+        pq = r["qwen3_0.6b_prefill_layer"]
+        pq["pct_bf16_dense_peak"] = round(100.0 * pq["TFLOP_s"] / float(peaks.get("bf16_tflops", 1900.0)), 1)
+        line["qwen3_0.6b_prefill_layer"] = pq
     if "llama3_8b_prefill_layer" in r:
         pf = r["llama3_8b_prefill_layer"]
         pf["pct_bf16_dense_peak"] = round(100.0 * pf["TFLOP_s"] / float(peaks.get("bf16_tflops", 1900.0)), 1)
