@@ -225,6 +225,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int units = p.mtu * p.nt * p.splits;
 
     if (threadIdx.x == 0) {
+        // the TMA unit reads the tensor maps on first use: fetch them while the set-up runs
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_w)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_x)) : "memory");
         for (int s = 0; s < p.stages; s++) {
             mbar_init(smem_u32(&full_bar[s]), 1);
             mbar_init(smem_u32(&empty_bar[s]), 1);
@@ -567,29 +570,38 @@ int plan_gemm(Plan *pl, int64_t rows, int64_t k, int64_t ncols, const DeviceInfo
     p.k = (int)k;
     p.num_kb = (int)((k + kBK - 1) / kBK);
     const int64_t n16 = (ncols + 15) / 16 * 16;
-    p.bn = (int)(n16 < 256 ? n16 : 256);
-    p.bn_alloc = pow2_at_least(p.bn);
     p.mt = (int)((rows + kBM - 1) / kBM);
-    p.nt = (int)((ncols + p.bn - 1) / p.bn);
-    if ((int64_t)p.mt * p.nt * kMaxSplits > 0x7fffffffLL)
+    if ((int64_t)p.mt * ((ncols + 15) / 16) * kMaxSplits > 0x7fffffffLL)
         return fail(BM_ERR_INVALID_ARG, "tensor-core product: too many tiles");
-    // Row tiles per unit (MT) and k-splits with the least predicted time.  256-row units
-    // (two MMAs sharing the X tile: fewer operand bytes per unit of work) are taken only
-    // with full 256-column tiles, where they were measured.
-    int mt_unit = 1, splits = 1;
+    // Tile width, row tiles per unit (MT) and k-splits with the least predicted time.
+    // 256-column tiles move the fewest operand bytes per unit of work; 128-column tiles
+    // (a k-block takes about as long) double the units of a product with few row tiles,
+    // which can beat splitting k and reducing.  256-row units (two MMAs sharing the X
+    // tile) are taken only with full 256-column tiles, where they were measured.
+    int mt_unit = 1, splits = 1, bn = (int)(n16 < 256 ? n16 : 256);
     double best_us = 1e300;
-    const int64_t tiles128 = (int64_t)p.mt * p.nt;
-    for (int mt = 1; mt <= (allow_mt2 && p.mt >= 2 && p.bn == 256 ? 2 : 1); mt++) {
-        const int64_t tiles = (int64_t)((p.mt + mt - 1) / mt) * p.nt;
-        for (int sp = 1; sp <= (allow_split ? std::min(kMaxSplits, p.num_kb) : 1); sp++) {
-            const double us = plan_us(tiles, tiles128, p.num_kb, p.bn, mt, sp, dev.sm_count, rows, ncols);
-            if (us < best_us - 1e-9) {
-                best_us = us;
-                mt_unit = mt;
-                splits = sp;
+    const int widths[2] = {(int)(n16 < 256 ? n16 : 256), n16 > 128 ? 128 : 0};
+    for (int wi = 0; wi < 2; wi++) {
+        const int bw = widths[wi];
+        if (bw == 0) continue;
+        const int64_t nt = (ncols + bw - 1) / bw;
+        const int64_t tiles128 = (int64_t)p.mt * nt;
+        for (int mt = 1; mt <= (allow_mt2 && p.mt >= 2 && bw == 256 ? 2 : 1); mt++) {
+            const int64_t tiles = (int64_t)((p.mt + mt - 1) / mt) * nt;
+            for (int sp = 1; sp <= (allow_split ? std::min(kMaxSplits, p.num_kb) : 1); sp++) {
+                const double us = plan_us(tiles, tiles128, p.num_kb, bw, mt, sp, dev.sm_count, rows, ncols);
+                if (us < best_us - 1e-9) {
+                    best_us = us;
+                    mt_unit = mt;
+                    splits = sp;
+                    bn = bw;
+                }
             }
         }
     }
+    p.bn = bn;
+    p.bn_alloc = pow2_at_least(p.bn);
+    p.nt = (int)((ncols + p.bn - 1) / p.bn);
     pl->mt_per_unit = mt_unit;
     p.mtu = (p.mt + mt_unit - 1) / mt_unit;
     p.nbuf = 2 * mt_unit * p.bn_alloc <= 512 ? 2 : 1;  // TMEM holds 512 columns
