@@ -38,10 +38,13 @@ def ambiguous_rows(X, k):
     the sum is not exact in every order (its bits span more than 53 places) and the
     exact mean lies within (k + 4) * 2^-53 (relative) of an f32 rounding boundary."""
     X = np.asarray(X, np.float32).reshape(-1, k)
-    q = (X * X).astype(np.float64)  # each square is one f32 multiply
+    with np.errstate(over="ignore", invalid="ignore"):
+        q = (X * X).astype(np.float64)  # each square is one f32 multiply (inf when it overflows)
     amb = np.zeros(X.shape[0], bool)
     rel = (k + 4) * 2.0 ** -53
     for r in range(X.shape[0]):
+        if not np.isfinite(q[r]).all():
+            continue  # an infinite or NaN square: the mean is +inf or NaN whatever the order
         s = math.fsum(q[r])
         nz = q[r][q[r] != 0]
         if s == 0 or math.frexp(s)[1] - min(_lsb_exponent(float(v)) for v in nz) <= 53:
@@ -248,3 +251,56 @@ def test_decode_front_end_graph_with_pdl(bm):
     finally:
         bm.bm_set_pdl(old)
     assert bm.bm_device_status() == 0
+
+
+def _same_or_both_nan(got, want):
+    got, want = np.asarray(got, np.float32), np.asarray(want, np.float32)
+    nan = np.isnan(want)
+    return np.array_equal(np.isnan(got), nan) and np.array_equal(bits32(got[~nan]), bits32(want[~nan]))
+
+
+@pytest.mark.parametrize("k", [576, 4096, 6000, 33])
+def test_special_rows(bm, k):
+    """Rows that take the norm's rarely used steps, against the oracle: an infinite value
+    (scale 0, so inf * 0 = NaN there and zeros elsewhere), a NaN, a value whose square
+    overflows, values so small that every square is subnormal or tiny (the accumulation
+    that keeps subnormal squares), a mean below the normal f32 range (the double
+    fallback), and a zero row with eps > 0."""
+    rng = np.random.default_rng(k)
+    X = rng.normal(0, 1, (7, k)).astype(np.float32)
+    X[0, 3] = np.inf
+    X[1, k // 2] = np.nan
+    X[2, 1] = np.float32(3e19)              # its square overflows to inf
+    X[3] *= np.float32(1e-12)               # every square below 2^-63: subnormal handling kept
+    X[4] *= np.float32(1e-21)               # squares subnormal or zero, mean below 2^-126
+    X[5] = 0.0
+    X[6] *= np.float32(1e-19)               # mean near the bottom of the normal range
+    g = norm_weight("norm.special.%d" % k, k)
+    for eps in (1e-5, 0.0):
+        out, _ = bm.bm_rms_norm_mul(to_dev(X), to_dev(g), eps)
+        want = oracle.rms_norm_mul(X, g, eps)
+        got = out.cpu().numpy()
+        amb = ambiguous_rows(np.nan_to_num(X, nan=0.0, posinf=0.0), k)
+        for r in range(X.shape[0]):
+            if amb[r] and r not in (0, 1, 2):
+                continue
+            assert _same_or_both_nan(got[r], want[r]), (eps, r)
+
+
+def test_special_rows_fused(bm):
+    """The fused front end takes the same steps (an infinite value and tiny rows)."""
+    import torch
+    k = 1024
+    rng = np.random.default_rng(5)
+    g = norm_weight("norm.special.fused", k)
+    W = synth.normal_f16(0, "w.special", 0.02, (64, k))
+    for scale, spike in ((1.0, np.inf), (1e-12, None), (1e-21, None)):
+        x = (rng.normal(0, 1, k) * scale).astype(np.float32)
+        if spike is not None:
+            x[10] = spike
+        n_out = torch.zeros(k, dtype=torch.float32, device="cuda")
+        y = bm.bm_f16_matvec_norm([to_dev(W)], to_dev(x), to_dev(g), EPS, n_out=n_out)[0]
+        n_want = oracle.rms_norm_mul(x, g, EPS)
+        assert _same_or_both_nan(n_out.cpu().numpy(), n_want)
+        y_want = oracle.matvec(W, oracle.to_f16(n_want))
+        assert _same_or_both_nan(y.cpu().numpy(), y_want)
