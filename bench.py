@@ -608,19 +608,31 @@ def bench_llama_prefill(bm, dev, stream, torch, reps=10):
         bm.bm_to_f16(Y["gate"], hd, stream=stream)  # stand-in FFN activation, same shape as in step()
         bm.bm_f16_matmul(W["down"], hd, Y=Y["down"], stream=stream)
 
+    def step_multi():
+        # the same with the separate matrices: bm_f16_matmul_multi shares one launch
+        bm.bm_to_f16(x, h, stream=stream)
+        bm.bm_f16_matmul_multi([W["q"], W["k"], W["v"]], h, [Y["q"], Y["k"], Y["v"]], stream=stream)
+        bm.bm_f16_matmul(W["o"], h, Y=Y["o"], stream=stream)
+        bm.bm_f16_matmul_multi([W["gate"], W["up"]], h, [Y["gate"], Y["up"]], stream=stream)
+        bm.bm_to_f16(Y["gate"], hd, stream=stream)
+        bm.bm_f16_matmul(W["down"], hd, Y=Y["down"], stream=stream)
+
     old = bm.bm_set_pdl(False)
     try:
         ms_plain = graph_time(torch, stream, step, reps=reps)
         bm.bm_set_pdl(True)
         ms_pdl = graph_time(torch, stream, step, reps=reps)
         ms_fused = graph_time(torch, stream, step_fused, reps=reps)
+        ms_multi = graph_time(torch, stream, step_multi, reps=reps)
     finally:
         bm.bm_set_pdl(old)
     res = {"tokens": n, "ms_per_step": round(ms_pdl, 4), "TFLOP_s": round(flops / ms_pdl / 1e9, 1),
            "ms_per_step_without_pdl": round(ms_plain, 4), "TFLOP_s_without_pdl": round(flops / ms_plain / 1e9, 1),
            "how": "one layer's 7 products at 512 columns plus 2 rounding kernels, CUDA graph, PDL on / off",
            "concatenated_weights": {"ms_per_step": round(ms_fused, 4), "TFLOP_s": round(flops / ms_fused / 1e9, 1),
-                                    "how": "Q/K/V and gate/up each stored as one matrix: 4 products, PDL on"}}
+                                    "how": "Q/K/V and gate/up each stored as one matrix: 4 products, PDL on"},
+           "multi": {"ms_per_step": round(ms_multi, 4), "TFLOP_s": round(flops / ms_multi / 1e9, 1),
+                     "how": "separate matrices, Q/K/V and gate/up through bm_f16_matmul_multi, PDL on"}}
     del W, Y, Wqkv, Wgu, Yqkv, Ygu
     return res
 

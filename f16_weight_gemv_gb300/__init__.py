@@ -17,7 +17,7 @@ import torch
 from . import _build
 
 __all__ = [
-    "BmError", "lib", "bm_to_f16", "bm_f16_matvec", "bm_f16_matvec_multi", "bm_f16_matvec_act", "bm_f16_matvec_norm", "bm_rms_norm_mul", "bm_f16_matmul", "bm_f16_matmul_noalloc",
+    "BmError", "lib", "bm_to_f16", "bm_f16_matvec", "bm_f16_matvec_multi", "bm_f16_matvec_act", "bm_f16_matvec_norm", "bm_rms_norm_mul", "bm_f16_matmul", "bm_f16_matmul_multi", "bm_f16_matmul_noalloc",
     "bm_f16_logits", "bm_f16_get_rows", "bm_takes_sgemm", "bm_device_status", "bm_status_string", "bm_last_error",
     "bm_selftest_wait_timeout", "bm_set_pdl", "bm_set_exact_sgemm_cols", "EXPORTS", "BM_MAX_K",
 ]
@@ -36,6 +36,7 @@ EXPORTS = {
                                 C.POINTER(_vp), _vp]),
     "bm_rms_norm_mul": (_i, [_vp, _vp, _i64, _i64, C.c_float, _vp, _vp, _vp]),
     "bm_f16_matmul": (_i, [_vp, _i64, _i64, _vp, _i64, _vp, _vp]),
+    "bm_f16_matmul_multi": (_i, [_i, C.POINTER(_vp), C.POINTER(_i64), _i64, _vp, _i64, C.POINTER(_vp), _vp]),
     "bm_f16_logits": (_i, [_vp, _i64, _i64, _vp, _i64, _vp, _vp]),
     "bm_f16_matmul_noalloc": (_i, [_vp, _i64, _i64, _vp, _i64, _vp, _vp]),
     "bm_f16_get_rows": (_i, [_vp, _i64, _i64, _vp, _i64, _vp, _vp]),
@@ -254,6 +255,29 @@ def _product(fn_name: str, W, X, Y, stream):
 def bm_f16_matmul(W, X, Y=None, stream=None):
     """Y[c][r] (Y[c*rows + r] in memory) for W [rows][k] and X [ncols][k]."""
     return _product("bm_f16_matmul", W, X, Y, stream)
+
+
+def bm_f16_matmul_multi(Ws, X, Ys=None, stream=None):
+    """bm_f16_matmul of each matrix in Ws with the shared activation X [ncols][k];
+    Ys[m] is [ncols][rows_m].  The tensor-core matrices share one launch.  Returns Ys."""
+    n = len(Ws)
+    if X.dim() == 1:
+        X = X.view(1, -1)
+    ncols, k = X.shape
+    if Ys is None:
+        Ys = [torch.empty((ncols, W.shape[0]), dtype=torch.float32, device=X.device) for W in Ws]
+    if len(Ys) != n:
+        raise ValueError("one output per matrix")
+    for W, Y in zip(Ws, Ys):
+        r, kk = _wk(W)
+        if kk != k or Y.numel() != r * ncols:
+            raise ValueError("shape mismatch in bm_f16_matmul_multi")
+    wp = (C.c_void_p * max(n, 1))(*[_dev(W, "W", _F16_LIKE) for W in Ws])
+    yp = (C.c_void_p * max(n, 1))(*[_dev(Y, "Y", (torch.float32,)) for Y in Ys])
+    rows = (C.c_int64 * max(n, 1))(*[W.shape[0] for W in Ws])
+    _check(lib().bm_f16_matmul_multi(n, wp, rows, k, _dev(X, "X", _F16_LIKE), ncols, yp, _stream(stream)),
+           "bm_f16_matmul_multi")
+    return Ys
 
 
 def bm_f16_matmul_noalloc(W, X, Y, stream=None):

@@ -373,6 +373,48 @@ int bm_f16_matmul(const uint16_t *W, int64_t rows, int64_t k, const uint16_t *X,
     return product("bm_f16_matmul", W, rows, k, X, ncols, Y, stream);
 }
 
+int bm_f16_matmul_multi(int nmat, const uint16_t *const *W, const int64_t *rows, int64_t k, const uint16_t *X,
+                        int64_t ncols, float *const *Y, bm_stream_t stream)
+{
+    clear_error();
+    if (nmat < 1 || nmat > 4) return fail(BM_ERR_INVALID_ARG, "bm_f16_matmul_multi: nmat = %d outside 1..4", nmat);
+    if (!W || !rows || !Y) return fail(BM_ERR_INVALID_ARG, "bm_f16_matmul_multi: null host array");
+    for (int m = 0; m < nmat; m++) {
+        int st = check_matrix_args("bm_f16_matmul_multi", W[m], rows[m], k, X, ncols, Y[m]);
+        if (st != BM_OK) return st;
+        for (int q = 0; q < m; q++)
+            if (overlap(Y[m], rows[m] * ncols * 4, Y[q], rows[q] * ncols * 4) ||
+                overlap(Y[m], rows[m] * ncols * 4, W[q], rows[q] * k * 2) ||
+                overlap(Y[q], rows[q] * ncols * 4, W[m], rows[m] * k * 2))
+                return fail(BM_ERR_INVALID_ARG, "bm_f16_matmul_multi: output %d overlaps an input or output", m);
+    }
+    if (ncols == 0) return BM_OK;
+    // The matrices whose own shape takes the tensor-core path share one launch; any other
+    // matrix (vec_dot, or tinyBLAS's bits on the CUDA-core kernel) is its own product.
+    const int exact_cols = g_exact_cols.load(std::memory_order_relaxed);
+    const uint16_t *tw[4];
+    int64_t trows[4];
+    float *ty[4];
+    int nt = 0;
+    for (int m = 0; m < nmat; m++) {
+        if (rows[m] == 0) continue;
+        if (bm_takes_sgemm(rows[m], k, ncols) && ncols > exact_cols) {
+            tw[nt] = W[m];
+            trows[nt] = rows[m];
+            ty[nt] = Y[m];
+            nt++;
+            continue;
+        }
+        int st = product("bm_f16_matmul_multi", W[m], rows[m], k, X, ncols, Y[m], stream);
+        if (st != BM_OK) return st;
+    }
+    if (nt == 0) return BM_OK;
+    int st;
+    DeviceInfo dev;
+    if (!current_device(&dev, &st)) return st;
+    return launch_gemm_tc_multi(nt, tw, trows, k, X, ncols, ty, reinterpret_cast<cudaStream_t>(stream), dev);
+}
+
 int bm_f16_matmul_noalloc(const uint16_t *W, int64_t rows, int64_t k, const uint16_t *X, int64_t ncols, float *Y,
                           bm_stream_t stream)
 {

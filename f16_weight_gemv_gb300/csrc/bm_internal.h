@@ -71,6 +71,10 @@ int launch_sgemm_stream(const uint16_t *W, int64_t rows, int64_t k, const uint16
 // Tensor-core product for bm_takes_sgemm shapes (rows % 4 == 0, k % 8 == 0, ncols >= 2).
 int launch_gemm_tc(const uint16_t *W, int64_t rows, int64_t k, const uint16_t *X, int64_t ncols,
                    float *Y, cudaStream_t s, const DeviceInfo &dev);
+// Up to four bm_takes_sgemm products sharing the activation X in one tensor-core launch:
+// Y[m] = W[m] (rows[m] x k) times X (ncols x k), each laid out [ncols][rows[m]].
+int launch_gemm_tc_multi(int nmat, const uint16_t *const *W, const int64_t *rows, int64_t k, const uint16_t *X,
+                         int64_t ncols, float *const *Y, cudaStream_t s, const DeviceInfo &dev);
 // As launch_gemm_tc, with the split-k workspace in a static device array instead of
 // a stream-ordered allocation (no allocation of any kind).
 int launch_gemm_tc_noalloc(const uint16_t *W, int64_t rows, int64_t k, const uint16_t *X, int64_t ncols,

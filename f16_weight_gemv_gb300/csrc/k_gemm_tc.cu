@@ -52,6 +52,7 @@
 
 #include <algorithm>
 #include <cmath>
+#include <cstring>
 #include <mutex>
 
 namespace bm {
@@ -66,17 +67,26 @@ constexpr int kThreads = 32 * (2 + kEpiWarps);
 constexpr int kTileABytes = kBM * kBK * 2;  // 16 KB
 constexpr int kMaxStages = 8;
 constexpr int kMaxSplits = 8;
+constexpr int kMaxMats = 4;       // matrices sharing one activation in one launch
 constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;  // 2 s
 
+// Up to kMaxMats matrices W[m] (rows[m] x k) times one activation X (ncols x k), each
+// into its own Y[m] (ncols x rows[m]).  The matrices' row units are laid end to end:
+// matrix m owns row units ubeg[m] .. ubeg[m+1]-1 and the split-k workspace's 128-row
+// tiles tbeg[m] .. (its row units x MT).
 struct GemmParams {
-    float *Y;
+    float *Y[kMaxMats];
+    int rows[kMaxMats];
+    int ubeg[kMaxMats + 1];
+    int tbeg[kMaxMats + 1];
+    int nmat;
     float *ws;                // partial tiles, [tile][split][BN][128] (split count > 1 only)
-    int rows, ncols, k;
+    int ncols, k;
     int num_kb;               // ceil(k / 64)
     int bn;                   // tile columns (MMA N), multiple of 16, <= 256
     int bn_alloc;             // TMEM columns per accumulator: power of two >= max(32, bn)
-    int mt, nt;               // row tiles (128 rows), column tiles
-    int mtu;                  // row units: MT row tiles each (one work unit's rows)
+    int nt;                   // column tiles
+    int mtu;                  // row units of all matrices (MT row tiles each): ubeg[nmat]
     int nbuf;                 // TMEM accumulator sets: 2 (double-buffered) or 1
     int splits;
     int stages;
@@ -171,10 +181,29 @@ __device__ __forceinline__ void tmem_wait_ld(uint32_t (&v)[32])
                    "+r"(v[29]), "+r"(v[30]), "+r"(v[31]));
 }
 
+// The tensor maps: one per weight matrix (box 64 x 128 * MT rows) and the activation's.
+struct TmaMaps {
+    CUtensorMap w[kMaxMats];
+    CUtensorMap x;
+};
+
+// a[m] for a small parameter array, by compile-time indices only (a run-time index
+// would copy the kernel's parameters to local memory)
+template <class T, int N>
+__device__ __forceinline__ T pick(const T (&a)[N], int m)
+{
+    T v = a[0];
+#pragma unroll
+    for (int q = 1; q < N; q++)
+        if (m == q) v = a[q];
+    return v;
+}
+
 struct Unit {
-    int m0;     // first row of the unit: MT row tiles of 128 rows
+    int mat;    // the matrix
+    int m0;     // first row of the unit in its matrix: MT row tiles of 128 rows
     int n0, s, kb0, kb1;
-    int tile0;  // split-k bookkeeping index of the unit's first row tile (row tile t: tile0 + t * nt)
+    int tile0;  // workspace index of the unit's first row tile (row tile t: tile0 + t * nt)
 };
 
 // Units are (row unit, column tile, k-split), ordered column tile fastest, then split,
@@ -188,9 +217,15 @@ __device__ __forceinline__ Unit unit_of(const GemmParams &p, int u)
     const int rest = u / p.nt;
     x.s = rest % p.splits;
     const int mu = rest / p.splits;
-    x.m0 = mu * MT * kBM;
+    int m = 0;
+#pragma unroll
+    for (int q = 1; q < kMaxMats; q++)
+        if (q < p.nmat && mu >= p.ubeg[q]) m = q;
+    const int local = mu - pick(p.ubeg, m);
+    x.mat = m;
+    x.m0 = local * MT * kBM;
     x.n0 = nt * p.bn;
-    x.tile0 = mu * MT * p.nt + nt;
+    x.tile0 = (pick(p.tbeg, m) + local * MT) * p.nt + nt;
     x.kb0 = (int)((int64_t)p.num_kb * x.s / p.splits);
     x.kb1 = (int)((int64_t)p.num_kb * (x.s + 1) / p.splits);
     return x;
@@ -203,8 +238,7 @@ __device__ __forceinline__ Unit unit_of(const GemmParams &p, int u)
 // (p.nbuf == 2) the epilogue of one unit overlaps the MMAs of the next.
 template <int MT>
 __global__ void __launch_bounds__(kThreads, 1)
-    k_gemm_tc(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_x,
-              const GemmParams p)
+    k_gemm_tc(const __grid_constant__ TmaMaps maps, const __grid_constant__ GemmParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[kMaxStages];
@@ -226,8 +260,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         // the TMA unit reads the tensor maps on first use: fetch them while the set-up runs
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_w)) : "memory");
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_x)) : "memory");
+        for (int m = 0; m < p.nmat; m++)
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&maps.w[m])) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&maps.x)) : "memory");
         for (int s = 0; s < p.stages; s++) {
             mbar_init(smem_u32(&full_bar[s]), 1);
             mbar_init(smem_u32(&empty_bar[s]), 1);
@@ -268,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 dev::pdl_wait();
                 waited = true;
                 for (int q = 0; q < pend; q++)
-                    tma_load_2d(ring_u32 + (uint32_t)pend_s[q] * stage_bytes + MT * kTileABytes, &map_x,
+                    tma_load_2d(ring_u32 + (uint32_t)pend_s[q] * stage_bytes + MT * kTileABytes, &maps.x,
                                 pend_kb[q] * kBK, pend_n0[q], smem_u32(&full_bar[pend_s[q]]));
                 pend = 0;
             };
@@ -285,9 +320,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t a_dst = ring_u32 + (uint32_t)s * stage_bytes;
                     const uint32_t fb = smem_u32(&full_bar[s]);
                     mbar_expect_tx(fb, stage_bytes);
-                    tma_load_2d(a_dst, &map_w, kb * kBK, x.m0, fb);  // MT * 128 rows in one box
+                    tma_load_2d(a_dst, &maps.w[x.mat], kb * kBK, x.m0, fb);  // MT * 128 rows in one box
                     if (waited) {
-                        tma_load_2d(a_dst + MT * kTileABytes, &map_x, kb * kBK, x.n0, fb);
+                        tma_load_2d(a_dst + MT * kTileABytes, &maps.x, kb * kBK, x.n0, fb);
                     } else {  // t < stages here, so at most kMaxStages stages wait for X
                         pend_s[pend] = s;
                         pend_kb[pend] = kb;
@@ -354,6 +389,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t taddr =
                     tmem_base + (uint32_t)((b * MT + m) * p.bn_alloc) + ((uint32_t)(quarter * 32) << 16);
                 const int row = x.m0 + m * kBM + rloc;
+                const int rows = pick(p.rows, x.mat);
+                float *const Y = pick(p.Y, x.mat);
                 const int tile = x.tile0 + m * p.nt;
                 float *ws_unit = p.splits > 1 ? p.ws + ((size_t)tile * p.splits + x.s) * (size_t)p.bn * kBM : nullptr;
                 // one chunk's 32 values of this row: to the split's partial tile, or to Y
@@ -362,11 +399,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int q = 0; q < 32; q++)
                             if (c + q < p.bn) ws_unit[(size_t)(c + q) * kBM + rloc] = __uint_as_float(v[q]);
-                    } else if (row < p.rows) {
+                    } else if (row < rows) {
 #pragma unroll
                         for (int q = 0; q < 32; q++) {
                             const int col = x.n0 + c + q;
-                            if (c + q < p.bn && col < p.ncols) p.Y[(size_t)col * p.rows + row] = __uint_as_float(v[q]);
+                            if (c + q < p.bn && col < p.ncols) Y[(size_t)col * rows + row] = __uint_as_float(v[q]);
                         }
                     }
                 };
@@ -419,44 +456,59 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-// Split-k reduction: Y[col * rows + row] = sum of the S partials in order 0..S-1,
-// where the partial of split s for (row, col) lies at
-// ws[((tile * S + s) * bn + col % bn) * 128 + row % 128], tile = (row / 128) * nt + col / bn.
-// Each thread takes four consecutive rows of one column (rows % 4 == 0 on this path)
-// and issues the 16-byte loads of every split before the first add (a loop bounded
-// only at run time left one round trip per split: 8 us for eight splits); vec4 says
-// Y is 16-byte aligned, else the four results are stored one by one.
+// Split-k reduction: Y[m][col * rows[m] + row] = sum of the S partials in order 0..S-1,
+// where the partial of split s for (matrix m, row, col) lies at
+// ws[((tile * S + s) * bn + col % bn) * 128 + row % 128],
+// tile = (tbeg[m] + row / 128) * nt + col / bn.  The elements of all matrices form one
+// index space (matrix m's four-row groups start at ebeg[m]).  Each thread takes four
+// consecutive rows of one column (rows % 4 == 0 on this path) and issues the 16-byte
+// loads of every split before the first add (a loop bounded only at run time left one
+// round trip per split: 8 us for eight splits); vec4 says every Y is 16-byte aligned,
+// else the four results are stored one by one.
 constexpr int kReduceThreads = 256;
 
-__global__ void __launch_bounds__(kReduceThreads) k_splitk_reduce(const float *__restrict__ ws, float *__restrict__ Y,
-                                                                  int rows, int ncols, int bn, int nt, int S, int vec4)
+struct ReduceJob {
+    float *Y[kMaxMats];
+    int rows[kMaxMats];
+    int tbeg[kMaxMats];
+    int64_t ebeg[kMaxMats + 1];
+    int nmat, ncols, bn, nt, S, vec4;
+};
+
+__global__ void __launch_bounds__(kReduceThreads) k_splitk_reduce(const float *__restrict__ ws,
+                                                                  const __grid_constant__ ReduceJob j)
 {
     dev::pdl_wait();  // the partials are the previous kernel's output
-    const int rows4 = rows >> 2;
-    const int64_t total = (int64_t)rows4 * ncols;
+    const int64_t total = j.ebeg[j.nmat];
     for (int64_t e = (int64_t)blockIdx.x * kReduceThreads + threadIdx.x; e < total;
          e += (int64_t)gridDim.x * kReduceThreads) {
-        const int col = (int)(e / rows4), row = (int)(e - (int64_t)col * rows4) * 4;
-        const int tile = (row >> 7) * nt + col / bn;
-        const float4 *src =
-            reinterpret_cast<const float4 *>(ws + (((size_t)tile * S) * bn + col % bn) * kBM + (row & (kBM - 1)));
-        const size_t split_stride = (size_t)bn * kBM / 4;  // in float4
+        int m = 0;
+#pragma unroll
+        for (int q = 1; q < kMaxMats; q++)
+            if (q < j.nmat && e >= j.ebeg[q]) m = q;
+        const int rows = pick(j.rows, m), rows4 = rows >> 2;
+        const int64_t le = e - pick(j.ebeg, m);
+        const int col = (int)(le / rows4), row = (int)(le - (int64_t)col * rows4) * 4;
+        const int tile = (pick(j.tbeg, m) + (row >> 7)) * j.nt + col / j.bn;
+        const float4 *src = reinterpret_cast<const float4 *>(
+            ws + (((size_t)tile * j.S) * j.bn + col % j.bn) * kBM + (row & (kBM - 1)));
+        const size_t split_stride = (size_t)j.bn * kBM / 4;  // in float4
         float4 v[kMaxSplits];
 #pragma unroll
         for (int sp = 0; sp < kMaxSplits; sp++)  // every split's load in flight before the first add
-            if (sp < S) v[sp] = __ldcg(src + sp * split_stride);
+            if (sp < j.S) v[sp] = __ldcg(src + sp * split_stride);
         float4 acc = v[0];
 #pragma unroll
         for (int sp = 1; sp < kMaxSplits; sp++) {
-            if (sp < S) {
+            if (sp < j.S) {
                 acc.x += v[sp].x;
                 acc.y += v[sp].y;
                 acc.z += v[sp].z;
                 acc.w += v[sp].w;
             }
         }
-        float *dst = Y + (size_t)col * rows + row;
-        if (vec4) {
+        float *dst = pick(j.Y, m) + (size_t)col * rows + row;
+        if (j.vec4) {
             *reinterpret_cast<float4 *>(dst) = acc;
         } else {
             dst[0] = acc.x;
@@ -558,20 +610,30 @@ struct Plan {
     size_t ws_bytes;
 };
 
-int plan_gemm(Plan *pl, int64_t rows, int64_t k, int64_t ncols, const DeviceInfo &dev, bool allow_split,
-              bool allow_mt2)
+// Plans one launch over nmat matrices of rows[m] x k sharing ncols activation columns.
+int plan_gemm(Plan *pl, int nmat, const int64_t *rows, int64_t k, int64_t ncols, const DeviceInfo &dev,
+              bool allow_split, bool allow_mt2)
 {
-    if (rows > 0x7fffffffLL || ncols > 0x7fffffffLL || k > 0x7fffffffLL)
-        return fail(BM_ERR_INVALID_ARG, "tensor-core product: rows, k and ncols must be below 2^31");
+    if (nmat < 1 || nmat > kMaxMats) return fail(BM_ERR_INVALID_ARG, "tensor-core product: 1..4 matrices");
     GemmParams &p = pl->p;
     p = GemmParams{};
-    p.rows = (int)rows;
+    int64_t mts[kMaxMats], total_mt = 0, total_rows = 0;
+    for (int m = 0; m < nmat; m++) {
+        if (rows[m] < 1 || rows[m] > 0x7fffffffLL)
+            return fail(BM_ERR_INVALID_ARG, "tensor-core product: rows must lie in 1 .. 2^31-1");
+        p.rows[m] = (int)rows[m];
+        mts[m] = (rows[m] + kBM - 1) / kBM;
+        total_mt += mts[m];
+        total_rows += rows[m];
+    }
+    if (ncols > 0x7fffffffLL || k > 0x7fffffffLL)
+        return fail(BM_ERR_INVALID_ARG, "tensor-core product: k and ncols must be below 2^31");
+    p.nmat = nmat;
     p.ncols = (int)ncols;
     p.k = (int)k;
     p.num_kb = (int)((k + kBK - 1) / kBK);
     const int64_t n16 = (ncols + 15) / 16 * 16;
-    p.mt = (int)((rows + kBM - 1) / kBM);
-    if ((int64_t)p.mt * ((ncols + 15) / 16) * kMaxSplits > 0x7fffffffLL)
+    if ((total_mt + nmat) * ((ncols + 15) / 16) * kMaxSplits > 0x7fffffffLL)
         return fail(BM_ERR_INVALID_ARG, "tensor-core product: too many tiles");
     // Tile width, row tiles per unit (MT) and k-splits with the least predicted time.
     // 256-column tiles move the fewest operand bytes per unit of work; 128-column tiles
@@ -585,11 +647,13 @@ int plan_gemm(Plan *pl, int64_t rows, int64_t k, int64_t ncols, const DeviceInfo
         const int bw = widths[wi];
         if (bw == 0) continue;
         const int64_t nt = (ncols + bw - 1) / bw;
-        const int64_t tiles128 = (int64_t)p.mt * nt;
-        for (int mt = 1; mt <= (allow_mt2 && p.mt >= 2 && bw == 256 ? 2 : 1); mt++) {
-            const int64_t tiles = (int64_t)((p.mt + mt - 1) / mt) * nt;
+        const int64_t tiles128 = total_mt * nt;
+        for (int mt = 1; mt <= (allow_mt2 && total_mt >= 2 && bw == 256 ? 2 : 1); mt++) {
+            int64_t units_rows = 0;
+            for (int m = 0; m < nmat; m++) units_rows += (mts[m] + mt - 1) / mt;
+            const int64_t tiles = units_rows * nt;
             for (int sp = 1; sp <= (allow_split ? std::min(kMaxSplits, p.num_kb) : 1); sp++) {
-                const double us = plan_us(tiles, tiles128, p.num_kb, bw, mt, sp, dev.sm_count, rows, ncols);
+                const double us = plan_us(tiles, tiles128, p.num_kb, bw, mt, sp, dev.sm_count, total_rows, ncols);
                 if (us < best_us - 1e-9) {
                     best_us = us;
                     mt_unit = mt;
@@ -603,7 +667,18 @@ int plan_gemm(Plan *pl, int64_t rows, int64_t k, int64_t ncols, const DeviceInfo
     p.bn_alloc = pow2_at_least(p.bn);
     p.nt = (int)((ncols + p.bn - 1) / p.bn);
     pl->mt_per_unit = mt_unit;
-    p.mtu = (p.mt + mt_unit - 1) / mt_unit;
+    p.ubeg[0] = 0;
+    p.tbeg[0] = 0;
+    for (int m = 0; m < nmat; m++) {
+        const int units_m = (int)((mts[m] + mt_unit - 1) / mt_unit);
+        p.ubeg[m + 1] = p.ubeg[m] + units_m;
+        p.tbeg[m + 1] = p.tbeg[m] + units_m * mt_unit;  // a unit's second tile past the matrix end included
+    }
+    for (int m = nmat; m < kMaxMats; m++) {
+        p.ubeg[m + 1] = p.ubeg[nmat];
+        p.tbeg[m + 1] = p.tbeg[nmat];
+    }
+    p.mtu = p.ubeg[nmat];
     p.nbuf = 2 * mt_unit * p.bn_alloc <= 512 ? 2 : 1;  // TMEM holds 512 columns
     const int64_t tiles = (int64_t)p.mtu * p.nt;       // work tiles of 128 * MT rows
     p.splits = splits;
@@ -618,14 +693,12 @@ int plan_gemm(Plan *pl, int64_t rows, int64_t k, int64_t ncols, const DeviceInfo
     const size_t smem = (size_t)p.stages * stage_bytes + 1024;
     const size_t one_per_sm = (size_t)dev.max_smem_optin / 2 + 4096;
     pl->smem = std::max(smem, one_per_sm);
-    // partial tiles of 128 rows, including a unit's second tile past the last row
-    const size_t ws_tiles = (size_t)tiles * mt_unit;
-    pl->ws_bytes = p.splits > 1 ? ws_tiles * p.splits * p.bn * kBM * sizeof(float) : 0;
+    pl->ws_bytes = p.splits > 1 ? (size_t)p.tbeg[nmat] * p.nt * p.splits * p.bn * kBM * sizeof(float) : 0;
     return BM_OK;
 }
 
 template <int MT>
-int launch_mt(const Plan &pl, const CUtensorMap &mw, const CUtensorMap &mx, cudaStream_t s, const DeviceInfo &dev)
+int launch_mt(const Plan &pl, const TmaMaps &maps, cudaStream_t s, const DeviceInfo &dev)
 {
     int dev_id = 0;
     cudaGetDevice(&dev_id);
@@ -642,7 +715,7 @@ int launch_mt(const Plan &pl, const CUtensorMap &mw, const CUtensorMap &mx, cuda
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl_enabled() ? 1 : 0;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, k_gemm_tc<MT>, mw, mx, pl.p);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, k_gemm_tc<MT>, maps, pl.p);
     if (e != cudaSuccess) return fail(BM_ERR_CUDA, "tensor-core product: launch failed: %s", cudaGetErrorString(e));
     return BM_OK;
 }
@@ -652,7 +725,23 @@ int launch_mt(const Plan &pl, const CUtensorMap &mw, const CUtensorMap &mx, cuda
 // (griddepcontrol.wait) for the product before it reads the partials.
 int launch_reduce(const Plan &pl, cudaStream_t s, const DeviceInfo &dev)
 {
-    const int64_t total = (int64_t)(pl.p.rows / 4) * pl.p.ncols;
+    ReduceJob j{};
+    j.nmat = pl.p.nmat;
+    j.ncols = pl.p.ncols;
+    j.bn = pl.p.bn;
+    j.nt = pl.p.nt;
+    j.S = pl.p.splits;
+    j.vec4 = 1;
+    j.ebeg[0] = 0;
+    for (int m = 0; m < pl.p.nmat; m++) {
+        j.Y[m] = pl.p.Y[m];
+        j.rows[m] = pl.p.rows[m];
+        j.tbeg[m] = pl.p.tbeg[m];
+        j.ebeg[m + 1] = j.ebeg[m] + (int64_t)(pl.p.rows[m] / 4) * pl.p.ncols;
+        if (reinterpret_cast<uintptr_t>(pl.p.Y[m]) & 15) j.vec4 = 0;
+    }
+    for (int m = pl.p.nmat; m < kMaxMats; m++) j.ebeg[m + 1] = j.ebeg[pl.p.nmat];
+    const int64_t total = j.ebeg[pl.p.nmat];
     int64_t blocks = (total + kReduceThreads - 1) / kReduceThreads;
     blocks = std::max<int64_t>(1, std::min<int64_t>(blocks, (int64_t)dev.sm_count * 8));
     cudaLaunchConfig_t cfg{};
@@ -664,36 +753,38 @@ int launch_reduce(const Plan &pl, cudaStream_t s, const DeviceInfo &dev)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const int vec4 = (reinterpret_cast<uintptr_t>(pl.p.Y) & 15) == 0 ? 1 : 0;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, k_splitk_reduce, (const float *)pl.p.ws, pl.p.Y, pl.p.rows, pl.p.ncols,
-                                       pl.p.bn, pl.p.nt, pl.p.splits, vec4);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, k_splitk_reduce, (const float *)pl.p.ws, j);
     if (e != cudaSuccess)
         return fail(BM_ERR_CUDA, "tensor-core product: reduction launch failed: %s", cudaGetErrorString(e));
     return BM_OK;
 }
 
-int launch_plan(const Plan &pl, const uint16_t *W, const uint16_t *X, cudaStream_t s, const DeviceInfo &dev)
+int launch_plan(const Plan &pl, const uint16_t *const *W, const uint16_t *X, cudaStream_t s, const DeviceInfo &dev)
 {
     if (!get_encoder()) return fail(BM_ERR_CUDA, "tensor-core product: cuTensorMapEncodeTiled unavailable");
-    CUtensorMap mw, mx;
-    if (!make_map(&mw, W, pl.p.rows, pl.p.k, kBM * pl.mt_per_unit) || !make_map(&mx, X, pl.p.ncols, pl.p.k, pl.p.bn))
+    TmaMaps maps;
+    memset(&maps, 0, sizeof(maps));
+    for (int m = 0; m < pl.p.nmat; m++)
+        if (!make_map(&maps.w[m], W[m], pl.p.rows[m], pl.p.k, kBM * pl.mt_per_unit))
+            return fail(BM_ERR_CUDA, "tensor-core product: tensor map encoding failed");
+    if (!make_map(&maps.x, X, pl.p.ncols, pl.p.k, pl.p.bn))
         return fail(BM_ERR_CUDA, "tensor-core product: tensor map encoding failed");
-    const int st = pl.mt_per_unit == 2 ? launch_mt<2>(pl, mw, mx, s, dev) : launch_mt<1>(pl, mw, mx, s, dev);
+    const int st = pl.mt_per_unit == 2 ? launch_mt<2>(pl, maps, s, dev) : launch_mt<1>(pl, maps, s, dev);
     if (st != BM_OK || pl.p.splits == 1) return st;
     return launch_reduce(pl, s, dev);
 }
 
 }  // namespace
 
-int launch_gemm_tc(const uint16_t *W, int64_t rows, int64_t k, const uint16_t *X, int64_t ncols, float *Y,
-                   cudaStream_t s, const DeviceInfo &dev)
+int launch_gemm_tc_multi(int nmat, const uint16_t *const *W, const int64_t *rows, int64_t k, const uint16_t *X,
+                         int64_t ncols, float *const *Y, cudaStream_t s, const DeviceInfo &dev)
 {
     unsigned int *err = device_error_word();
     if (!err) return fail(BM_ERR_CUDA, "tensor-core product: device error word unavailable");
     Plan pl;
-    int st = plan_gemm(&pl, rows, k, ncols, dev, true, true);
+    int st = plan_gemm(&pl, nmat, rows, k, ncols, dev, true, true);
     if (st != BM_OK) return st;
-    pl.p.Y = Y;
+    for (int m = 0; m < nmat; m++) pl.p.Y[m] = Y[m];
     pl.p.err = err;
     pl.p.timeout_ns = kDefaultTimeoutNs;
     if (pl.p.splits == 1) return launch_plan(pl, W, X, s, dev);
@@ -715,6 +806,12 @@ int launch_gemm_tc(const uint16_t *W, int64_t rows, int64_t k, const uint16_t *X
     if (st == BM_OK && e2 != cudaSuccess)
         return fail(BM_ERR_CUDA, "tensor-core product: workspace release failed: %s", cudaGetErrorString(e2));
     return st;
+}
+
+int launch_gemm_tc(const uint16_t *W, int64_t rows, int64_t k, const uint16_t *X, int64_t ncols, float *Y,
+                   cudaStream_t s, const DeviceInfo &dev)
+{
+    return launch_gemm_tc_multi(1, &W, &rows, k, X, ncols, &Y, s, dev);
 }
 
 // ----------------------------------------------------------------------------- no-allocation variant
@@ -739,7 +836,7 @@ int launch_gemm_tc_noalloc(const uint16_t *W, int64_t rows, int64_t k, const uin
     unsigned int *err = device_error_word();
     if (!err) return fail(BM_ERR_CUDA, "no-allocation product: device error word unavailable");
     Plan pl;
-    int st = plan_gemm(&pl, rows, k, ncols, dev, true, true);
+    int st = plan_gemm(&pl, 1, &rows, k, ncols, dev, true, true);
     if (st != BM_OK) return st;
     const size_t need = pl.ws_bytes;
     if (need > kNoAllocScratchBytes)
@@ -747,7 +844,7 @@ int launch_gemm_tc_noalloc(const uint16_t *W, int64_t rows, int64_t k, const uin
                     "bm_f16_matmul_noalloc: this product needs %zu bytes of split-k scratch; the static scratch "
                     "holds %zu (use bm_f16_matmul)",
                     need, kNoAllocScratchBytes);
-    pl.p.Y = Y;
+    pl.p.Y[0] = Y;
     pl.p.err = err;
     pl.p.timeout_ns = kDefaultTimeoutNs;
     if (pl.p.splits > 1) {
@@ -767,7 +864,7 @@ int launch_gemm_tc_noalloc(const uint16_t *W, int64_t rows, int64_t k, const uin
                         cudaGetErrorString(g_scratch_status[d]));
         pl.p.ws = reinterpret_cast<float *>(g_scratch_ptr[d]);
     }
-    return launch_plan(pl, W, X, s, dev);
+    return launch_plan(pl, &W, X, s, dev);
 }
 
 int launch_gemm_tc_withheld(const uint16_t *W, int64_t rows, int64_t k, const uint16_t *X, int64_t ncols, float *Y,
@@ -776,13 +873,13 @@ int launch_gemm_tc_withheld(const uint16_t *W, int64_t rows, int64_t k, const ui
     unsigned int *err = device_error_word();
     if (!err) return fail(BM_ERR_CUDA, "tensor-core product: device error word unavailable");
     Plan pl;
-    int st = plan_gemm(&pl, rows, k, ncols, dev, false, false);
+    int st = plan_gemm(&pl, 1, &rows, k, ncols, dev, false, false);
     if (st != BM_OK) return st;
-    pl.p.Y = Y;
+    pl.p.Y[0] = Y;
     pl.p.err = err;
     pl.p.timeout_ns = timeout_ns;
     pl.p.withhold_first_load = 1;
-    return launch_plan(pl, W, X, s, dev);
+    return launch_plan(pl, &W, X, s, dev);
 }
 
 }  // namespace bm

@@ -166,6 +166,24 @@ int bm_f16_matvec_norm(int nmat, const uint16_t *const *W, const int64_t *rows, 
 int bm_f16_matmul(const uint16_t *W, int64_t rows, int64_t k, const uint16_t *X, int64_t ncols,
                   float *Y, bm_stream_t stream);
 
+/*
+ * bm_f16_matmul for up to four matrices that share one activation X -- the
+ * prefill counterpart of bm_f16_matvec_multi (Q, K and V of a micro-batch; gate
+ * and up): Y[m][c*rows[m] + r] = W[m][r] . X[c].  Each matrix keeps its own
+ * path by its own shape, exactly as bm_f16_matmul (forward.md, "Batched
+ * prefill": each element keeps the bits of its per-pair dot): the matrices
+ * that take the tensor cores share one launch (more work units, one set-up and
+ * one tail), each within the same 4e-6 * sum|w*a| bound of tinyBLAS -- the
+ * f32 sums may be ordered differently from a separate bm_f16_matmul of the same
+ * matrix; the others (vec_dot, or tinyBLAS's bits on the CUDA-core kernel) run
+ * as their own products with the same bits as bm_f16_matmul.
+ *   nmat in 1..4.  W, rows and Y are HOST arrays of nmat entries; W[m] is a
+ *   device f16[rows[m]][k], Y[m] a device f32[ncols][rows[m]]; rows[m] >= 0.
+ *   X : device, f16[ncols][k].  1 <= k <= BM_MAX_K, ncols >= 0.
+ */
+int bm_f16_matmul_multi(int nmat, const uint16_t *const *W, const int64_t *rows, int64_t k,
+                        const uint16_t *X, int64_t ncols, float *const *Y, bm_stream_t stream);
+
 /* Size of the static device scratch that bm_f16_matmul_noalloc uses (8 MiB). */
 #define BM_NOALLOC_SCRATCH_BYTES (8u << 20)
 

@@ -195,3 +195,19 @@ def test_rms_norm_host_checks(L):
     assert f(x, g, 4, 64, 1e-5, x + 4, h, None) == 1                      # out overlaps x, not in place
     assert f(x, g, 4, 64, 1e-5, o, x + 256, None) == 1                    # h overlaps x
     assert f(x, g, 4, 64, 1e-5, g, None, None) == 1                       # out overlaps g
+
+
+def test_matmul_multi_host_checks(L):
+    f = L.bm_f16_matmul_multi
+    W = (C.c_void_p * 2)(A, A + 2 ** 20)
+    Y = (C.c_void_p * 2)(A + 2 ** 24, A + 2 ** 25)
+    rows = (C.c_int64 * 2)(16, 16)
+    X = A + 2 ** 26
+    assert f(0, W, rows, 64, X, 8, Y, None) == 1
+    assert f(5, W, rows, 64, X, 8, Y, None) == 1
+    assert f(2, None, rows, 64, X, 8, Y, None) == 1
+    assert f(2, W, rows, 0, X, 8, Y, None) == 1
+    assert f(2, W, rows, 64, X + 2, 8, Y, None) == 2                    # X misaligned
+    Yo = (C.c_void_p * 2)(A + 2 ** 24, A + 2 ** 24 + 64)                  # the outputs overlap
+    assert f(2, W, rows, 64, X, 8, Yo, None) == 1
+    assert f(2, W, rows, 64, X, 0, Y, None) == 0                        # no columns: nothing to do
