@@ -10,6 +10,7 @@ fallback: when libbm.so is missing the import fails.
 from __future__ import annotations
 
 import ctypes as C
+import threading
 import os
 
 import torch
@@ -19,7 +20,7 @@ from . import _build
 __all__ = [
     "BmError", "lib", "bm_to_f16", "bm_f16_matvec", "bm_f16_matvec_multi", "bm_f16_matvec_act", "bm_f16_matvec_norm", "bm_rms_norm_mul", "bm_f16_matmul", "bm_f16_matmul_multi", "bm_f16_matmul_noalloc",
     "bm_f16_logits", "bm_f16_get_rows", "bm_takes_sgemm", "bm_device_status", "bm_status_string", "bm_last_error",
-    "bm_selftest_wait_timeout", "bm_set_pdl", "bm_set_exact_sgemm_cols", "EXPORTS", "BM_MAX_K",
+    "bm_selftest_wait_timeout", "bm_set_pdl", "prepare", "Prepared", "bm_set_exact_sgemm_cols", "EXPORTS", "BM_MAX_K",
 ]
 
 BM_OK, BM_ERR_INVALID_ARG, BM_ERR_ALIGNMENT, BM_ERR_UNSUPPORTED_DEVICE, BM_ERR_CUDA, BM_ERR_TIMEOUT = range(6)
@@ -81,6 +82,53 @@ def _check(status: int, fn: str):
         raise BmError(status, fn)
 
 
+_tls = threading.local()
+
+
+def _call(fn_name: str, *args):
+    """Calls the library function, or, inside prepare(), records the marshalled call."""
+    rec = getattr(_tls, "record", None)
+    if rec is not None:
+        rec.append((getattr(lib(), fn_name), args, fn_name))
+        return
+    _check(getattr(lib(), fn_name)(*args), fn_name)
+
+
+class Prepared:
+    """Calls of this module recorded by prepare(), replayed with the same arguments."""
+
+    def __init__(self, calls, tensors):
+        self._calls = tuple(calls)
+        self._tensors = tuple(tensors)
+
+    def __len__(self):
+        return len(self._calls)
+
+    def __call__(self):
+        for fn, args, name in self._calls:
+            st = fn(*args)
+            if st != BM_OK:
+                raise BmError(st, name)
+
+
+def prepare(thunk) -> Prepared:
+    """Runs thunk() -- calls of this module -- once with every argument checked and
+    marshalled but nothing launched, and returns a callable that launches the same
+    calls with the same device pointers, sizes and streams (the stream of a call made
+    with stream=None is the current stream at prepare time).  For loops that repeat
+    the same calls (a decode step): a replay costs one C call per entry point, not
+    the per-call tensor checks.  The Prepared object holds every tensor the calls
+    point into (inputs and outputs, including outputs a wrapper allocated inside
+    thunk), so their memory stays in place while it lives."""
+    _tls.record, _tls.keep = [], []
+    try:
+        thunk()
+    finally:
+        calls, tensors = _tls.record, _tls.keep
+        _tls.record, _tls.keep = None, None
+    return Prepared(calls, tensors)
+
+
 def _stream(stream) -> int:
     if stream is None:
         return torch.cuda.current_stream().cuda_stream
@@ -99,6 +147,9 @@ def _dev(t: torch.Tensor, name: str, dtypes) -> int:
         raise TypeError("%s has dtype %s, expected one of %s" % (name, t.dtype, dtypes))
     if not t.is_contiguous():
         raise ValueError("%s must be contiguous" % name)
+    keep = getattr(_tls, "keep", None)
+    if keep is not None:
+        keep.append(t)  # a prepared call holds every tensor it points into
     return t.data_ptr()
 
 
@@ -112,8 +163,7 @@ def bm_to_f16(x: torch.Tensor, h: torch.Tensor | None = None, stream=None) -> to
         h = torch.empty(x.shape, dtype=torch.float16, device=x.device)
     if h.numel() != x.numel():
         raise ValueError("h must have x's size")
-    _check(lib().bm_to_f16(_dev(x, "x", (torch.float32,)), _dev(h, "h", _F16_LIKE), x.numel(), _stream(stream)),
-           "bm_to_f16")
+    _call("bm_to_f16", _dev(x, "x", (torch.float32,)), _dev(h, "h", _F16_LIKE), x.numel(), _stream(stream))
     return h
 
 
@@ -131,8 +181,8 @@ def bm_f16_matvec(W: torch.Tensor, x: torch.Tensor, y: torch.Tensor | None = Non
         y = torch.empty(rows, dtype=torch.float32, device=W.device)
     if y.numel() != rows:
         raise ValueError("y must have rows elements")
-    _check(lib().bm_f16_matvec(_dev(W, "W", _F16_LIKE), rows, k, _dev(x, "x", _F16_LIKE),
-                               _dev(y, "y", (torch.float32,)), _stream(stream)), "bm_f16_matvec")
+    _call("bm_f16_matvec", _dev(W, "W", _F16_LIKE), rows, k, _dev(x, "x", _F16_LIKE),
+                               _dev(y, "y", (torch.float32,)), _stream(stream))
     return y
 
 
@@ -150,8 +200,7 @@ def bm_f16_matvec_multi(Ws, x: torch.Tensor, ys=None, stream=None):
     wp = (C.c_void_p * max(n, 1))(*[_dev(W, "W", _F16_LIKE) for W in Ws])
     yp = (C.c_void_p * max(n, 1))(*[_dev(y, "y", (torch.float32,)) for y in ys])
     rows = (C.c_int64 * max(n, 1))(*[W.shape[0] for W in Ws])
-    _check(lib().bm_f16_matvec_multi(n, wp, rows, k, _dev(x, "x", _F16_LIKE), yp, _stream(stream)),
-           "bm_f16_matvec_multi")
+    _call("bm_f16_matvec_multi", n, wp, rows, k, _dev(x, "x", _F16_LIKE), yp, _stream(stream))
     return ys
 
 
@@ -174,8 +223,7 @@ def bm_f16_matvec_act(Ws, x: torch.Tensor, ys=None, h: torch.Tensor | None = Non
     yp = (C.c_void_p * max(n, 1))(*[_dev(y, "y", (torch.float32,)) for y in ys])
     rows = (C.c_int64 * max(n, 1))(*[W.shape[0] for W in Ws])
     hp = _dev(h, "h", _F16_LIKE) if h is not None else None
-    _check(lib().bm_f16_matvec_act(n, wp, rows, k, _dev(x, "x", (torch.float32,)), hp, yp, _stream(stream)),
-           "bm_f16_matvec_act")
+    _call("bm_f16_matvec_act", n, wp, rows, k, _dev(x, "x", (torch.float32,)), hp, yp, _stream(stream))
     return ys
 
 
@@ -205,8 +253,8 @@ def bm_f16_matvec_norm(Ws, x: torch.Tensor, g: torch.Tensor, eps: float, ys=None
     rows = (C.c_int64 * max(n, 1))(*[W.shape[0] for W in Ws])
     hp = _dev(h, "h", _F16_LIKE) if h is not None else None
     np_ = _dev(n_out, "n_out", (torch.float32,)) if n_out is not None else None
-    _check(lib().bm_f16_matvec_norm(n, wp, rows, k, _dev(x, "x", (torch.float32,)), _dev(g, "g", (torch.float32,)),
-                                    float(eps), np_, hp, yp, _stream(stream)), "bm_f16_matvec_norm")
+    _call("bm_f16_matvec_norm", n, wp, rows, k, _dev(x, "x", (torch.float32,)), _dev(g, "g", (torch.float32,)),
+                                    float(eps), np_, hp, yp, _stream(stream))
     return ys
 
 
@@ -230,8 +278,8 @@ def bm_rms_norm_mul(x: torch.Tensor, g: torch.Tensor, eps: float, out=None, h=No
             raise ValueError(name + " must have as many elements as x")
     op = _dev(out, "out", (torch.float32,)) if out is not None else None
     hp = _dev(h, "h", _F16_LIKE) if h is not None else None
-    _check(lib().bm_rms_norm_mul(_dev(x, "x", (torch.float32,)), _dev(g, "g", (torch.float32,)), nrows, k,
-                                 float(eps), op, hp, _stream(stream)), "bm_rms_norm_mul")
+    _call("bm_rms_norm_mul", _dev(x, "x", (torch.float32,)), _dev(g, "g", (torch.float32,)), nrows, k,
+                                 float(eps), op, hp, _stream(stream))
     return out, h
 
 
@@ -246,9 +294,8 @@ def _product(fn_name: str, W, X, Y, stream):
         Y = torch.empty((ncols, rows), dtype=torch.float32, device=W.device)
     if Y.numel() != rows * ncols:
         raise ValueError("Y must have ncols*rows elements")
-    fn = getattr(lib(), fn_name)
-    _check(fn(_dev(W, "W", _F16_LIKE), rows, k, _dev(X, "X", _F16_LIKE), ncols, _dev(Y, "Y", (torch.float32,)),
-              _stream(stream)), fn_name)
+    _call(fn_name, _dev(W, "W", _F16_LIKE), rows, k, _dev(X, "X", _F16_LIKE), ncols, _dev(Y, "Y", (torch.float32,)),
+          _stream(stream))
     return Y
 
 
@@ -275,8 +322,7 @@ def bm_f16_matmul_multi(Ws, X, Ys=None, stream=None):
     wp = (C.c_void_p * max(n, 1))(*[_dev(W, "W", _F16_LIKE) for W in Ws])
     yp = (C.c_void_p * max(n, 1))(*[_dev(Y, "Y", (torch.float32,)) for Y in Ys])
     rows = (C.c_int64 * max(n, 1))(*[W.shape[0] for W in Ws])
-    _check(lib().bm_f16_matmul_multi(n, wp, rows, k, _dev(X, "X", _F16_LIKE), ncols, yp, _stream(stream)),
-           "bm_f16_matmul_multi")
+    _call("bm_f16_matmul_multi", n, wp, rows, k, _dev(X, "X", _F16_LIKE), ncols, yp, _stream(stream))
     return Ys
 
 
@@ -305,8 +351,8 @@ def bm_f16_get_rows(E, ids, out=None, stream=None):
         out = torch.empty((n, hidden), dtype=torch.float32, device=E.device)
     if out.numel() != n * hidden:
         raise ValueError("out must have n*hidden elements")
-    _check(lib().bm_f16_get_rows(_dev(E, "E", _F16_LIKE), vocab, hidden, _dev(ids, "ids", (torch.int32,)), n,
-                                 _dev(out, "out", (torch.float32,)), _stream(stream)), "bm_f16_get_rows")
+    _call("bm_f16_get_rows", _dev(E, "E", _F16_LIKE), vocab, hidden, _dev(ids, "ids", (torch.int32,)), n,
+                                 _dev(out, "out", (torch.float32,)), _stream(stream))
     return out
 
 

@@ -413,6 +413,37 @@ bool make_row_map(CUtensorMap *map, const uint16_t *W, int64_t rows, int64_t k)
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Encoding a tensor map is a driver call on every product; a decode step makes the
+// same products with the same weights over and over.  A small direct-mapped cache per
+// host thread keeps the maps made: a map depends only on the base address and the
+// sizes it was made from, so an entry is valid for as long as its key matches.
+struct RowMapEntry {
+    CUtensorMap map;
+    const void *W;
+    int64_t rows, k;
+    bool valid;
+};
+constexpr int kRowMapCache = 64;
+thread_local RowMapEntry g_row_maps[kRowMapCache];
+
+bool row_map_cached(CUtensorMap *map, const uint16_t *W, int64_t rows, int64_t k)
+{
+    const uint64_t h = (reinterpret_cast<uint64_t>(W) >> 8) * 0x9E3779B97F4A7C15ull ^ (uint64_t)rows * 0xC2B2AE3Dull ^
+                       (uint64_t)k;
+    RowMapEntry &e = g_row_maps[(h >> 32) & (kRowMapCache - 1)];
+    if (e.valid && e.W == W && e.rows == rows && e.k == k) {
+        *map = e.map;
+        return true;
+    }
+    if (!make_row_map(map, W, rows, k)) return false;
+    e.map = *map;
+    e.W = W;
+    e.rows = rows;
+    e.k = k;
+    e.valid = true;
+    return true;
+}
+
 constexpr int kMaxDevices = 64;
 std::once_flag g_attr_once[kMaxDevices];
 
@@ -439,7 +470,7 @@ int launch_gemv_stream(const VecdotJob &vj, const float *x_f32, uint16_t *h_out,
     job.gbeg[0] = 0;
     for (int m = 0; m < vj.nmat; m++) {
         if (vj.rows[m] > 0x7fffffffLL) return fail(BM_ERR_INVALID_ARG, "vec_dot: rows must be below 2^31");
-        if (!make_row_map(&job.map[m], vj.W[m], vj.rows[m], vj.k))
+        if (!row_map_cached(&job.map[m], vj.W[m], vj.rows[m], vj.k))
             return fail(BM_ERR_CUDA, "vec_dot: tensor map encoding failed");
         job.y[m] = vj.y[m];
         job.rows[m] = (int)vj.rows[m];
