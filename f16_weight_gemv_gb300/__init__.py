@@ -20,7 +20,8 @@ from . import _build
 __all__ = [
     "BmError", "lib", "bm_to_f16", "bm_f16_matvec", "bm_f16_matvec_multi", "bm_f16_matvec_act", "bm_f16_matvec_norm", "bm_rms_norm_mul", "bm_f16_matmul", "bm_f16_matmul_multi", "bm_f16_matmul_noalloc",
     "bm_f16_logits", "bm_f16_get_rows", "bm_takes_sgemm", "bm_device_status", "bm_status_string", "bm_last_error",
-    "bm_selftest_wait_timeout", "bm_set_pdl", "prepare", "Prepared", "bm_set_exact_sgemm_cols", "EXPORTS", "BM_MAX_K",
+    "bm_selftest_wait_timeout", "bm_set_pdl", "prepare", "Prepared", "bm_set_exact_sgemm_cols", "bm_set_stream_k", "EXPORTS",
+    "BM_MAX_K",
 ]
 
 BM_OK, BM_ERR_INVALID_ARG, BM_ERR_ALIGNMENT, BM_ERR_UNSUPPORTED_DEVICE, BM_ERR_CUDA, BM_ERR_TIMEOUT = range(6)
@@ -45,6 +46,7 @@ EXPORTS = {
     "bm_device_status": (_i, [_vp]),
     "bm_set_pdl": (_i, [_i]),
     "bm_set_exact_sgemm_cols": (_i, [_i]),
+    "bm_set_stream_k": (_i, [_i]),
     "bm_selftest_wait_timeout": (_i, [_vp, _vp, _vp, _vp]),
     "bm_status_string": (C.c_char_p, [_i]),
     "bm_last_error": (C.c_char_p, []),
@@ -374,6 +376,12 @@ def bm_set_exact_sgemm_cols(ncols: int) -> int:
     """tinyBLAS-path products of at most `ncols` columns (0..8) take the bit-exact
     CUDA-core kernel, wider ones the tensor cores; returns the old setting."""
     return int(lib().bm_set_exact_sgemm_cols(int(ncols)))
+
+
+def bm_set_stream_k(mode: int) -> int:
+    """Balanced k ranges for the tensor-core products: -1 where the time model
+    predicts them faster (default), 0 never, 1 always; returns the old setting."""
+    return int(lib().bm_set_stream_k(int(mode)))
 
 
 def bm_status_string(status: int) -> str:

@@ -34,6 +34,7 @@ std::once_flag g_once[kMaxDevices];
 int g_dev_status[kMaxDevices];
 std::atomic<int> g_pdl{0};
 std::atomic<int> g_exact_cols{2};  // bm_set_exact_sgemm_cols
+std::atomic<int> g_stream_k{-1};   // bm_set_stream_k
 unsigned int *g_err_addr[kMaxDevices];
 std::once_flag g_err_once[kMaxDevices];
 }  // namespace
@@ -53,6 +54,7 @@ unsigned int *device_error_word()
 }
 
 bool pdl_enabled() { return g_pdl.load(std::memory_order_relaxed) != 0; }
+int stream_k_mode() { return g_stream_k.load(std::memory_order_relaxed); }
 
 int read_device_error(cudaStream_t s)
 {
@@ -457,6 +459,12 @@ int bm_set_exact_sgemm_cols(int ncols)
 {
     clear_error();
     return g_exact_cols.exchange(std::max(0, std::min(ncols, kSgemmStreamMaxCols)));
+}
+
+int bm_set_stream_k(int mode)
+{
+    clear_error();
+    return g_stream_k.exchange(mode < 0 ? -1 : mode > 0 ? 1 : 0);
 }
 
 int bm_device_status(bm_stream_t stream)

@@ -26,6 +26,7 @@ unsigned int *device_error_word();
 
 // Whether products are launched with programmatic dependent launch (bm_set_pdl).
 bool pdl_enabled();
+int stream_k_mode();  // bm_set_stream_k: -1 by the time model, 0 never, 1 always
 
 // Up to four matrices that share one activation (the fused Q/K/V or gate/up
 // products), or one matrix with several activation columns.

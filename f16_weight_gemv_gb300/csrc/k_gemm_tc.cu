@@ -35,8 +35,26 @@
 // programmatic dependent launch, sums the S partials of every element in split
 // order 0..S-1 across the whole GPU -- so the result does not depend on which unit
 // finished last, and the reduction runs with every SM's memory parallelism instead
-// of in the tail of a few units.  MT and S come from a model of the predicted time
-// (waves x per-unit time + the reduction, calibrated by measurements).
+// of in the tail of a few units.
+//
+// Balanced k ranges (stream-K, Osama et al., PPoPP 2023): when whole units leave
+// part of the last wave idle, the CTAs are dealt to the column tiles in turn (CTA c
+// serves column tile c % nt, so neighbouring CTAs read the same W rows at the same
+// time and share them through L2, as in the unit order above), and each column's
+// k-blocks, laid end to end (row unit after row unit, k fastest), are cut into one
+// contiguous range per CTA of equal length.  A CTA walks its range from the top
+// down, so the piece it shares with
+// the CTA above (the start of a tile that continues there) comes first and is
+// written to the CTA's own partial slot early; the piece it shares with the CTAs
+// below (the end of a tile that started there) comes last, and the CTA that holds
+// a tile's last k-block owns the tile: it adds the lower pieces in k order to its
+// own accumulators and stores Y.  Each epilogue warp publishes its part of a piece
+// with its own flag (a 64-bit token unique to the launch; the owner resets the
+// flag to zero after reading), so no barrier spans warps and every wait is bounded.
+// A CTA only ever waits for CTAs of lower index, which the GPU starts first.
+// MT, the tile width, S and the mode come from a model of the predicted time (waves
+// x per-unit time, plus the reduction or the owners' reads, calibrated by
+// measurements).
 //
 // Out-of-range rows, columns and the k % 64 end are zero-filled by TMA and add
 // +0 exactly.  Every mbarrier wait is bounded by the global timer; on a
@@ -51,6 +69,8 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
+#include <chrono>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -68,6 +88,8 @@ constexpr int kTileABytes = kBM * kBK * 2;  // 16 KB
 constexpr int kMaxStages = 8;
 constexpr int kMaxSplits = 8;
 constexpr int kMaxMats = 4;       // matrices sharing one activation in one launch
+constexpr int kWarpChunks = 4;    // 32-column chunks per epilogue warp and row tile (bn <= 256)
+constexpr int kOwnerDepth = 4;    // 4 KB blocks in flight per epilogue warp while an owner reads pieces
 constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;  // 2 s
 
 // Up to kMaxMats matrices W[m] (rows[m] x k) times one activation X (ncols x k), each
@@ -90,6 +112,15 @@ struct GemmParams {
     int nbuf;                 // TMEM accumulator sets: 2 (double-buffered) or 1
     int splits;
     int stages;
+    // balanced k ranges (sk != 0; splits == 1): CTA c serves column tile c % nt and
+    // takes iterations [iters * g / G, iters * (g + 1) / G) of that column's
+    // iters = mtu x num_kb (row unit after row unit, k fastest), g = c / nt, G = grid / nt
+    int sk;
+    int64_t iters;
+    float *skws;                 // one partial slot per CTA: 4 KB blocks [m][epilogue warp][chunk][col][lane]
+    int64_t slot_floats;         // MT * kEpiWarps * kWarpChunks * 1024
+    unsigned long long *flags;   // [CTA][epilogue warp]: token once the slot's part is written
+    unsigned long long token;
     unsigned long long timeout_ns;
     unsigned int *err;        // device error word
     int withhold_first_load;  // self-test only: the producer never fills its first stage
@@ -231,6 +262,195 @@ __device__ __forceinline__ Unit unit_of(const GemmParams &p, int u)
     return x;
 }
 
+// What the epilogue does with a segment's accumulators.
+enum SegRole {
+    kWhole = 0,  // all k-blocks of the tile: store Y
+    kSplit = 1,  // one k-split: store the partial tile for k_splitk_reduce
+    kPiece = 2,  // balanced ranges, not the tile's last k-block: this CTA's partial slot
+    kOwner = 3,  // balanced ranges, the tile's last k-block after lower CTAs' pieces
+};
+
+// One stretch of k-blocks of one unit: what the producer, the MMA warp and the
+// epilogue walk, in the same order.
+struct Seg {
+    Unit x;
+    int kb0, kb1;
+    int role;
+    int cfirst, ncon;  // kOwner: CTAs cfirst + i * nt (i < ncon) hold the tile's earlier k-blocks
+};
+
+struct SegIter {
+    int64_t beg, end;  // balanced ranges: this CTA's iterations
+    int64_t t;         // the next tile (balanced ranges, walked downwards) or unit
+};
+
+__device__ __forceinline__ void seg_begin(const GemmParams &p, SegIter &it)
+{
+    if (p.sk) {
+        const int64_t G = gridDim.x / p.nt, g = blockIdx.x / p.nt;
+        it.beg = p.iters * g / G;
+        it.end = p.iters * (g + 1) / G;
+        it.t = it.end > it.beg ? (it.end - 1) / p.num_kb : -1;
+    } else {
+        it.beg = it.end = 0;
+        it.t = blockIdx.x;
+    }
+}
+
+// The range (of G per column tile) that holds iteration i: the largest g with
+// floor(iters * g / G) <= i.
+__device__ __forceinline__ int range_of(const GemmParams &p, int64_t i)
+{
+    const int64_t G = gridDim.x / p.nt;
+    return (int)(((i + 1) * G + p.iters - 1) / p.iters) - 1;
+}
+
+template <int MT>
+__device__ __forceinline__ bool seg_next(const GemmParams &p, SegIter &it, Seg &sg)
+{
+    if (p.sk) {
+        // row unit it.t of column tile blockIdx.x % nt, walked downwards
+        if (it.t < 0 || it.t < it.beg / p.num_kb) return false;
+        const int64_t t0 = it.t * p.num_kb;
+        const int n = (int)(blockIdx.x % p.nt);
+        sg.x = unit_of<MT>(p, (int)it.t * p.nt + n);
+        sg.kb0 = (int)(max(it.beg, t0) - t0);
+        sg.kb1 = (int)(min(it.end, t0 + p.num_kb) - t0);
+        sg.cfirst = 0;
+        sg.ncon = 0;
+        if (sg.kb0 == 0 && sg.kb1 == p.num_kb) {
+            sg.role = kWhole;
+        } else if (sg.kb1 < p.num_kb) {
+            sg.role = kPiece;  // the top of this CTA's range; at most one per CTA
+        } else {
+            sg.role = kOwner;
+            const int g0 = range_of(p, t0);
+            sg.cfirst = g0 * p.nt + n;
+            sg.ncon = (int)(blockIdx.x / p.nt) - g0;
+        }
+        it.t--;
+        return true;
+    }
+    const int units = p.mtu * p.nt * p.splits;
+    if (it.t >= units) return false;
+    sg.x = unit_of<MT>(p, (int)it.t);
+    sg.kb0 = sg.x.kb0;
+    sg.kb1 = sg.x.kb1;
+    sg.role = p.splits > 1 ? kSplit : kWhole;
+    sg.cfirst = 0;
+    sg.ncon = 0;
+    it.t += gridDim.x;
+    return true;
+}
+
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long *f)
+{
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(f) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release_u64(unsigned long long *f, unsigned long long v)
+{
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(f), "l"(v) : "memory");
+}
+
+// 16-byte asynchronous global -> shared copy (through L2 only) and its groups.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// Waits until *f holds `token`; gives up on the CTA's abort flag or after timeout_ns
+// (raising the flag and recording BM_ERR_TIMEOUT).
+__device__ __forceinline__ bool flag_wait(const unsigned long long *f, unsigned long long token,
+                                          volatile int *abort_flag, unsigned long long timeout_ns,
+                                          unsigned int *err_word)
+{
+    if (ld_acquire_u64(f) == token) return true;
+    const unsigned long long t0 = now_ns();
+    while (true) {
+        __nanosleep(100);
+        if (ld_acquire_u64(f) == token) return true;
+        if (*abort_flag) return false;
+        if (now_ns() - t0 > timeout_ns) {
+            *abort_flag = 1;
+            atomicExch(err_word, dev::kTimeoutStatus);
+            return false;
+        }
+    }
+}
+
+// Float offset of the 4 KB block (32 columns x 32 rows, column-major) that epilogue
+// warp ew writes for its chunk j of row tile m in a partial slot.
+__device__ __forceinline__ size_t slot_block(int m, int ew, int j)
+{
+    return ((size_t)(m * kEpiWarps + ew) * kWarpChunks + j) * 1024;
+}
+
+// The owner's epilogue of a tile whose earlier k-blocks lie in CTAs cfirst + i * nt:
+// for each (row tile m, chunk j) of this warp, the accumulators plus every lower piece's
+// block in CTA order, stored to Y.  The blocks come through the operand ring, idle by
+// now (this is the CTA's last segment and its MMAs have completed): each warp owns
+// kOwnerDepth 4 KB buffers there and keeps that many blocks in flight with cp.async.
+template <int MT>
+__device__ __forceinline__ void owner_epilogue(const GemmParams &p, const Seg &sg, uint32_t tacc, uint32_t ring_u32,
+                                               uint8_t *smem_raw, int ew, int half, int quarter, int lane, int nch)
+{
+    // the ring's last readers were the tensor cores (async proxy); these are generic writes
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    const int ncon = sg.ncon;
+    const int jobs = MT * nch * ncon;  // (m, j, piece), piece fastest
+    const uint32_t buf_u32 = ring_u32 + (uint32_t)ew * (kOwnerDepth * 4096u);
+    const float *buf = reinterpret_cast<const float *>(smem_raw + (buf_u32 - smem_u32(smem_raw)));
+    auto issue = [&](int n) {
+        if (n < jobs) {
+            const int cc = sg.cfirst + (n % ncon) * p.nt, mj = n / ncon;
+            const float *src = p.skws + (size_t)cc * p.slot_floats + slot_block(mj / nch, ew, mj % nch);
+            const uint32_t dst = buf_u32 + (uint32_t)(n % kOwnerDepth) * 4096u;
+#pragma unroll
+            for (int r = 0; r < 8; r++) cp_async16(dst + (uint32_t)(r * 32 + lane) * 16u, src + (r * 32 + lane) * 4);
+        }
+        cp_async_commit();  // one group per job slot, empty past the end: the wait count stays fixed
+    };
+#pragma unroll
+    for (int n = 0; n < kOwnerDepth; n++) issue(n);
+    const int rows = pick(p.rows, sg.x.mat);
+    float *const Y = pick(p.Y, sg.x.mat);
+    float acc[32];
+    for (int n = 0; n < jobs; n++) {
+        const int mj = n / ncon, m = mj / nch, j = mj % nch, c0 = 32 * (2 * j + half);
+        if (n % ncon == 0) {
+            uint32_t v[32];
+            tmem_ld32(tacc + (uint32_t)(m * p.bn_alloc) + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c0, v);
+            tmem_wait_ld(v);
+#pragma unroll
+            for (int q = 0; q < 32; q++) acc[q] = __uint_as_float(v[q]);
+        }
+        cp_async_wait<kOwnerDepth - 1>();  // this lane's copies of job n have landed
+        __syncwarp();                      // and every other lane's
+        const float *bk = buf + (n % kOwnerDepth) * 1024;
+#pragma unroll
+        for (int q = 0; q < 32; q++) acc[q] += bk[q * 32 + lane];
+        __syncwarp();  // the buffer is read before it is refilled
+        issue(n + kOwnerDepth);
+        if (n % ncon == ncon - 1) {
+            const int row = sg.x.m0 + m * kBM + quarter * 32 + lane;
+            if (row < rows) {
+#pragma unroll
+                for (int q = 0; q < 32; q++) {
+                    const int col = sg.x.n0 + c0 + q;
+                    if (c0 + q < p.bn && col < p.ncols) Y[(size_t)col * rows + row] = acc[q];
+                }
+            }
+        }
+    }
+    cp_async_wait<0>();
+}
+
 // MT = 1: a unit is 128 rows x BN columns.  MT = 2: 256 rows x BN columns, two
 // M = 128 MMAs per k-step sharing the X tile, so each k-block moves 64 KB of operands
 // for twice the work (32 KB per 128 x 256 x 64 block instead of 48 KB).  The
@@ -256,7 +476,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t stage_bytes = MT * kTileABytes + (uint32_t)p.bn * kBK * 2;
     const uint32_t tmem_cols = (uint32_t)(p.nbuf * MT * p.bn_alloc);
     volatile int *abort_v = &abort_flag;
-    const int units = p.mtu * p.nt * p.splits;
 
     if (threadIdx.x == 0) {
         // the TMA unit reads the tensor maps on first use: fetch them while the set-up runs
@@ -307,9 +526,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 pend_kb[q] * kBK, pend_n0[q], smem_u32(&full_bar[pend_s[q]]));
                 pend = 0;
             };
-            for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-                const Unit x = unit_of<MT>(p, u);
-                for (int kb = x.kb0; kb < x.kb1; kb++, t++) {
+            SegIter it;
+            seg_begin(p, it);
+            Seg sg;
+            while (ok && seg_next<MT>(p, it, sg)) {
+                const Unit &x = sg.x;
+                for (int kb = sg.kb0; kb < sg.kb1; kb++, t++) {
                     const int s = t % p.stages;
                     const uint32_t ph = (uint32_t)(t / p.stages) & 1u;
                     if (!dev::mbar_wait(smem_u32(&empty_bar[s]), ph ^ 1u, abort_v, p.timeout_ns, p.err)) {
@@ -342,14 +564,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t idesc = instr_desc_f16(kBM, p.bn);
             int t = 0, i = 0;
             bool ok = true;
-            for (int u = blockIdx.x; u < units && ok; u += gridDim.x, i++) {
-                const Unit x = unit_of<MT>(p, u);
+            SegIter it;
+            seg_begin(p, it);
+            Seg sg;
+            for (; ok && seg_next<MT>(p, it, sg); i++) {
                 const int b = i % p.nbuf;
                 const uint32_t use = (uint32_t)(i / p.nbuf);  // how many times set b was used before
                 if (!dev::mbar_wait(smem_u32(&acc_empty[b]), (use & 1u) ^ 1u, abort_v, p.timeout_ns, p.err)) break;
                 tc_fence_after();
                 const uint32_t d = tmem_base + (uint32_t)(b * MT * p.bn_alloc);
-                for (int kb = x.kb0; kb < x.kb1; kb++, t++) {
+                for (int kb = sg.kb0; kb < sg.kb1; kb++, t++) {
                     const int s = t % p.stages;
                     const uint32_t ph = (uint32_t)(t / p.stages) & 1u;
                     if (!dev::mbar_wait(smem_u32(&full_bar[s]), ph, abort_v, p.timeout_ns, p.err)) {
@@ -364,7 +588,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int m = 0; m < MT; m++)
                             mma_f16(d + (uint32_t)(m * p.bn_alloc), smem_desc_sw128(a_addr + m * kTileABytes + kk * kUmmaK * 2),
-                                    smem_desc_sw128(b_addr + kk * kUmmaK * 2), idesc, (kb > x.kb0 || kk > 0) ? 1u : 0u);
+                                    smem_desc_sw128(b_addr + kk * kUmmaK * 2), idesc, (kb > sg.kb0 || kk > 0) ? 1u : 0u);
                     mma_commit(smem_u32(&empty_bar[s]));  // the stage is free once these MMAs have read it
                 }
                 if (!ok) break;
@@ -378,52 +602,88 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int quarter = warp & 3;                 // TMEM lanes 32*quarter .. +31 (warp % 4 rule)
         const int half = (warp - 2) >> 2;             // this warp's 32-column chunks: 32 * (2j + half)
         const int rloc = quarter * 32 + lane;         // row inside a 128-row tile
+        const int ew = warp - 2;                      // epilogue warp: its flag in a CTA's row of flags
         int i = 0;
-        for (int u = blockIdx.x; u < units; u += gridDim.x, i++) {
-            const Unit x = unit_of<MT>(p, u);
+        SegIter it;
+        seg_begin(p, it);
+        Seg sg;
+        for (; seg_next<MT>(p, it, sg); i++) {
+            const Unit &x = sg.x;
             const int b = i % p.nbuf;
             const uint32_t use = (uint32_t)(i / p.nbuf);
             if (!dev::mbar_wait_warp(smem_u32(&acc_full[b]), use & 1u, abort_v, p.timeout_ns, p.err)) break;
             tc_fence_after();
-            for (int m = 0; m < MT; m++) {
-                const uint32_t taddr =
-                    tmem_base + (uint32_t)((b * MT + m) * p.bn_alloc) + ((uint32_t)(quarter * 32) << 16);
-                const int row = x.m0 + m * kBM + rloc;
-                const int rows = pick(p.rows, x.mat);
-                float *const Y = pick(p.Y, x.mat);
-                const int tile = x.tile0 + m * p.nt;
-                float *ws_unit = p.splits > 1 ? p.ws + ((size_t)tile * p.splits + x.s) * (size_t)p.bn * kBM : nullptr;
-                // one chunk's 32 values of this row: to the split's partial tile, or to Y
-                auto store = [&](const uint32_t(&v)[32], int c) {
-                    if (p.splits > 1) {
+            // this warp's 32-column chunks of a row tile: columns 32 * (2j + half), j < nch
+            const int nch = (p.bn / 32 - half + 1) / 2 + ((p.bn % 32) && (p.bn / 32) % 2 == half ? 1 : 0);
+            if (sg.role == kOwner) {
+                // The tile's last k-blocks: wait, warp by warp, for the same warp's part of
+                // every lower CTA's piece (bounded; a give-up leaves Y unwritten and raised),
+                // then add the pieces in k order to the accumulators and store Y.
+                bool have = true;
+                for (int i = 0; i < sg.ncon && have; i++)
+                    have = flag_wait(p.flags + (size_t)(sg.cfirst + i * p.nt) * kEpiWarps + ew, p.token, abort_v,
+                                     p.timeout_ns, p.err);
+                have = __all_sync(0xffffffffu, have);
+                if (have) {
+                    owner_epilogue<MT>(p, sg, tmem_base + (uint32_t)(b * MT * p.bn_alloc), ring_u32, smem_raw, ew, half,
+                                       quarter, lane, nch);
+                    // the lower pieces are read: their flags go back to zero for the next launch
+                    __syncwarp();
+                    if (lane == 0)
+                        for (int i = 0; i < sg.ncon; i++) p.flags[(size_t)(sg.cfirst + i * p.nt) * kEpiWarps + ew] = 0ull;
+                }
+            } else {
+                for (int m = 0; m < MT; m++) {
+                    const uint32_t taddr =
+                        tmem_base + (uint32_t)((b * MT + m) * p.bn_alloc) + ((uint32_t)(quarter * 32) << 16);
+                    const int row = x.m0 + m * kBM + rloc;
+                    const int rows = pick(p.rows, x.mat);
+                    float *const Y = pick(p.Y, x.mat);
+                    const int tile = x.tile0 + m * p.nt;
+                    float *ws_unit =
+                        sg.role == kSplit ? p.ws + ((size_t)tile * p.splits + x.s) * (size_t)p.bn * kBM : nullptr;
+                    // one chunk's 32 values of this row: to the split's partial tile, to this
+                    // CTA's partial slot, or to Y
+                    auto store = [&](const uint32_t(&v)[32], int c) {
+                        if (sg.role == kSplit) {
 #pragma unroll
-                        for (int q = 0; q < 32; q++)
-                            if (c + q < p.bn) ws_unit[(size_t)(c + q) * kBM + rloc] = __uint_as_float(v[q]);
-                    } else if (row < rows) {
+                            for (int q = 0; q < 32; q++)
+                                if (c + q < p.bn) ws_unit[(size_t)(c + q) * kBM + rloc] = __uint_as_float(v[q]);
+                        } else if (sg.role == kPiece) {
+                            float *blk = p.skws + (size_t)blockIdx.x * p.slot_floats + slot_block(m, ew, (c / 32 - half) / 2);
 #pragma unroll
-                        for (int q = 0; q < 32; q++) {
-                            const int col = x.n0 + c + q;
-                            if (c + q < p.bn && col < p.ncols) Y[(size_t)col * rows + row] = __uint_as_float(v[q]);
+                            for (int q = 0; q < 32; q++) blk[q * 32 + lane] = __uint_as_float(v[q]);
+                        } else if (row < rows) {
+#pragma unroll
+                            for (int q = 0; q < 32; q++) {
+                                const int col = x.n0 + c + q;
+                                if (c + q < p.bn && col < p.ncols) Y[(size_t)col * rows + row] = __uint_as_float(v[q]);
+                            }
+                        }
+                    };
+                    // two chunks in flight: the next chunk's TMEM load overlaps this chunk's stores
+                    uint32_t va[32], vb[32];
+                    if (nch > 0) {
+                        tmem_ld32(taddr + (uint32_t)(32 * half), va);
+                        tmem_wait_ld(va);
+                    }
+                    for (int j = 0; j < nch; j += 2) {
+                        const int ca = 32 * (2 * j + half), cb = ca + 64;
+                        if (j + 1 < nch) tmem_ld32(taddr + (uint32_t)cb, vb);
+                        store(va, ca);
+                        if (j + 1 < nch) {
+                            tmem_wait_ld(vb);
+                            if (j + 2 < nch) tmem_ld32(taddr + (uint32_t)(cb + 64), va);
+                            store(vb, cb);
+                            if (j + 2 < nch) tmem_wait_ld(va);
                         }
                     }
-                };
-                // two chunks in flight: the next chunk's TMEM load overlaps this chunk's stores
-                const int nch = (p.bn / 32 - half + 1) / 2 + ((p.bn % 32) && (p.bn / 32) % 2 == half ? 1 : 0);
-                uint32_t va[32], vb[32];
-                if (nch > 0) {
-                    tmem_ld32(taddr + (uint32_t)(32 * half), va);
-                    tmem_wait_ld(va);
                 }
-                for (int j = 0; j < nch; j += 2) {
-                    const int ca = 32 * (2 * j + half), cb = ca + 64;
-                    if (j + 1 < nch) tmem_ld32(taddr + (uint32_t)cb, vb);
-                    store(va, ca);
-                    if (j + 1 < nch) {
-                        tmem_wait_ld(vb);
-                        if (j + 2 < nch) tmem_ld32(taddr + (uint32_t)(cb + 64), va);
-                        store(vb, cb);
-                        if (j + 2 < nch) tmem_wait_ld(va);
-                    }
+                if (sg.role == kPiece) {
+                    // this warp's part of the slot is written: publish it for the owner
+                    __threadfence();
+                    __syncwarp();
+                    if (lane == 0) st_release_u64(p.flags + (size_t)blockIdx.x * kEpiWarps + ew, p.token);
                 }
             }
             // hand the accumulators back to the MMA warp
@@ -577,6 +837,38 @@ double plan_us(int64_t units_per_split, int64_t tiles128, int num_kb, int bn, in
     return us;
 }
 
+// Balanced k ranges, calibrated on GB300 with an L2 flush before each product: with
+// every SM busy a k-block takes longer than in the whole-tile plans (0.55 / 0.85 us
+// for 128- / 256-row units); a CTA writes its piece while every other CTA writes
+// theirs (about 5.5 MB/us in all), and with one TMEM set its next MMAs wait for
+// that; an owner reads each lower piece at about 0.15 MB/us.  Where the time
+// model is free to choose (bm_set_stream_k(-1)) the balanced plan must be predicted
+// 5 % faster than the best other plan: measured gains were small and the model is
+// coarse.
+constexpr double kSkKblockUs[3] = {0.0, 0.55, 0.85};
+constexpr double kSkFixedUs = 1.0;
+constexpr double kSkStoreBytesPerUs = 5.5e6;  // all CTAs' partial-tile stores at once
+constexpr double kSkOverlap = 0.3;            // share of that hidden behind MMAs with two TMEM sets
+constexpr double kSkReadBytesPerUs = 1.5e5;   // one SM's piece loads
+constexpr double kSkMargin = 0.95;
+
+// Predicted time of balanced ranges over `units` row units of MT * 128 rows of each of
+// nt column tiles, `ctas` CTAs per column tile; nbuf TMEM accumulator sets.
+double plan_sk_us(int64_t units, int num_kb, int bn, int mt, int ctas, int64_t nt, int nbuf)
+{
+    const int64_t iters = units * num_kb;
+    const int64_t per = (iters + ctas - 1) / ctas;
+    double us = (double)per * kSkKblockUs[mt];
+    const bool aligned = iters % ctas == 0 && per % num_kb == 0;  // every range whole tiles
+    if (!aligned) {
+        const double slot = (double)mt * kBM * bn * 4.0;
+        const double lower = std::ceil((double)num_kb / (double)per);  // pieces an owner adds, at most
+        const double write = (double)ctas * nt * slot / kSkStoreBytesPerUs;
+        us += kSkFixedUs + (nbuf == 1 ? write : kSkOverlap * write) + lower * slot / kSkReadBytesPerUs;
+    }
+    return us;
+}
+
 constexpr int kMaxDevices = 64;
 std::once_flag g_attr_once[kMaxDevices][2];
 std::once_flag g_pool_once[kMaxDevices];
@@ -602,6 +894,28 @@ cudaMemPool_t workspace_pool(int dev_id)
     return g_pool[dev_id];
 }
 
+// Balanced ranges' workspace: the CTAs' partial slots, then their flags.
+size_t sk_flags_offset(int grid, int64_t slot_floats)
+{
+    return ((size_t)grid * (size_t)slot_floats * sizeof(float) + 255) / 256 * 256;
+}
+
+// A 64-bit value for the flags of one launch: never zero, and unique within the
+// process (a counter through the splitmix64 finaliser, seeded per process), so no
+// value left in reused workspace memory by another launch can stand for it.
+unsigned long long next_token()
+{
+    static std::atomic<unsigned long long> seq{0};
+    static const unsigned long long seed =
+        (unsigned long long)std::chrono::steady_clock::now().time_since_epoch().count() ^
+        (unsigned long long)reinterpret_cast<uintptr_t>(&seq);
+    unsigned long long z = seed + 0x9E3779B97F4A7C15ull * (seq.fetch_add(1) + 1);
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    z ^= z >> 31;
+    return z | 1ull;
+}
+
 struct Plan {
     GemmParams p;
     int mt_per_unit;  // MT: 128-row tiles per work unit (1 or 2)
@@ -611,8 +925,9 @@ struct Plan {
 };
 
 // Plans one launch over nmat matrices of rows[m] x k sharing ncols activation columns.
+// sk_mode: balanced k ranges never (0), always (1) or where predicted faster (-1).
 int plan_gemm(Plan *pl, int nmat, const int64_t *rows, int64_t k, int64_t ncols, const DeviceInfo &dev,
-              bool allow_split, bool allow_mt2)
+              bool allow_split, bool allow_mt2, int sk_mode)
 {
     if (nmat < 1 || nmat > kMaxMats) return fail(BM_ERR_INVALID_ARG, "tensor-core product: 1..4 matrices");
     GemmParams &p = pl->p;
@@ -640,7 +955,7 @@ int plan_gemm(Plan *pl, int nmat, const int64_t *rows, int64_t k, int64_t ncols,
     // (a k-block takes about as long) double the units of a product with few row tiles,
     // which can beat splitting k and reducing.  256-row units (two MMAs sharing the X
     // tile) are taken only with full 256-column tiles, where they were measured.
-    int mt_unit = 1, splits = 1, bn = (int)(n16 < 256 ? n16 : 256);
+    int mt_unit = 1, splits = 1, bn = (int)(n16 < 256 ? n16 : 256), sk = 0;
     double best_us = 1e300;
     const int widths[2] = {(int)(n16 < 256 ? n16 : 256), n16 > 128 ? 128 : 0};
     for (int wi = 0; wi < 2; wi++) {
@@ -652,14 +967,26 @@ int plan_gemm(Plan *pl, int nmat, const int64_t *rows, int64_t k, int64_t ncols,
             int64_t units_rows = 0;
             for (int m = 0; m < nmat; m++) units_rows += (mts[m] + mt - 1) / mt;
             const int64_t tiles = units_rows * nt;
-            for (int sp = 1; sp <= (allow_split ? std::min(kMaxSplits, p.num_kb) : 1); sp++) {
-                const double us = plan_us(tiles, tiles128, p.num_kb, bw, mt, sp, dev.sm_count, total_rows, ncols);
+            auto consider = [&](double us, int sp, int with_sk) {
                 if (us < best_us - 1e-9) {
                     best_us = us;
                     mt_unit = mt;
                     splits = sp;
                     bn = bw;
+                    sk = with_sk;
                 }
+            };
+            if (sk_mode != 1)
+                for (int sp = 1; sp <= (allow_split ? std::min(kMaxSplits, p.num_kb) : 1); sp++)
+                    consider(plan_us(tiles, tiles128, p.num_kb, bw, mt, sp, dev.sm_count, total_rows, ncols), sp, 0);
+            // balanced ranges need the operand ring to hold the owners' read buffers
+            const int stage_b = mt * kTileABytes + bw * kBK * 2;
+            const int ring_b = std::min(kMaxStages, (dev.max_smem_optin - 2048) / stage_b) * stage_b;
+            const int64_t per_col = std::min<int64_t>(dev.sm_count / nt, units_rows * p.num_kb);  // CTAs per column
+            if (sk_mode != 0 && ring_b >= kEpiWarps * kOwnerDepth * 4096 && per_col >= 1) {
+                const int nbuf = 2 * mt * pow2_at_least(bw) <= 512 ? 2 : 1;
+                const double us = plan_sk_us(units_rows, p.num_kb, bw, mt, (int)per_col, nt, nbuf);
+                consider(sk_mode == 1 ? us : us / kSkMargin, 1, 1);
             }
         }
     }
@@ -688,12 +1015,21 @@ int plan_gemm(Plan *pl, int nmat, const int64_t *rows, int64_t k, int64_t ncols,
     if (p.stages < 2) return fail(BM_ERR_CUDA, "tensor-core product: not enough shared memory");
     const int64_t units = tiles * p.splits;
     pl->grid = (int)std::min<int64_t>(units, dev.sm_count);
+    p.sk = sk;
+    if (sk) {
+        p.iters = (int64_t)p.mtu * p.num_kb;
+        if (p.iters > ((int64_t)1 << 40))
+            return fail(BM_ERR_INVALID_ARG, "tensor-core product: too many k-blocks");
+        pl->grid = (int)(std::min<int64_t>(dev.sm_count / p.nt, p.iters) * p.nt);
+        p.slot_floats = (int64_t)mt_unit * kEpiWarps * kWarpChunks * 1024;
+    }
     // One CTA per SM (this request is more than half of the SM's shared memory), so the
     // accumulators (up to 512 columns) never exceed the SM's TMEM.
     const size_t smem = (size_t)p.stages * stage_bytes + 1024;
     const size_t one_per_sm = (size_t)dev.max_smem_optin / 2 + 4096;
     pl->smem = std::max(smem, one_per_sm);
     pl->ws_bytes = p.splits > 1 ? (size_t)p.tbeg[nmat] * p.nt * p.splits * p.bn * kBM * sizeof(float) : 0;
+    if (sk) pl->ws_bytes = sk_flags_offset(pl->grid, p.slot_floats) + (size_t)pl->grid * kEpiWarps * 8;
     return BM_OK;
 }
 
@@ -782,16 +1118,16 @@ int launch_gemm_tc_multi(int nmat, const uint16_t *const *W, const int64_t *rows
     unsigned int *err = device_error_word();
     if (!err) return fail(BM_ERR_CUDA, "tensor-core product: device error word unavailable");
     Plan pl;
-    int st = plan_gemm(&pl, nmat, rows, k, ncols, dev, true, true);
+    int st = plan_gemm(&pl, nmat, rows, k, ncols, dev, true, true, stream_k_mode());
     if (st != BM_OK) return st;
     for (int m = 0; m < nmat; m++) pl.p.Y[m] = Y[m];
     pl.p.err = err;
     pl.p.timeout_ns = kDefaultTimeoutNs;
-    if (pl.p.splits == 1) return launch_plan(pl, W, X, s, dev);
+    if (pl.ws_bytes == 0) return launch_plan(pl, W, X, s, dev);
 
-    // Split-k workspace for the partial tiles, stream-ordered (so concurrent products
-    // on other streams never share it, and graph capture records it as an allocation
-    // node).
+    // Workspace for the partial tiles (split-k, or balanced ranges' slots and flags),
+    // stream-ordered (so concurrent products on other streams never share it, and
+    // graph capture records it as an allocation node).
     int dev_id = 0;
     cudaGetDevice(&dev_id);
     cudaMemPool_t pool = workspace_pool(dev_id & (kMaxDevices - 1));
@@ -800,7 +1136,14 @@ int launch_gemm_tc_multi(int nmat, const uint16_t *const *W, const int64_t *rows
     cudaError_t e = cudaMallocFromPoolAsync(&ws, pl.ws_bytes, pool, s);
     if (e != cudaSuccess)
         return fail(BM_ERR_CUDA, "tensor-core product: workspace allocation failed: %s", cudaGetErrorString(e));
-    pl.p.ws = static_cast<float *>(ws);
+    if (pl.p.sk) {
+        pl.p.skws = static_cast<float *>(ws);
+        pl.p.flags = reinterpret_cast<unsigned long long *>(static_cast<unsigned char *>(ws) +
+                                                            sk_flags_offset(pl.grid, pl.p.slot_floats));
+        pl.p.token = next_token();
+    } else {
+        pl.p.ws = static_cast<float *>(ws);
+    }
     st = launch_plan(pl, W, X, s, dev);
     cudaError_t e2 = cudaFreeAsync(ws, s);
     if (st == BM_OK && e2 != cudaSuccess)
@@ -836,7 +1179,7 @@ int launch_gemm_tc_noalloc(const uint16_t *W, int64_t rows, int64_t k, const uin
     unsigned int *err = device_error_word();
     if (!err) return fail(BM_ERR_CUDA, "no-allocation product: device error word unavailable");
     Plan pl;
-    int st = plan_gemm(&pl, 1, &rows, k, ncols, dev, true, true);
+    int st = plan_gemm(&pl, 1, &rows, k, ncols, dev, true, true, 0);
     if (st != BM_OK) return st;
     const size_t need = pl.ws_bytes;
     if (need > kNoAllocScratchBytes)
@@ -873,7 +1216,7 @@ int launch_gemm_tc_withheld(const uint16_t *W, int64_t rows, int64_t k, const ui
     unsigned int *err = device_error_word();
     if (!err) return fail(BM_ERR_CUDA, "tensor-core product: device error word unavailable");
     Plan pl;
-    int st = plan_gemm(&pl, 1, &rows, k, ncols, dev, false, false);
+    int st = plan_gemm(&pl, 1, &rows, k, ncols, dev, false, false, 0);
     if (st != BM_OK) return st;
     pl.p.Y[0] = Y;
     pl.p.err = err;

@@ -273,6 +273,22 @@ int bm_set_pdl(int enable);
  */
 int bm_set_exact_sgemm_cols(int ncols);
 
+/*
+ * Balanced k ranges for the tensor-core products (process-wide; no counterpart on
+ * the pages: a work split of this library, stream-K after Osama et al., PPoPP 2023).
+ * The k-blocks of all tiles of a product are cut into equal ranges, one per SM;
+ * a tile shared by several SMs is finished by the SM holding its last k-block,
+ * which adds the other pieces in k order.  mode -1 (default): used where the
+ * library's time model predicts it clearly faster than whole tiles or k-splits;
+ * 0: never; 1: wherever it applies (at least one SM per column tile of the
+ * product).  Any other value counts as its sign.  The result stays within the
+ * tensor-core bound in every mode and is repeatable (the same bits for the same
+ * product, mode and GPU).  The workspace (one partial tile per SM and a flag word
+ * per epilogue warp) comes from the library's stream-ordered pool like the k-split
+ * one; bm_f16_matmul_noalloc never uses this mode.  Returns the previous setting.
+ */
+int bm_set_stream_k(int mode);
+
 /* Waits for `stream`, then reads and clears this library's device error word
  * on the current device: BM_OK, BM_ERR_TIMEOUT (a kernel gave up a bounded
  * wait and wrote nothing trustworthy), BM_ERR_INVALID_ARG (bm_f16_get_rows met
