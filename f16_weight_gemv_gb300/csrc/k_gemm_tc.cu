@@ -257,8 +257,8 @@ __device__ __forceinline__ Unit unit_of(const GemmParams &p, int u)
     x.m0 = local * MT * kBM;
     x.n0 = nt * p.bn;
     x.tile0 = (pick(p.tbeg, m) + local * MT) * p.nt + nt;
-    x.kb0 = (int)((int64_t)p.num_kb * x.s / p.splits);
-    x.kb1 = (int)((int64_t)p.num_kb * (x.s + 1) / p.splits);
+    x.kb0 = p.num_kb * x.s / p.splits;  // num_kb <= 1024, splits <= 8: no overflow
+    x.kb1 = p.num_kb * (x.s + 1) / p.splits;
     return x;
 }
 
@@ -282,6 +282,7 @@ struct Seg {
 struct SegIter {
     int64_t beg, end;  // balanced ranges: this CTA's iterations
     int64_t t;         // the next tile (balanced ranges, walked downwards) or unit
+    int64_t lo;        // balanced ranges: the lowest row unit of the range
 };
 
 __device__ __forceinline__ void seg_begin(const GemmParams &p, SegIter &it)
@@ -291,8 +292,9 @@ __device__ __forceinline__ void seg_begin(const GemmParams &p, SegIter &it)
         it.beg = p.iters * g / G;
         it.end = p.iters * (g + 1) / G;
         it.t = it.end > it.beg ? (it.end - 1) / p.num_kb : -1;
+        it.lo = it.beg / p.num_kb;
     } else {
-        it.beg = it.end = 0;
+        it.beg = it.end = it.lo = 0;
         it.t = blockIdx.x;
     }
 }
@@ -310,7 +312,7 @@ __device__ __forceinline__ bool seg_next(const GemmParams &p, SegIter &it, Seg &
 {
     if (p.sk) {
         // row unit it.t of column tile blockIdx.x % nt, walked downwards
-        if (it.t < 0 || it.t < it.beg / p.num_kb) return false;
+        if (it.t < it.lo) return false;
         const int64_t t0 = it.t * p.num_kb;
         const int n = (int)(blockIdx.x % p.nt);
         sg.x = unit_of<MT>(p, (int)it.t * p.nt + n);
@@ -514,85 +516,123 @@ __global__ void __launch_bounds__(kThreads, 1)
             // Under programmatic dependent launch the weights (constants) of the first
             // ring's worth of stages are requested before griddepcontrol.wait; the
             // activation tiles (the previous kernel's output) only after it.
-            int t = 0;
+            // Everything the loop needs is hoisted into registers and the stage and its
+            // phase advance by increments: this one thread's per-k-block instruction chain
+            // (divisions, parameter loads) otherwise took longer than the copies it issues.
+            const int stages = p.stages;
+            const int withhold = p.withhold_first_load;
+            const unsigned long long tmo = p.timeout_ns;
+            unsigned int *const errw = p.err;
+            const uint32_t full0 = smem_u32(&full_bar[0]), empty0 = smem_u32(&empty_bar[0]);
+            int t = 0;        // k-blocks walked
+            int st = 0;       // the stage of k-block t
+            uint32_t ph = 0;  // and the parity of its phase
             bool ok = true, waited = false;
-            int pend = 0;  // stages that hold their W copy, X still to come
-            int pend_s[kMaxStages], pend_kb[kMaxStages], pend_n0[kMaxStages];
+            int pend = 0;  // stages that hold their W copy, X still to come: k-blocks 0 .. pend-1
+            // (walked again rather than remembered: stores to a local array before each
+            // barrier arrive cost a memory round trip per k-block)
             auto issue_pending_x = [&]() {
                 dev::pdl_wait();
                 waited = true;
-                for (int q = 0; q < pend; q++)
-                    tma_load_2d(ring_u32 + (uint32_t)pend_s[q] * stage_bytes + MT * kTileABytes, &maps.x,
-                                pend_kb[q] * kBK, pend_n0[q], smem_u32(&full_bar[pend_s[q]]));
+                SegIter it2;
+                seg_begin(p, it2);
+                Seg s2;
+                int q = 0;
+                while (q < pend && seg_next<MT>(p, it2, s2))
+                    for (int kb = s2.kb0; kb < s2.kb1 && q < pend; kb++, q++)
+                        if (!(withhold && q == 0))
+                            tma_load_2d(ring_u32 + (uint32_t)q * stage_bytes + MT * kTileABytes, &maps.x, kb * kBK,
+                                        s2.x.n0, full0 + 8u * (uint32_t)q);
                 pend = 0;
             };
             SegIter it;
             seg_begin(p, it);
             Seg sg;
             while (ok && seg_next<MT>(p, it, sg)) {
-                const Unit &x = sg.x;
-                for (int kb = sg.kb0; kb < sg.kb1; kb++, t++) {
-                    const int s = t % p.stages;
-                    const uint32_t ph = (uint32_t)(t / p.stages) & 1u;
-                    if (!dev::mbar_wait(smem_u32(&empty_bar[s]), ph ^ 1u, abort_v, p.timeout_ns, p.err)) {
+                const CUtensorMap *wmap = &maps.w[sg.x.mat];
+                const int32_t m0 = sg.x.m0, n0 = sg.x.n0;
+                for (int kb = sg.kb0; kb < sg.kb1; kb++) {
+                    if (!dev::mbar_wait(empty0 + 8u * (uint32_t)st, ph ^ 1u, abort_v, tmo, errw)) {
                         ok = false;
                         break;
                     }
-                    if (p.withhold_first_load && t == 0) continue;  // self-test: stage 0 is never filled
-                    const uint32_t a_dst = ring_u32 + (uint32_t)s * stage_bytes;
-                    const uint32_t fb = smem_u32(&full_bar[s]);
-                    mbar_expect_tx(fb, stage_bytes);
-                    tma_load_2d(a_dst, &maps.w[x.mat], kb * kBK, x.m0, fb);  // MT * 128 rows in one box
-                    if (waited) {
-                        tma_load_2d(a_dst + MT * kTileABytes, &maps.x, kb * kBK, x.n0, fb);
-                    } else {  // t < stages here, so at most kMaxStages stages wait for X
-                        pend_s[pend] = s;
-                        pend_kb[pend] = kb;
-                        pend_n0[pend] = x.n0;
+                    if (withhold && t == 0) {  // self-test: stage 0 is never filled
                         pend++;
-                        if (t + 1 == p.stages) issue_pending_x();
+                    } else {
+                        const uint32_t a_dst = ring_u32 + (uint32_t)st * stage_bytes;
+                        const uint32_t fb = full0 + 8u * (uint32_t)st;
+                        mbar_expect_tx(fb, stage_bytes);
+                        tma_load_2d(a_dst, wmap, kb * kBK, m0, fb);  // MT * 128 rows in one box
+                        if (waited) {
+                            tma_load_2d(a_dst + MT * kTileABytes, &maps.x, kb * kBK, n0, fb);
+                        } else {  // t < stages here: k-block t fills stage t
+                            pend++;
+                            if (t + 1 == stages) issue_pending_x();
+                        }
                     }
-                    issued_slot = t + 1;
+                    t++;
+                    if (++st == stages) {
+                        st = 0;
+                        ph ^= 1u;
+                    }
                 }
             }
+            issued_slot = t;
             if (!waited) issue_pending_x();  // fewer k-blocks than stages, or a give-up: complete every stage
         }
         __syncwarp();
     } else if (warp == 1) {
         // ---------------------------------------------------------------- MMA issuer
         if (lane == 0) {
+            // Hoisted and incremental as in the producer.  The operand descriptors of a
+            // stage differ from the ring's first one only in the start address field
+            // (address / 16, below 2^14 for any shared-memory address), so each is that
+            // descriptor plus an offset.
             const uint32_t idesc = instr_desc_f16(kBM, p.bn);
-            int t = 0, i = 0;
+            const int stages = p.stages, nbuf = p.nbuf;
+            const uint32_t bn_alloc = (uint32_t)p.bn_alloc;
+            const unsigned long long tmo = p.timeout_ns;
+            unsigned int *const errw = p.err;
+            const uint32_t full0 = smem_u32(&full_bar[0]), empty0 = smem_u32(&empty_bar[0]);
+            const uint32_t accf0 = smem_u32(&acc_full[0]), acce0 = smem_u32(&acc_empty[0]);
+            const uint64_t desc0 = smem_desc_sw128(ring_u32);
+            const uint32_t stage16 = stage_bytes >> 4;
+            int st = 0, b = 0;
+            uint32_t ph = 0, uph = 0;  // phase parities: the stage's, and accumulator set b's uses
             bool ok = true;
             SegIter it;
             seg_begin(p, it);
             Seg sg;
-            for (; ok && seg_next<MT>(p, it, sg); i++) {
-                const int b = i % p.nbuf;
-                const uint32_t use = (uint32_t)(i / p.nbuf);  // how many times set b was used before
-                if (!dev::mbar_wait(smem_u32(&acc_empty[b]), (use & 1u) ^ 1u, abort_v, p.timeout_ns, p.err)) break;
+            while (ok && seg_next<MT>(p, it, sg)) {
+                if (!dev::mbar_wait(acce0 + 8u * (uint32_t)b, uph ^ 1u, abort_v, tmo, errw)) break;
                 tc_fence_after();
-                const uint32_t d = tmem_base + (uint32_t)(b * MT * p.bn_alloc);
-                for (int kb = sg.kb0; kb < sg.kb1; kb++, t++) {
-                    const int s = t % p.stages;
-                    const uint32_t ph = (uint32_t)(t / p.stages) & 1u;
-                    if (!dev::mbar_wait(smem_u32(&full_bar[s]), ph, abort_v, p.timeout_ns, p.err)) {
+                const uint32_t d = tmem_base + (uint32_t)(b * MT) * bn_alloc;
+                for (int kb = sg.kb0; kb < sg.kb1; kb++) {
+                    if (!dev::mbar_wait(full0 + 8u * (uint32_t)st, ph, abort_v, tmo, errw)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a_addr = ring_u32 + (uint32_t)s * stage_bytes;
-                    const uint32_t b_addr = a_addr + MT * kTileABytes;
+                    const uint64_t ad = desc0 + (uint64_t)((uint32_t)st * stage16);
+                    const uint64_t bd = ad + (uint64_t)(MT * kTileABytes >> 4);
 #pragma unroll
                     for (int kk = 0; kk < kBK / kUmmaK; kk++)
 #pragma unroll
                         for (int m = 0; m < MT; m++)
-                            mma_f16(d + (uint32_t)(m * p.bn_alloc), smem_desc_sw128(a_addr + m * kTileABytes + kk * kUmmaK * 2),
-                                    smem_desc_sw128(b_addr + kk * kUmmaK * 2), idesc, (kb > sg.kb0 || kk > 0) ? 1u : 0u);
-                    mma_commit(smem_u32(&empty_bar[s]));  // the stage is free once these MMAs have read it
+                            mma_f16(d + (uint32_t)m * bn_alloc, ad + (uint64_t)(m * (kTileABytes >> 4) + kk * (kUmmaK * 2 >> 4)),
+                                    bd + (uint64_t)(kk * (kUmmaK * 2 >> 4)), idesc, (kb > sg.kb0 || kk > 0) ? 1u : 0u);
+                    mma_commit(empty0 + 8u * (uint32_t)st);  // the stage is free once these MMAs have read it
+                    if (++st == stages) {
+                        st = 0;
+                        ph ^= 1u;
+                    }
                 }
                 if (!ok) break;
-                mma_commit(smem_u32(&acc_full[b]));  // the accumulators are complete
+                mma_commit(accf0 + 8u * (uint32_t)b);  // the accumulators are complete
+                if (++b == nbuf) {
+                    b = 0;
+                    uph ^= 1u;
+                }
             }
             mma_commit(smem_u32(&done_bar));  // always: completes when every issued MMA has finished
         }
