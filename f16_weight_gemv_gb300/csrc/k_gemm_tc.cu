@@ -86,6 +86,7 @@ constexpr int kEpiWarps = 8;  // two per TMEM lane quarter, splitting the column
 constexpr int kThreads = 32 * (2 + kEpiWarps);
 constexpr int kTileABytes = kBM * kBK * 2;  // 16 KB
 constexpr int kMaxStages = 8;
+constexpr int kPreWaitStages = 2;  // stages whose W copy is requested before griddepcontrol.wait
 constexpr int kMaxSplits = 8;
 constexpr int kMaxMats = 4;       // matrices sharing one activation in one launch
 constexpr int kWarpChunks = 4;    // 32-column chunks per epilogue warp and row tile (bn <= 256)
@@ -514,12 +515,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------------------------------------------------------- TMA producer
         if (lane == 0) {
             // Under programmatic dependent launch the weights (constants) of the first
-            // ring's worth of stages are requested before griddepcontrol.wait; the
-            // activation tiles (the previous kernel's output) only after it.
+            // stages are requested before griddepcontrol.wait; the activation tiles (the
+            // previous kernel's output) only after it.
             // Everything the loop needs is hoisted into registers and the stage and its
             // phase advance by increments: this one thread's per-k-block instruction chain
             // (divisions, parameter loads) otherwise took longer than the copies it issues.
             const int stages = p.stages;
+            // W copies requested before griddepcontrol.wait: the engine serves copies in
+            // order, so every W box queued ahead delays the first X tile (and the first
+            // MMA) when the kernel ahead has already finished; two stages keep that
+            // delay short and still start the weights early when it has not.
+            const int pre_wait = stages < kPreWaitStages ? stages : kPreWaitStages;
             const int withhold = p.withhold_first_load;
             const unsigned long long tmo = p.timeout_ns;
             unsigned int *const errw = p.err;
@@ -558,6 +564,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     if (withhold && t == 0) {  // self-test: stage 0 is never filled
                         pend++;
+                        if (t + 1 == pre_wait) issue_pending_x();
                     } else {
                         const uint32_t a_dst = ring_u32 + (uint32_t)st * stage_bytes;
                         const uint32_t fb = full0 + 8u * (uint32_t)st;
@@ -567,7 +574,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             tma_load_2d(a_dst + MT * kTileABytes, &maps.x, kb * kBK, n0, fb);
                         } else {  // t < stages here: k-block t fills stage t
                             pend++;
-                            if (t + 1 == stages) issue_pending_x();
+                            if (t + 1 == pre_wait) issue_pending_x();
                         }
                     }
                     t++;
@@ -883,14 +890,15 @@ double plan_us(int64_t units_per_split, int64_t tiles128, int num_kb, int bn, in
 // theirs (about 5.5 MB/us in all), and with one TMEM set its next MMAs wait for
 // that; an owner reads each lower piece at about 0.15 MB/us.  Where the time
 // model is free to choose (bm_set_stream_k(-1)) the balanced plan must be predicted
-// 5 % faster than the best other plan: measured gains were small and the model is
-// coarse.
+// 10 % faster than the best other plan: measured gains were small (at most 3 % on the
+// Llama-3-8B shapes at 512 columns, 10 % on gate at 64), losses on others up to 8 %,
+// and the model is coarse.
 constexpr double kSkKblockUs[3] = {0.0, 0.55, 0.85};
 constexpr double kSkFixedUs = 1.0;
 constexpr double kSkStoreBytesPerUs = 5.5e6;  // all CTAs' partial-tile stores at once
 constexpr double kSkOverlap = 0.3;            // share of that hidden behind MMAs with two TMEM sets
 constexpr double kSkReadBytesPerUs = 1.5e5;   // one SM's piece loads
-constexpr double kSkMargin = 0.95;
+constexpr double kSkMargin = 0.90;
 
 // Predicted time of balanced ranges over `units` row units of MT * 128 rows of each of
 // nt column tiles, `ctas` CTAs per column tile; nbuf TMEM accumulator sets.

@@ -199,7 +199,9 @@ int bm_f16_matmul_multi(int nmat, const uint16_t *const *W, const int64_t *rows,
  * large, held by every GPU that loads the library until the process exits.
  * It allocates nothing: no cudaMalloc, no stream-ordered allocation, no
  * allocating library routine.  The caller still passes W, X and Y, with the
- * same layout, validation, path selection and results as bm_f16_matmul.
+ * same layout, validation, path selection and results as bm_f16_matmul with
+ * balanced k ranges off (bm_set_stream_k(0)); where bm_f16_matmul takes them the
+ * two results may differ in their last bits, both within the tensor-core bound.
  *   - A product whose split-k workspace would exceed the scratch is refused with
  *     BM_ERR_INVALID_ARG and a reason (bm_last_error); nothing is launched.
  *   - The first call on a device looks up the scratch's device address (once per
