@@ -162,6 +162,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv_stream(const __grid_consta
     __shared__ int abort_flag;
     __shared__ int issued_slot;
     __shared__ norm::Scratch norm_sh;
+    __shared__ int first_sub[4];  // the first sub-block: matrix, groups, slices, group within the matrix
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int k = job.k;
@@ -244,6 +245,18 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv_stream(const __grid_consta
                 w[i] = c < n4 ? __ldg(reinterpret_cast<const float4 *>(job.g) + c) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
         }
+        if (threadIdx.x == 0 && glo < ghi) {
+            // The first sub-block's set-up depends on the parameters alone: done here, before
+            // the wait, it stays off a small product's critical path (read after the barrier
+            // that follows the activation's conversion).
+            const int m = matrix_of(job, glo);
+            const int ng = min(kGroupsPerBlock, min(ghi, job.gbeg[m + 1]) - glo);
+            const int sw = boxes_per_group(ng) * kBoxCols;
+            first_sub[0] = m;
+            first_sub[1] = ng;
+            first_sub[2] = (k + sw - 1) / sw;
+            first_sub[3] = glo - job.gbeg[m];
+        }
         dev::pdl_wait();  // the activation is the previous kernel's output; outputs follow too
         if (held) {
             // the norm with this thread's chunks of x held in registers: one read of x
@@ -265,6 +278,25 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv_stream(const __grid_consta
                                                  norm::apply(v[i].z, scale, w[i].z), norm::apply(v[i].w, scale, w[i].w));
                     if (job.n_out && blockIdx.x == 0) reinterpret_cast<float4 *>(job.n_out)[c] = o;
                     const uint2 p = make_uint2(pack_rn(o.x, o.y), pack_rn(o.z, o.w));
+                    xo[c] = p;
+                    if (job.h_out && blockIdx.x == 0) reinterpret_cast<uint2 *>(job.h_out)[c] = p;
+                }
+            }
+        } else if (job.x_is_f32 && !job.g && k <= 4 * kHeldChunks * kNormThreadsC) {
+            // every load of this thread in flight before the first conversion
+            const float4 *xf = reinterpret_cast<const float4 *>(job.x);
+            uint2 *xo = reinterpret_cast<uint2 *>(xs);
+            float4 v[kHeldChunks];
+#pragma unroll
+            for (int i = 0; i < kHeldChunks; i++) {
+                const int c = threadIdx.x + i * kNormThreadsC;
+                v[i] = c < n4 ? __ldg(xf + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int i = 0; i < kHeldChunks; i++) {
+                const int c = threadIdx.x + i * kNormThreadsC;
+                if (c < n4) {
+                    const uint2 p = make_uint2(pack_rn(v[i].x, v[i].y), pack_rn(v[i].z, v[i].w));
                     xo[c] = p;
                     if (job.h_out && blockIdx.x == 0) reinterpret_cast<uint2 *>(job.h_out)[c] = p;
                 }
@@ -292,6 +324,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv_stream(const __grid_consta
         } else {
             const uint4 *xg = reinterpret_cast<const uint4 *>(job.x);
             uint4 *xo = reinterpret_cast<uint4 *>(xs);
+#pragma unroll 4
             for (int i = threadIdx.x; i < (k >> 3); i += 32 * kConsumerWarps) xo[i] = __ldg(xg + i);
         }
         consumers_sync();
@@ -303,12 +336,22 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv_stream(const __grid_consta
         bool ok = true;
         int t = 0;
         for (int g = glo; g < ghi && ok;) {
-            const int m = matrix_of(job, g);
-            const int ng = min(kGroupsPerBlock, min(ghi, job.gbeg[m + 1]) - g);
+            int m, ng, nslices, g_in_m;
+            if (g == glo) {
+                m = first_sub[0];
+                ng = first_sub[1];
+                nslices = first_sub[2];
+                g_in_m = first_sub[3];
+            } else {
+                m = matrix_of(job, g);
+                ng = min(kGroupsPerBlock, min(ghi, job.gbeg[m + 1]) - g);
+                const int sw0 = boxes_per_group(ng) * kBoxCols;
+                nslices = (k + sw0 - 1) / sw0;
+                g_in_m = g - job.gbeg[m];
+            }
             const int bpg = boxes_per_group(ng);
             const int sw = bpg * kBoxCols;
-            const int nslices = (k + sw - 1) / sw;
-            const int row = (g - job.gbeg[m] + warp) * kGroupRows + rho;  // this thread's row (< 2^31)
+            const int row = (g_in_m + warp) * kGroupRows + rho;  // this thread's row (< 2^31)
             const bool active = warp < ng;                                     // warp-uniform
             float acc[8];
 #pragma unroll
@@ -327,6 +370,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv_stream(const __grid_consta
                 if (active) {
                     const int nst = min(2 * bpg, nsteps - kc0 / 32);  // chain steps in this slice
                     int s = 0;
+#pragma unroll 4
                     for (; s + 2 <= nst; s += 2) {  // one 64-element box: two steps
                         const uint8_t *bx = rbase + (s >> 1) * kBoxBytes;
                         const uint4 w0 = *reinterpret_cast<const uint4 *>(bx + ((j) ^ rho) * 16);
