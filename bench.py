@@ -58,7 +58,7 @@ W_SIGMA, A_SIGMA = 0.02, 1.0
 # timed step (profiles/decode_step_smollm2_launches.md), valid only for the kernel
 # source it was measured on (sha256 prefix of k_gemv_stream.cu).
 NCU_TRAFFIC = {"kernel": "k_gemv_stream", "source": "f16_weight_gemv_gb300/csrc/k_gemv_stream.cu",
-               "sha256_16": "0483b8ea9f0c8e6a", "bytes_per_launch": 2293017}
+               "sha256_16": "0726f8ef9831c452", "bytes_per_launch": 2292165}
 
 
 def ncu_traffic():

@@ -370,7 +370,6 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv_stream(const __grid_consta
                 if (active) {
                     const int nst = min(2 * bpg, nsteps - kc0 / 32);  // chain steps in this slice
                     int s = 0;
-#pragma unroll 4
                     for (; s + 2 <= nst; s += 2) {  // one 64-element box: two steps
                         const uint8_t *bx = rbase + (s >> 1) * kBoxBytes;
                         const uint4 w0 = *reinterpret_cast<const uint4 *>(bx + ((j) ^ rho) * 16);
