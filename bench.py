@@ -58,7 +58,7 @@ W_SIGMA, A_SIGMA = 0.02, 1.0
 # timed step (profiles/decode_step_smollm2_launches.md), valid only for the kernel
 # source it was measured on (sha256 prefix of k_gemv_stream.cu).
 NCU_TRAFFIC = {"kernel": "k_gemv_stream", "source": "f16_weight_gemv_gb300/csrc/k_gemv_stream.cu",
-               "sha256_16": "0726f8ef9831c452", "bytes_per_launch": 2292165}
+               "sha256_16": "78fefbba59017a3a", "bytes_per_launch": 2294604}
 
 
 def ncu_traffic():
@@ -409,11 +409,12 @@ def bench_products(bm, dev, stream, torch):
         gbs = algorithmic_bytes(rows, k) / ms / 1e6
         out.append({"product": name, "rows": rows, "k": k, "ncols": 1, "ms": round(ms, 5), "GB_s": round(gbs, 1),
                     "how": "%d back-to-back launches over %d weight replicas, PDL" % (launches, nrep)})
-        few = [(nc, None) for nc in (2, 3, 5, 8, 16, 17, 64)] + [(nc, 8) for nc in (3, 5, 8)]
+        few = [(nc, None) for nc in (2, 3, 5, 8, 16, 17, 64)] + [(nc, 8) for nc in (3, 5, 8)] + [(2, 0)]
         for nc, exact_cols in (few if name in ("llama3_8b.q", "llama3_8b.gate") else []):
             # few columns: HBM-bound, timed like the one-column products.  The library's
             # default takes the bit-exact CUDA-core kernel for 2 columns and the tensor
-            # cores for more; the (nc, 8) entries time the bit-exact kernel at 3..8 too.
+            # cores for more; the (nc, 8) entries time the bit-exact kernel at 3..8 too,
+            # the (2, 0) entry the tensor cores at 2.
             Yn = torch.empty((nc, rows), dtype=torch.float32, device=dev)
             xn = x[:nc].contiguous()
 
