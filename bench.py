@@ -678,20 +678,47 @@ def oracle_step_runner():
     return run, tot_bytes, oracle.threads()
 
 
-def cpu_baseline(budget_s=10.0):
+def host_cpu():
+    """The host's architecture and CPU model, as the kernel reports them."""
+    import platform
+    model = ""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key = line.split(":")[0].strip().lower()
+                if key in ("model name", "cpu part", "hardware") and not model:
+                    model = line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return {"machine": platform.machine(), "cpu": model, "logical_cpus": os.cpu_count()}
+
+
+def cpu_baseline(budget_s=10.0, budget_1core_s=4.0):
+    import oracle
     run, nbytes, cores = oracle_step_runner()
-    run()
-    n = 0
-    t0 = time.perf_counter()
-    while True:
+
+    def timed(budget):
         run()
-        n += 1
-        if time.perf_counter() - t0 >= budget_s:
-            break
-    dt = time.perf_counter() - t0
+        n = 0
+        t0 = time.perf_counter()
+        while True:
+            run()
+            n += 1
+            if time.perf_counter() - t0 >= budget:
+                break
+        return n, time.perf_counter() - t0
+
+    n, dt = timed(budget_s)
+    oracle.set_threads(1)
+    try:
+        n1, dt1 = timed(budget_1core_s)
+    finally:
+        oracle.set_threads(cores)
     return {"value": round(nbytes * n / dt / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
             "sample": "%d full SmolLM2-135M decode steps (30 layers + logits, 269 MB of f16 weights each) "
-                      "in %.1f s on the host" % (n, dt)}
+                      "in %.1f s on the host" % (n, dt),
+            "value_1core": round(nbytes * n1 / dt1 / 1e9, 4),
+            "sample_1core": "%d full steps in %.1f s on one core" % (n1, dt1), "host": host_cpu()}
 
 
 def step_config(world, no_pdl):

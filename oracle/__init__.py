@@ -68,6 +68,7 @@ def lib():
             L.or_check_to_f16_vs_compiler.argtypes = [C.c_uint64, C.c_uint64, C.POINTER(C.c_uint32)]
             L.or_check_to_f16_vs_compiler.restype = C.c_int64
             L.or_threads.argtypes = []; L.or_threads.restype = C.c_int
+            L.or_set_threads.argtypes = [C.c_int]; L.or_set_threads.restype = None
             L.or_rms_norm_mul_rows.argtypes = [f32p, f32p, C.c_int64, C.c_int64, C.c_float, f32p]
             L.or_rms_norm_mul_rows.restype = None
             _lib = L
@@ -87,6 +88,11 @@ def _u16(a) -> np.ndarray:
 
 def threads() -> int:
     return lib().or_threads()
+
+
+def set_threads(n: int) -> None:
+    """Threads the oracle's row loops use from now on (timing only: results do not depend on it)."""
+    lib().or_set_threads(int(n))
 
 
 def to_f16(x) -> np.ndarray:

@@ -261,3 +261,12 @@ int or_threads(void)
     return 1;
 #endif
 }
+
+void or_set_threads(int n)
+{
+#ifdef _OPENMP
+    omp_set_num_threads(n > 0 ? n : 1);
+#else
+    (void)n;
+#endif
+}

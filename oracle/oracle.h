@@ -76,6 +76,8 @@ void or_rms_norm_mul_rows(const float *X, const float *w, int64_t rows, int64_t 
  * _Float16 conversion, and stores the first such pattern in *first_bad. */
 int64_t or_check_to_f16_vs_compiler(uint64_t lo, uint64_t hi, uint32_t *first_bad);
 int     or_threads(void);
+/* Threads the row loops use from now on (n < 1 counts as 1); timing only, never results. */
+void    or_set_threads(int n);
 
 #ifdef __cplusplus
 }
