@@ -20,7 +20,7 @@ from . import _build
 __all__ = [
     "BmError", "lib", "bm_to_f16", "bm_f16_matvec", "bm_f16_matvec_multi", "bm_f16_matvec_act", "bm_f16_matvec_norm", "bm_rms_norm_mul", "bm_f16_matmul", "bm_f16_matmul_multi", "bm_f16_matmul_noalloc",
     "bm_f16_logits", "bm_f16_get_rows", "bm_takes_sgemm", "bm_device_status", "bm_status_string", "bm_last_error",
-    "bm_selftest_wait_timeout", "bm_set_pdl", "prepare", "Prepared", "bm_set_exact_sgemm_cols", "bm_set_stream_k", "EXPORTS",
+    "bm_selftest_wait_timeout", "bm_set_pdl", "prepare", "Prepared", "PreparedGraph", "bm_set_exact_sgemm_cols", "bm_set_stream_k", "EXPORTS",
     "BM_MAX_K",
 ]
 
@@ -111,6 +111,36 @@ class Prepared:
             st = fn(*args)
             if st != BM_OK:
                 raise BmError(st, name)
+
+    def graph(self, stream=None) -> "PreparedGraph":
+        """Runs the recorded calls once, then captures them into a CUDA graph on
+        `stream` (a torch.cuda.Stream; default: the current stream).  Every recorded
+        call must have been made on that stream.  Calling the result replays the whole
+        sequence as one graph launch on the current stream, with the same pointers, so
+        in-place changes of the inputs are followed as with a plain replay."""
+        s = stream if stream is not None else torch.cuda.current_stream()
+        with torch.cuda.stream(s):
+            self()
+        s.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            self()
+        return PreparedGraph(g, self)
+
+
+class PreparedGraph:
+    """Recorded calls captured as one CUDA graph (Prepared.graph); holds the Prepared
+    object, and with it every tensor the calls point into."""
+
+    def __init__(self, graph, prepared):
+        self._graph = graph
+        self._prepared = prepared
+
+    def __len__(self):
+        return len(self._prepared)
+
+    def __call__(self):
+        self._graph.replay()
 
 
 def prepare(thunk) -> Prepared:
