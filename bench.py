@@ -920,7 +920,11 @@ def main():
         line["qwen3_0.6b_prefill_layer"] = pq
     if "llama3_8b_prefill_layer" in r:
         pf = r["llama3_8b_prefill_layer"]
-        pf["pct_bf16_dense_peak"] = round(100.0 * pf["TFLOP_s"] / float(peaks.get("bf16_tflops", 1900.0)), 1)
+        pk = float(peaks.get("bf16_tflops", 1900.0))
+        pf["pct_bf16_dense_peak"] = round(100.0 * pf["TFLOP_s"] / pk, 1)
+        for key in ("multi", "concatenated_weights"):
+            if key in pf:
+                pf[key]["pct_bf16_dense_peak"] = round(100.0 * pf[key]["TFLOP_s"] / pk, 1)
         line["llama3_8b_prefill_layer"] = pf
     if "products" in r:
         line["products"] = r["products"]
