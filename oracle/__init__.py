@@ -69,6 +69,10 @@ def lib():
             L.or_check_to_f16_vs_compiler.restype = C.c_int64
             L.or_threads.argtypes = []; L.or_threads.restype = C.c_int
             L.or_set_threads.argtypes = [C.c_int]; L.or_set_threads.restype = None
+            L.or_f16_mad.argtypes = [C.POINTER(C.c_uint16), C.POINTER(C.c_uint16), C.c_float, C.c_int64]
+            L.or_f16_mad.restype = None
+            L.or_f16_scale.argtypes = [C.POINTER(C.c_uint16), C.c_float, C.c_int64]
+            L.or_f16_scale.restype = None
             L.or_rms_norm_mul_rows.argtypes = [f32p, f32p, C.c_int64, C.c_int64, C.c_float, f32p]
             L.or_rms_norm_mul_rows.restype = None
             _lib = L
@@ -88,6 +92,22 @@ def _u16(a) -> np.ndarray:
 
 def threads() -> int:
     return lib().or_threads()
+
+
+def f16_mad(acc, v, w) -> np.ndarray:
+    """ggml_vec_mad_f16 on copies: to_f16(fma(widen(v), w, widen(acc))) per element."""
+    acc = _u16(acc).copy()
+    v = _u16(v)
+    assert acc.size == v.size
+    lib().or_f16_mad(_p(acc, C.c_uint16), _p(v, C.c_uint16), float(np.float32(w)), acc.size)
+    return acc
+
+
+def f16_scale(acc, s) -> np.ndarray:
+    """ggml_vec_scale_f16 on a copy: to_f16(widen(acc) * s) per element."""
+    acc = _u16(acc).copy()
+    lib().or_f16_scale(_p(acc, C.c_uint16), float(np.float32(s)), acc.size)
+    return acc
 
 
 def set_threads(n: int) -> None:

@@ -253,6 +253,22 @@ void or_rms_norm_mul_rows(const float *X, const float *w, int64_t rows, int64_t 
     for (int64_t r = 0; r < rows; r++) or_rms_norm_mul(X + r * n, w, n, eps, out + r * n);
 }
 
+/* mad and scale (page "docs/modules/f16.md", Technical usage: `mad` is
+ * ggml_vec_mad_f16, the V accumulator of flash attention; `scale` is
+ * ggml_vec_scale_f16), element by element in index order.  mad's product and sum
+ * round once together (C99 fmaf is correctly rounded); scale is one f32 multiply
+ * (this file is compiled with -ffp-contract=off, so nothing else is fused).  Both
+ * results go to f16 by or_to_f16 (nearest-even). */
+void or_f16_mad(uint16_t *acc, const uint16_t *v, float w, int64_t n)
+{
+    for (int64_t i = 0; i < n; i++) acc[i] = or_to_f16(fmaf(or_widen(v[i]), w, or_widen(acc[i])));
+}
+
+void or_f16_scale(uint16_t *acc, float s, int64_t n)
+{
+    for (int64_t i = 0; i < n; i++) acc[i] = or_to_f16(or_widen(acc[i]) * s);
+}
+
 int or_threads(void)
 {
 #ifdef _OPENMP

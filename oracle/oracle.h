@@ -71,6 +71,16 @@ void or_rms_norm_mul(const float *x, const float *w, int64_t n, float eps, float
 void or_rms_norm_mul_rows(const float *X, const float *w, int64_t rows, int64_t n, float eps,
                           float *out);
 
+/* The attention-side accumulator helpers (page "docs/modules/f16.md", Technical usage:
+ * `mad` is ggml_vec_mad_f16, flash attention's V accumulator; `scale` is
+ * ggml_vec_scale_f16).  In place on acc[0..n):
+ *   or_f16_mad:   acc[i] = to_f16(fmaf(widen(v[i]), w, widen(acc[i])))
+ *   or_f16_scale: acc[i] = to_f16(widen(acc[i]) * s)
+ * Reading where the page is silent: mad rounds once in f32 (a fused multiply-add, as
+ * ggml's F16C + FMA path does), then to f16 nearest-even. */
+void or_f16_mad(uint16_t *acc, const uint16_t *v, float w, int64_t n);
+void or_f16_scale(uint16_t *acc, float s, int64_t n);
+
 /* Exhaustive self-checks over every f32 bit pattern in [lo, hi): returns the
  * number of non-NaN inputs whose or_to_f16 differs from the C compiler's own
  * _Float16 conversion, and stores the first such pattern in *first_bad. */

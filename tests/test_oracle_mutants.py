@@ -62,6 +62,13 @@ MUTANTS = {
     "norm_sign_lost": ("float y = x[i] * scale;", "float y = fabsf(x[i]) * scale;"),
     "norm_weight_reversed": ("out[i] = y * w[i];", "out[i] = y * w[n - 1 - i];"),
     "norm_weight_dropped": ("out[i] = y * w[i];", "out[i] = y;"),
+    "mad_two_roundings": ("acc[i] = or_to_f16(fmaf(or_widen(v[i]), w, or_widen(acc[i])));",
+                          "acc[i] = or_to_f16(or_widen(v[i]) * w + or_widen(acc[i]));"),
+    "mad_roles_swapped": ("acc[i] = or_to_f16(fmaf(or_widen(v[i]), w, or_widen(acc[i])));",
+                          "acc[i] = or_to_f16(fmaf(or_widen(acc[i]), w, or_widen(v[i])));"),
+    "mad_last_element_skipped": ("for (int64_t i = 0; i < n; i++) acc[i] = or_to_f16(fmaf(",
+                                 "for (int64_t i = 0; i + 1 < n; i++) acc[i] = or_to_f16(fmaf("),
+    "scale_divides": ("acc[i] = or_to_f16(or_widen(acc[i]) * s);", "acc[i] = or_to_f16(or_widen(acc[i]) / s);"),
 }
 
 
@@ -81,6 +88,8 @@ def build(src_text, d, name):
     L.or_widen.argtypes = [C.c_uint16]; L.or_widen.restype = C.c_float
     L.or_matmul.argtypes = [u16p, C.c_int64, C.c_int64, u16p, C.c_int64, f32p]; L.or_matmul.restype = None
     L.or_rms_norm_mul.argtypes = [f32p, f32p, C.c_int64, C.c_float, f32p]; L.or_rms_norm_mul.restype = None
+    L.or_f16_mad.argtypes = [u16p, u16p, C.c_float, C.c_int64]; L.or_f16_mad.restype = None
+    L.or_f16_scale.argtypes = [u16p, C.c_float, C.c_int64]; L.or_f16_scale.restype = None
     return L
 
 
@@ -137,6 +146,30 @@ def failures(L):
         return out
 
     bad += ["norm:" + b for b in norm_cases.failures(norm)]
+
+    # mad and scale against numpy's float32 arithmetic and float16 conversion
+    def f16(x):
+        with np.errstate(over="ignore"):
+            return np.asarray(x, np.float32).astype(np.float16).view(np.uint16)
+
+    hs = np.arange(0, 1 << 16, 7, dtype=np.uint32).astype(np.uint16)
+    hs = hs[np.isfinite(hs.view(np.float16))]
+    for sc in (0.5, 3.0, 0.1):
+        got = hs.copy()
+        L.or_f16_scale(P(got), float(np.float32(sc)), got.size)
+        with np.errstate(over="ignore"):
+            if not np.array_equal(got, f16(hs.view(np.float16).astype(np.float32) * np.float32(sc))):
+                bad.append("scale:%g" % sc)
+    v = f16(rng.uniform(1, 2, 20000))
+    wm = np.float32(1.00123456)  # 24 significant bits: v * wm is not exact in f32
+    prod = v.view(np.float16).astype(np.float64) * np.float64(wm)
+    acc = f16(-prod.astype(np.float32))  # near cancellation: the f32 rounding of a product shows
+    acc[::2] = f16(rng.uniform(-4, 4, acc[::2].size))
+    want = f16((acc.view(np.float16).astype(np.float64) + prod).astype(np.float32))
+    got = acc.copy()
+    L.or_f16_mad(P(got), P(v), float(wm), got.size)
+    if not np.array_equal(got, want):
+        bad.append("mad")
     return bad
 
 
