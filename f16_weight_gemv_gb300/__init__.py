@@ -19,7 +19,7 @@ from . import _build
 
 __all__ = [
     "BmError", "lib", "bm_to_f16", "bm_f16_matvec", "bm_f16_matvec_multi", "bm_f16_matvec_act", "bm_f16_matvec_norm", "bm_rms_norm_mul", "bm_f16_matmul", "bm_f16_matmul_multi", "bm_f16_matmul_noalloc",
-    "bm_f16_logits", "bm_f16_get_rows", "bm_takes_sgemm", "bm_device_status", "bm_status_string", "bm_last_error",
+    "bm_f16_logits", "bm_f16_get_rows", "bm_f16_mad", "bm_f16_scale", "bm_takes_sgemm", "bm_device_status", "bm_status_string", "bm_last_error",
     "bm_selftest_wait_timeout", "bm_set_pdl", "prepare", "Prepared", "PreparedGraph", "bm_set_exact_sgemm_cols", "bm_set_stream_k", "EXPORTS",
     "BM_MAX_K",
 ]
@@ -42,6 +42,8 @@ EXPORTS = {
     "bm_f16_logits": (_i, [_vp, _i64, _i64, _vp, _i64, _vp, _vp]),
     "bm_f16_matmul_noalloc": (_i, [_vp, _i64, _i64, _vp, _i64, _vp, _vp]),
     "bm_f16_get_rows": (_i, [_vp, _i64, _i64, _vp, _i64, _vp, _vp]),
+    "bm_f16_mad": (_i, [_vp, _vp, C.c_float, _i64, _vp]),
+    "bm_f16_scale": (_i, [_vp, C.c_float, _i64, _vp]),
     "bm_takes_sgemm": (_i, [_i64, _i64, _i64]),
     "bm_device_status": (_i, [_vp]),
     "bm_set_pdl": (_i, [_i]),
@@ -197,6 +199,20 @@ def bm_to_f16(x: torch.Tensor, h: torch.Tensor | None = None, stream=None) -> to
         raise ValueError("h must have x's size")
     _call("bm_to_f16", _dev(x, "x", (torch.float32,)), _dev(h, "h", _F16_LIKE), x.numel(), _stream(stream))
     return h
+
+
+def bm_f16_mad(acc: torch.Tensor, v: torch.Tensor, w: float, stream=None) -> torch.Tensor:
+    """In place: acc = f16(fma(v, w, acc)) element by element (ggml_vec_mad_f16); returns acc."""
+    if v.numel() != acc.numel():
+        raise ValueError("v must have acc's size")
+    _call("bm_f16_mad", _dev(acc, "acc", _F16_LIKE), _dev(v, "v", _F16_LIKE), float(w), acc.numel(), _stream(stream))
+    return acc
+
+
+def bm_f16_scale(acc: torch.Tensor, s: float, stream=None) -> torch.Tensor:
+    """In place: acc = f16(acc * s) element by element (ggml_vec_scale_f16); returns acc."""
+    _call("bm_f16_scale", _dev(acc, "acc", _F16_LIKE), float(s), acc.numel(), _stream(stream))
+    return acc
 
 
 def _wk(W: torch.Tensor):

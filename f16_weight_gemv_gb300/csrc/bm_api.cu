@@ -209,6 +209,34 @@ int bm_to_f16(const float *x, uint16_t *h, int64_t n, bm_stream_t stream)
     return launch_to_f16(x, h, n, reinterpret_cast<cudaStream_t>(stream), dev);
 }
 
+int bm_f16_mad(uint16_t *acc, const uint16_t *v, float w, int64_t n, bm_stream_t stream)
+{
+    clear_error();
+    if (n < 0 || n > INT64_MAX / 8) return fail(BM_ERR_INVALID_ARG, "bm_f16_mad: bad n = %lld", (long long)n);
+    if (n == 0) return BM_OK;
+    if (!acc || !v) return fail(BM_ERR_INVALID_ARG, "bm_f16_mad: null pointer");
+    if (!aligned(acc, 2) || !aligned(v, 2)) return fail(BM_ERR_ALIGNMENT, "bm_f16_mad: acc and v must be 2-byte aligned");
+    if (static_cast<const void *>(v) != static_cast<const void *>(acc) && overlap(v, n * 2, acc, n * 2))
+        return fail(BM_ERR_INVALID_ARG, "bm_f16_mad: v overlaps acc (only v == acc may share memory)");
+    int st;
+    DeviceInfo dev;
+    if (!current_device(&dev, &st)) return st;
+    return launch_f16_accum(true, acc, v, w, n, reinterpret_cast<cudaStream_t>(stream), dev);
+}
+
+int bm_f16_scale(uint16_t *acc, float s, int64_t n, bm_stream_t stream)
+{
+    clear_error();
+    if (n < 0 || n > INT64_MAX / 8) return fail(BM_ERR_INVALID_ARG, "bm_f16_scale: bad n = %lld", (long long)n);
+    if (n == 0) return BM_OK;
+    if (!acc) return fail(BM_ERR_INVALID_ARG, "bm_f16_scale: null pointer");
+    if (!aligned(acc, 2)) return fail(BM_ERR_ALIGNMENT, "bm_f16_scale: acc must be 2-byte aligned");
+    int st;
+    DeviceInfo dev;
+    if (!current_device(&dev, &st)) return st;
+    return launch_f16_accum(false, acc, nullptr, s, n, reinterpret_cast<cudaStream_t>(stream), dev);
+}
+
 int bm_f16_matvec(const uint16_t *W, int64_t rows, int64_t k, const uint16_t *x, float *y, bm_stream_t stream)
 {
     clear_error();

@@ -43,6 +43,9 @@ struct VecdotJob {
 
 // Launchers (each returns a bm_status; nothing is launched for empty jobs).
 int launch_to_f16(const float *x, uint16_t *h, int64_t n, cudaStream_t s, const DeviceInfo &dev);
+// bm_f16_mad (mad = true: acc = f16(fma(v, w, acc))) and bm_f16_scale (acc = f16(acc * w)).
+int launch_f16_accum(bool mad, uint16_t *acc, const uint16_t *v, float w, int64_t n, cudaStream_t s,
+                     const DeviceInfo &dev);
 // One column, any k; uses the 16-byte fast kernel when k % 8 == 0.
 int launch_vecdot_1col(const VecdotJob &job, cudaStream_t s, const DeviceInfo &dev);
 // The rms_norm then mul that may precede the rounding of an f32 activation.

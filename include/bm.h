@@ -245,6 +245,22 @@ int bm_f16_logits(const uint16_t *E, int64_t vocab, int64_t hidden, const uint16
 int bm_f16_get_rows(const uint16_t *E, int64_t vocab, int64_t hidden, const int32_t *ids, int64_t n,
                     float *out, bm_stream_t stream);
 
+/*
+ * The f16 accumulator helpers of the attention side (f16.md, "Technical usage":
+ * `mad` is ggml_vec_mad_f16, flash attention's V accumulator; `scale` is
+ * ggml_vec_scale_f16), in place on acc[0..n):
+ *   bm_f16_mad:   acc[i] = RNE_f16(fma(widen(v[i]), w, widen(acc[i])))
+ *   bm_f16_scale: acc[i] = RNE_f16(widen(acc[i]) * s)
+ * mad's product and sum round once in f32 (a fused multiply-add, as ggml's F16C + FMA
+ * path computes it -- the page names the function, not its rounding), then to f16
+ * nearest-even; scale is one f32 multiply, then f16.  acc, v: device f16[n], 2-byte
+ * aligned (16-byte aligned vectors take an 8-wide path); v may be acc itself but may
+ * not otherwise overlap it.  n >= 0 (0: nothing launched).  NaN results are NaN (their
+ * payload is unspecified).
+ */
+int bm_f16_mad(uint16_t *acc, const uint16_t *v, float w, int64_t n, bm_stream_t stream);
+int bm_f16_scale(uint16_t *acc, float s, int64_t n, bm_stream_t stream);
+
 /* ggml's path selector (f16.md, "Technical usage"): 1 when
  * ncols >= 2 && rows % 4 == 0 && k % 8 == 0, else 0.  Pure; never fails. */
 int bm_takes_sgemm(int64_t rows, int64_t k, int64_t ncols);

@@ -211,3 +211,19 @@ def test_matmul_multi_host_checks(L):
     Yo = (C.c_void_p * 2)(A + 2 ** 24, A + 2 ** 24 + 64)                  # the outputs overlap
     assert f(2, W, rows, 64, X, 8, Yo, None) == 1
     assert f(2, W, rows, 64, X, 0, Y, None) == 0                        # no columns: nothing to do
+
+
+def test_mad_and_scale_host_checks(L):
+    f = "bm_f16_mad"
+    assert st(L, f, A, A + 4096, 0.5, -1, None) == 1        # n < 0
+    assert st(L, f, A, A + 4096, 0.5, 0, None) == 0         # nothing to do
+    assert st(L, f, None, A + 4096, 0.5, 8, None) == 1
+    assert st(L, f, A, None, 0.5, 8, None) == 1
+    assert st(L, f, A + 1, A + 4096, 0.5, 8, None) == 2     # odd address
+    assert st(L, f, A, A + 4097, 0.5, 8, None) == 2
+    assert st(L, f, A, A + 8, 0.5, 8, None) == 1            # v overlaps acc without being it
+    g = "bm_f16_scale"
+    assert st(L, g, A, 2.0, -1, None) == 1
+    assert st(L, g, A, 2.0, 0, None) == 0
+    assert st(L, g, None, 2.0, 8, None) == 1
+    assert st(L, g, A + 3, 2.0, 8, None) == 2
