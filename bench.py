@@ -352,6 +352,7 @@ def run_gpu(args, rank, world, local_rank):
         result["llama3_8b_prefill_layer"] = bench_llama_prefill(bm, dev, stream, torch)
         result["qwen3_0.6b_decode_step"] = bench_qwen3_decode(bm, dev, stream, torch)
         result["qwen3_0.6b_prefill_layer"] = bench_qwen3_prefill(bm, dev, stream, torch)
+        result["helpers"] = bench_helpers(bm, dev, stream, torch)
     return result
 
 
@@ -539,6 +540,42 @@ def bench_qwen3_decode(bm, dev, stream, torch, steps=10):
         (sum(t.numel() for t in base.values()) * layers + emb.numel()) * 2 / 1e9, 3), "launches": 4 * layers + 1}
     del lw, emb, base
     return res
+
+
+def bench_helpers(bm, dev, stream, torch, launches=8):
+    """The standalone pieces around the products, each timed as a CUDA graph of
+    `launches` back-to-back calls (PDL on) at a realistic size, as algorithmic bytes /
+    time: the RMS norm of a 512-token Llama-3-8B prefill micro-batch (f32 rows in, f32
+    and f16 out), the token-embedding lookup of 512 ids from the Llama-3-8B table, and
+    the f16 V-accumulator helpers over 64 M elements (larger than L2)."""
+    out = []
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(SEED)
+
+    def timed(name, shape, nbytes, call):
+        ms = graph_time(torch, stream, lambda: [call() for _ in range(launches)]) / launches
+        out.append({"op": name, "shape": shape, "us": round(ms * 1e3, 2), "GB_s": round(nbytes / ms / 1e6, 1)})
+
+    rows, hid = 512, 4096
+    x = torch.randn(rows, hid, device=dev, generator=gen)
+    g = torch.rand(hid, device=dev, generator=gen) + 0.5
+    y = torch.empty_like(x)
+    h = torch.empty(rows, hid, dtype=torch.float16, device=dev)
+    timed("bm_rms_norm_mul", "512 x 4096 (f32 and f16 out)", rows * hid * (4 + 4 + 2) + hid * 4,
+          lambda: bm.bm_rms_norm_mul(x, g, 1e-5, y, h, stream=stream))
+    vocab = 128256
+    E = (torch.randn(vocab, hid, device=dev, generator=gen) * 0.01).to(torch.float16)
+    ids = torch.randint(0, vocab, (rows,), device=dev, dtype=torch.int32, generator=gen)
+    emb = torch.empty(rows, hid, dtype=torch.float32, device=dev)
+    timed("bm_f16_get_rows", "512 ids of 128256 x 4096", rows * hid * (2 + 4) + rows * 4,
+          lambda: bm.bm_f16_get_rows(E, ids, emb, stream=stream))
+    n = 64 << 20
+    acc = (torch.randn(n, device=dev, generator=gen) * 0.1).to(torch.float16)
+    v = (torch.randn(n, device=dev, generator=gen) * 0.1).to(torch.float16)
+    timed("bm_f16_mad", "64 M elements", 6 * n, lambda: bm.bm_f16_mad(acc, v, 0.999, stream=stream))
+    timed("bm_f16_scale", "64 M elements", 4 * n, lambda: bm.bm_f16_scale(acc, 1.0001, stream=stream))
+    del x, y, h, E, ids, emb, acc, v
+    return out
 
 
 def bench_qwen3_prefill(bm, dev, stream, torch, reps=10):
@@ -914,6 +951,10 @@ def main():
     if "qwen3_0.6b_decode_step" in r:
         r["qwen3_0.6b_decode_step"]["pct_hbm"] = round(100.0 * r["qwen3_0.6b_decode_step"]["GB_s"] / hbm_peak, 1)
         line["qwen3_0.6b_decode_step"] = r["qwen3_0.6b_decode_step"]
+    if "helpers" in r:
+        for p in r["helpers"]:
+            p["pct_hbm"] = round(100.0 * p["GB_s"] / hbm_peak, 1)
+        line["helpers"] = r["helpers"]
     if "qwen3_0.6b_prefill_layer" in r:
         pq = r["qwen3_0.6b_prefill_layer"]
         pq["pct_bf16_dense_peak"] = round(100.0 * pq["TFLOP_s"] / float(peaks.get("bf16_tflops", 1900.0)), 1)
