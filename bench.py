@@ -825,6 +825,43 @@ def run_single(spec: str, reps: int):
     return 0
 
 
+def run_helper(name: str, reps: int):
+    """One of the bench's helpers (bench_helpers) at its size, `reps` times (for
+    profilers; prints nothing timed): mad, scale, norm or get_rows."""
+    import torch
+
+    import __graft_entry__
+    import f16_weight_gemv_gb300 as bm
+
+    __graft_entry__.build()
+    dev = torch.device("cuda", 0)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(SEED)
+    if name in ("mad", "scale"):
+        n = 64 << 20
+        acc = (torch.randn(n, device=dev, generator=gen) * 0.1).to(torch.float16)
+        v = (torch.randn(n, device=dev, generator=gen) * 0.1).to(torch.float16)
+        call = (lambda: bm.bm_f16_mad(acc, v, 0.999)) if name == "mad" else (lambda: bm.bm_f16_scale(acc, 1.0001))
+    elif name == "norm":
+        x = torch.randn(512, 4096, device=dev, generator=gen)
+        g = torch.rand(4096, device=dev, generator=gen) + 0.5
+        y = torch.empty_like(x)
+        h = torch.empty(512, 4096, dtype=torch.float16, device=dev)
+        call = lambda: bm.bm_rms_norm_mul(x, g, 1e-5, y, h)
+    elif name == "get_rows":
+        E = (torch.randn(128256, 4096, device=dev, generator=gen) * 0.01).to(torch.float16)
+        ids = torch.randint(0, 128256, (512,), device=dev, dtype=torch.int32, generator=gen)
+        out = torch.empty(512, 4096, dtype=torch.float32, device=dev)
+        call = lambda: bm.bm_f16_get_rows(E, ids, out)
+    else:
+        raise SystemExit("unknown helper " + name)
+    for _ in range(reps):
+        call()
+    torch.cuda.synchronize()
+    print(json.dumps({"helper": name, "reps": reps, "status": bm.bm_device_status()}))
+    return 0
+
+
 def run_prefill(reps: int):
     """The Llama-3-8B-shaped prefill layer (bench_llama_prefill), eagerly, `reps` times with
     programmatic dependent launch on (for profilers; prints nothing timed)."""
@@ -861,6 +898,8 @@ def main():
     ap.add_argument("--single", default=None, help="profile mode: run one product ROWSxKxNCOLS --reps times")
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--prefill", action="store_true", help="profile mode: run the Llama-3-8B prefill layer --reps times")
+    ap.add_argument("--helper", default=None, choices=["mad", "scale", "norm", "get_rows"],
+                    help="profile mode: run one of the helpers --reps times")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=20)
@@ -877,6 +916,8 @@ def main():
         return run_single(args.single, args.reps)
     if args.prefill:
         return run_prefill(args.reps)
+    if args.helper:
+        return run_helper(args.helper, args.reps)
 
     import torch
 
