@@ -754,11 +754,31 @@ def cpu_baseline(budget_s=10.0, budget_1core_s=4.0):
         n1, dt1 = timed(budget_1core_s)
     finally:
         oracle.set_threads(cores)
+    # the largest products on all cores: a deterministic subset of rows, the time scaled
+    # per row to the whole matrix (extrapolated, and said so)
+    products = []
+    for name, rows, k, nc, sub in (("llama3_8b.output", 128256, 4096, 512, 32), ("llama3_8b.gate", 14336, 4096, 1, 2048)):
+        W = synth.normal_f16(SEED, "cpu." + name, 0.01, (sub, k))
+        X = oracle.to_f16(synth.normal_f32(SEED, "cpu." + name + ".x", 1.0, (nc, k)))
+        t0 = time.perf_counter()
+        if nc == 1:
+            oracle.matvec(W, X[0])
+        else:
+            oracle.matmul(W, X)
+        full_s = (time.perf_counter() - t0) * rows / sub
+        entry = {"product": name, "rows": rows, "k": k, "ncols": nc, "rows_timed": sub,
+                 "seconds_extrapolated": round(full_s, 3)}
+        if nc == 1:
+            entry["GB_s"] = round(algorithmic_bytes(rows, k) / full_s / 1e9, 2)
+        else:
+            entry["TFLOP_s"] = round(2.0 * rows * k * nc / full_s / 1e12, 5)
+        products.append(entry)
     return {"value": round(nbytes * n / dt / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
             "sample": "%d full SmolLM2-135M decode steps (30 layers + logits, 269 MB of f16 weights each) "
                       "in %.1f s on the host" % (n, dt),
             "value_1core": round(nbytes * n1 / dt1 / 1e9, 4),
-            "sample_1core": "%d full steps in %.1f s on one core" % (n1, dt1), "host": host_cpu()}
+            "sample_1core": "%d full steps in %.1f s on one core" % (n1, dt1), "host": host_cpu(),
+            "products": products}
 
 
 def step_config(world, no_pdl):
