@@ -892,21 +892,26 @@ double plan_us(int64_t units_per_split, int64_t tiles128, int num_kb, int bn, in
 // model is free to choose (bm_set_stream_k(-1)) the balanced plan must be predicted
 // 10 % faster than the best other plan: measured gains were small (at most 3 % on the
 // Llama-3-8B shapes at 512 columns, 10 % on gate at 64), losses on others up to 8 %,
-// and the model is coarse.
+// and the model is coarse.  The exception is a product of three or more full waves
+// of whole 256-column tiles (the output product at 512 columns): there every SM streams
+// in both plans, so a k-block costs the same, the balanced plan only removes the idle
+// part of the last wave, and it measured 2-4 % faster in chains of launches; a 2 %
+// margin.  (At 16 and 64 columns the same rule measured no gain.)
 constexpr double kSkKblockUs[3] = {0.0, 0.55, 0.85};
 constexpr double kSkFixedUs = 1.0;
 constexpr double kSkStoreBytesPerUs = 5.5e6;  // all CTAs' partial-tile stores at once
 constexpr double kSkOverlap = 0.3;            // share of that hidden behind MMAs with two TMEM sets
 constexpr double kSkReadBytesPerUs = 1.5e5;   // one SM's piece loads
 constexpr double kSkMargin = 0.90;
+constexpr double kSkMarginManyWaves = 0.98;
 
 // Predicted time of balanced ranges over `units` row units of MT * 128 rows of each of
 // nt column tiles, `ctas` CTAs per column tile; nbuf TMEM accumulator sets.
-double plan_sk_us(int64_t units, int num_kb, int bn, int mt, int ctas, int64_t nt, int nbuf)
+double plan_sk_us(int64_t units, int num_kb, int bn, int mt, int ctas, int64_t nt, int nbuf, bool many_waves)
 {
     const int64_t iters = units * num_kb;
     const int64_t per = (iters + ctas - 1) / ctas;
-    double us = (double)per * kSkKblockUs[mt];
+    double us = (double)per * (many_waves ? kKblockUs[mt] : kSkKblockUs[mt]);
     const bool aligned = iters % ctas == 0 && per % num_kb == 0;  // every range whole tiles
     if (!aligned) {
         const double slot = (double)mt * kBM * bn * 4.0;
@@ -1033,8 +1038,9 @@ int plan_gemm(Plan *pl, int nmat, const int64_t *rows, int64_t k, int64_t ncols,
             const int64_t per_col = std::min<int64_t>(dev.sm_count / nt, units_rows * p.num_kb);  // CTAs per column
             if (sk_mode != 0 && ring_b >= kEpiWarps * kOwnerDepth * 4096 && per_col >= 1) {
                 const int nbuf = 2 * mt * pow2_at_least(bw) <= 512 ? 2 : 1;
-                const double us = plan_sk_us(units_rows, p.num_kb, bw, mt, (int)per_col, nt, nbuf);
-                consider(sk_mode == 1 ? us : us / kSkMargin, 1, 1);
+                const bool many_waves = tiles >= 3 * (int64_t)dev.sm_count && bw == 256;  // measured there only
+                const double us = plan_sk_us(units_rows, p.num_kb, bw, mt, (int)per_col, nt, nbuf, many_waves);
+                consider(sk_mode == 1 ? us : us / (many_waves ? kSkMarginManyWaves : kSkMargin), 1, 1);
             }
         }
     }
