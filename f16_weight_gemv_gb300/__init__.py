@@ -20,7 +20,7 @@ from . import _build
 __all__ = [
     "BmError", "lib", "bm_to_f16", "bm_f16_matvec", "bm_f16_matvec_multi", "bm_f16_matvec_act", "bm_f16_matvec_norm", "bm_rms_norm_mul", "bm_f16_matmul", "bm_f16_matmul_multi", "bm_f16_matmul_noalloc",
     "bm_f16_logits", "bm_f16_get_rows", "bm_f16_mad", "bm_f16_scale", "bm_takes_sgemm", "bm_device_status", "bm_status_string", "bm_last_error",
-    "bm_selftest_wait_timeout", "bm_set_pdl", "prepare", "Prepared", "PreparedGraph", "bm_set_exact_sgemm_cols", "bm_set_stream_k", "EXPORTS",
+    "bm_selftest_wait_timeout", "bm_set_pdl", "prepare", "Prepared", "PreparedGraph", "bm_set_exact_sgemm_cols", "bm_set_stream_k", "bm_tc_plan", "EXPORTS",
     "BM_MAX_K",
 ]
 
@@ -46,6 +46,7 @@ EXPORTS = {
     "bm_f16_scale": (_i, [_vp, C.c_float, _i64, _vp]),
     "bm_takes_sgemm": (_i, [_i64, _i64, _i64]),
     "bm_device_status": (_i, [_vp]),
+    "bm_tc_plan": (_i, [_i64, _i64, _i64, _i, C.POINTER(_i64)]),
     "bm_set_pdl": (_i, [_i]),
     "bm_set_exact_sgemm_cols": (_i, [_i]),
     "bm_set_stream_k": (_i, [_i]),
@@ -428,6 +429,15 @@ def bm_set_stream_k(mode: int) -> int:
     """Balanced k ranges for the tensor-core products: -1 where the time model
     predicts them faster (default), 0 never, 1 always; returns the old setting."""
     return int(lib().bm_set_stream_k(int(mode)))
+
+
+def bm_tc_plan(rows: int, k: int, ncols: int, noalloc: bool = False) -> dict:
+    """The plan of a tensor-core product on the current device (nothing launched):
+    row tiles per unit, tile columns, k-splits, balanced k ranges, scratch bytes, CTAs."""
+    info = (C.c_int64 * 6)()
+    _check(lib().bm_tc_plan(int(rows), int(k), int(ncols), 1 if noalloc else 0, info), "bm_tc_plan")
+    return {"mt": int(info[0]), "bn": int(info[1]), "splits": int(info[2]), "balanced": int(info[3]),
+            "scratch_bytes": int(info[4]), "ctas": int(info[5])}
 
 
 def bm_status_string(status: int) -> str:

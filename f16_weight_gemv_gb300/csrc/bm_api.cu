@@ -495,6 +495,21 @@ int bm_set_stream_k(int mode)
     return g_stream_k.exchange(mode < 0 ? -1 : mode > 0 ? 1 : 0);
 }
 
+int bm_tc_plan(int64_t rows, int64_t k, int64_t ncols, int noalloc, int64_t *info)
+{
+    clear_error();
+    if (!info) return fail(BM_ERR_INVALID_ARG, "bm_tc_plan: null info");
+    if (k < 1 || k > BM_MAX_K || rows < 1 || !bm_takes_sgemm(rows, k, ncols))
+        return fail(BM_ERR_INVALID_ARG, "bm_tc_plan: %lld x %lld x %lld is not a tensor-core product",
+                    (long long)rows, (long long)k, (long long)ncols);
+    if (!sizes_ok(rows, k) || !sizes_ok(ncols, k) || ncols > INT64_MAX / 8 / rows)
+        return fail(BM_ERR_INVALID_ARG, "bm_tc_plan: sizes overflow");
+    int st;
+    DeviceInfo dev;
+    if (!current_device(&dev, &st)) return st;
+    return plan_info_gemm_tc(rows, k, ncols, noalloc != 0, dev, info);
+}
+
 int bm_device_status(bm_stream_t stream)
 {
     clear_error();

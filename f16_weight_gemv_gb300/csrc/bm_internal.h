@@ -83,6 +83,10 @@ int launch_gemm_tc_multi(int nmat, const uint16_t *const *W, const int64_t *rows
 // a stream-ordered allocation (no allocation of any kind).
 int launch_gemm_tc_noalloc(const uint16_t *W, int64_t rows, int64_t k, const uint16_t *X, int64_t ncols,
                            float *Y, cudaStream_t s, const DeviceInfo &dev);
+// The plan the tensor-core product takes for one rows x k x ncols product on the current
+// device (noalloc: bm_f16_matmul_noalloc's plan): info[0..5] = row tiles per unit (MT),
+// tile columns, k-splits, balanced k ranges (0/1), scratch bytes, CTAs.
+int plan_info_gemm_tc(int64_t rows, int64_t k, int64_t ncols, bool noalloc, const DeviceInfo &dev, int64_t *info);
 // Self-test of the bounded waits: a 128 x 64 x 16 product whose producer never
 // fills its only stage, so the MMA issuer gives up after `timeout_ns`.
 int launch_gemm_tc_withheld(const uint16_t *W, int64_t rows, int64_t k, const uint16_t *X, int64_t ncols,

@@ -258,7 +258,7 @@ __device__ __forceinline__ Unit unit_of(const GemmParams &p, int u)
     x.m0 = local * MT * kBM;
     x.n0 = nt * p.bn;
     x.tile0 = (pick(p.tbeg, m) + local * MT) * p.nt + nt;
-    x.kb0 = p.num_kb * x.s / p.splits;  // num_kb <= 1024, splits <= 8: no overflow
+    x.kb0 = p.num_kb * x.s / p.splits;  // num_kb < 2^25 (k < 2^31), s < splits <= 8: below 2^31
     x.kb1 = p.num_kb * (x.s + 1) / p.splits;
     return x;
 }
@@ -977,10 +977,41 @@ struct Plan {
     size_t ws_bytes;
 };
 
+template <int MT>
+void set_smem_attr(const DeviceInfo &dev)
+{
+    int dev_id = 0;
+    cudaGetDevice(&dev_id);
+    std::call_once(g_attr_once[dev_id & (kMaxDevices - 1)][MT - 1], [&] {
+        cudaFuncSetAttribute(k_gemm_tc<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, dev.max_smem_optin - 1024);
+    });
+}
+
+// CTAs of k_gemm_tc<mt> with `smem` bytes of dynamic shared memory that one SM can
+// hold at once, by the occupancy calculator (0 when the query fails).
+int resident_ctas_per_sm(int mt, size_t smem, const DeviceInfo &dev)
+{
+    int n = 0;
+    cudaError_t e;
+    if (mt == 2) {
+        set_smem_attr<2>(dev);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_gemm_tc<2>, kThreads, smem);
+    } else {
+        set_smem_attr<1>(dev);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_gemm_tc<1>, kThreads, smem);
+    }
+    if (e != cudaSuccess) {
+        cudaGetLastError();  // a failed query leaves no sticky error behind
+        return 0;
+    }
+    return n;
+}
+
 // Plans one launch over nmat matrices of rows[m] x k sharing ncols activation columns.
-// sk_mode: balanced k ranges never (0), always (1) or where predicted faster (-1).
+// sk_mode: balanced k ranges never (0), always (1) or where predicted faster (-1);
+// max_splits: the most k-splits a plan may take (1: none).
 int plan_gemm(Plan *pl, int nmat, const int64_t *rows, int64_t k, int64_t ncols, const DeviceInfo &dev,
-              bool allow_split, bool allow_mt2, int sk_mode)
+              int max_splits, bool allow_mt2, int sk_mode)
 {
     if (nmat < 1 || nmat > kMaxMats) return fail(BM_ERR_INVALID_ARG, "tensor-core product: 1..4 matrices");
     GemmParams &p = pl->p;
@@ -1030,7 +1061,7 @@ int plan_gemm(Plan *pl, int nmat, const int64_t *rows, int64_t k, int64_t ncols,
                 }
             };
             if (sk_mode != 1)
-                for (int sp = 1; sp <= (allow_split ? std::min(kMaxSplits, p.num_kb) : 1); sp++)
+                for (int sp = 1; sp <= std::max(1, std::min(std::min(kMaxSplits, max_splits), p.num_kb)); sp++)
                     consider(plan_us(tiles, tiles128, p.num_kb, bw, mt, sp, dev.sm_count, total_rows, ncols), sp, 0);
             // balanced ranges need the operand ring to hold the owners' read buffers
             const int stage_b = mt * kTileABytes + bw * kBK * 2;
@@ -1083,18 +1114,21 @@ int plan_gemm(Plan *pl, int nmat, const int64_t *rows, int64_t k, int64_t ncols,
     const size_t one_per_sm = (size_t)dev.max_smem_optin / 2 + 4096;
     pl->smem = std::max(smem, one_per_sm);
     pl->ws_bytes = p.splits > 1 ? (size_t)p.tbeg[nmat] * p.nt * p.splits * p.bn * kBM * sizeof(float) : 0;
-    if (sk) pl->ws_bytes = sk_flags_offset(pl->grid, p.slot_floats) + (size_t)pl->grid * kEpiWarps * 8;
+    if (sk) {
+        // An owner waits for the CTAs below it, so every CTA of the grid must be resident
+        // at once: one per SM by design, confirmed by the occupancy calculator (a plan the
+        // SMs could not hold whole falls back to the whole-tile plans).
+        if (resident_ctas_per_sm(mt_unit, pl->smem, dev) < 1 || pl->grid > dev.sm_count)
+            return plan_gemm(pl, nmat, rows, k, ncols, dev, max_splits, allow_mt2, 0);
+        pl->ws_bytes = sk_flags_offset(pl->grid, p.slot_floats) + (size_t)pl->grid * kEpiWarps * 8;
+    }
     return BM_OK;
 }
 
 template <int MT>
 int launch_mt(const Plan &pl, const TmaMaps &maps, cudaStream_t s, const DeviceInfo &dev)
 {
-    int dev_id = 0;
-    cudaGetDevice(&dev_id);
-    std::call_once(g_attr_once[dev_id & (kMaxDevices - 1)][MT - 1], [&] {
-        cudaFuncSetAttribute(k_gemm_tc<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, dev.max_smem_optin - 1024);
-    });
+    set_smem_attr<MT>(dev);
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3((unsigned)pl.grid);
     cfg.blockDim = dim3(kThreads);
@@ -1172,7 +1206,7 @@ int launch_gemm_tc_multi(int nmat, const uint16_t *const *W, const int64_t *rows
     unsigned int *err = device_error_word();
     if (!err) return fail(BM_ERR_CUDA, "tensor-core product: device error word unavailable");
     Plan pl;
-    int st = plan_gemm(&pl, nmat, rows, k, ncols, dev, true, true, stream_k_mode());
+    int st = plan_gemm(&pl, nmat, rows, k, ncols, dev, kMaxSplits, true, stream_k_mode());
     if (st != BM_OK) return st;
     for (int m = 0; m < nmat; m++) pl.p.Y[m] = Y[m];
     pl.p.err = err;
@@ -1227,16 +1261,30 @@ unsigned char *g_scratch_ptr[kMaxDevices];
 cudaError_t g_scratch_status[kMaxDevices];
 }  // namespace
 
+// The plan of the no-allocation product: whole tiles (no balanced ranges), and, when
+// the fastest plan's partial tiles would not fit the scratch, the fastest plan with
+// fewer k-splits whose partials do -- at worst no split, which needs no scratch.
+int plan_noalloc(Plan *pl, int64_t rows, int64_t k, int64_t ncols, const DeviceInfo &dev)
+{
+    int max_splits = kMaxSplits;
+    while (true) {
+        int st = plan_gemm(pl, 1, &rows, k, ncols, dev, max_splits, true, 0);
+        if (st != BM_OK) return st;
+        if (pl->ws_bytes <= kNoAllocScratchBytes || pl->p.splits <= 1) return BM_OK;
+        max_splits = pl->p.splits - 1;
+    }
+}
+
 int launch_gemm_tc_noalloc(const uint16_t *W, int64_t rows, int64_t k, const uint16_t *X, int64_t ncols, float *Y,
                            cudaStream_t s, const DeviceInfo &dev)
 {
     unsigned int *err = device_error_word();
     if (!err) return fail(BM_ERR_CUDA, "no-allocation product: device error word unavailable");
     Plan pl;
-    int st = plan_gemm(&pl, 1, &rows, k, ncols, dev, true, true, 0);
+    int st = plan_noalloc(&pl, rows, k, ncols, dev);
     if (st != BM_OK) return st;
     const size_t need = pl.ws_bytes;
-    if (need > kNoAllocScratchBytes)
+    if (need > kNoAllocScratchBytes)  // cannot happen: an unsplit plan needs no scratch
         return fail(BM_ERR_INVALID_ARG,
                     "bm_f16_matmul_noalloc: this product needs %zu bytes of split-k scratch; the static scratch "
                     "holds %zu (use bm_f16_matmul)",
@@ -1270,13 +1318,28 @@ int launch_gemm_tc_withheld(const uint16_t *W, int64_t rows, int64_t k, const ui
     unsigned int *err = device_error_word();
     if (!err) return fail(BM_ERR_CUDA, "tensor-core product: device error word unavailable");
     Plan pl;
-    int st = plan_gemm(&pl, 1, &rows, k, ncols, dev, false, false, 0);
+    int st = plan_gemm(&pl, 1, &rows, k, ncols, dev, 1, false, 0);
     if (st != BM_OK) return st;
     pl.p.Y[0] = Y;
     pl.p.err = err;
     pl.p.timeout_ns = timeout_ns;
     pl.p.withhold_first_load = 1;
     return launch_plan(pl, &W, X, s, dev);
+}
+
+int plan_info_gemm_tc(int64_t rows, int64_t k, int64_t ncols, bool noalloc, const DeviceInfo &dev, int64_t *info)
+{
+    Plan pl;
+    int st = noalloc ? plan_noalloc(&pl, rows, k, ncols, dev)
+                     : plan_gemm(&pl, 1, &rows, k, ncols, dev, kMaxSplits, true, stream_k_mode());
+    if (st != BM_OK) return st;
+    info[0] = pl.mt_per_unit;
+    info[1] = pl.p.bn;
+    info[2] = pl.p.splits;
+    info[3] = pl.p.sk;
+    info[4] = (int64_t)pl.ws_bytes;
+    info[5] = pl.grid;
+    return BM_OK;
 }
 
 }  // namespace bm

@@ -202,14 +202,19 @@ int bm_f16_matmul_multi(int nmat, const uint16_t *const *W, const int64_t *rows,
  * same layout, validation, path selection and results as bm_f16_matmul with
  * balanced k ranges off (bm_set_stream_k(0)); where bm_f16_matmul takes them the
  * two results may differ in their last bits, both within the tensor-core bound.
- *   - A product whose split-k workspace would exceed the scratch is refused with
- *     BM_ERR_INVALID_ARG and a reason (bm_last_error); nothing is launched.
+ *   - When the fastest plan's split-k partial tiles would not fit the scratch,
+ *     the product takes the fastest plan with fewer k-splits whose partials do
+ *     (at worst no split, which needs no scratch), so no valid product is
+ *     refused for its size; it may then run slower than bm_f16_matmul.  Should
+ *     a plan ever exceed the scratch all the same, the call fails with
+ *     BM_ERR_INVALID_ARG and a reason (bm_last_error) and launches nothing.
  *   - The first call on a device looks up the scratch's device address (once per
  *     device, with that device current); make that first call before any stream
  *     capture.
  *   - Every call shares the one scratch array, which keeps the last call's
- *     contents; the parts that must start at zero are cleared on the stream by
- *     each call.  Calls whose kernels overlap on the GPU (e.g. on two streams at
+ *     contents.  Nothing in it needs to start at zero: every split writes its
+ *     whole partial tile before the reduction reads it, so stale contents are
+ *     never read.  Calls whose kernels overlap on the GPU (e.g. on two streams at
  *     once) race on the scratch and must be ordered by the caller.
  */
 int bm_f16_matmul_noalloc(const uint16_t *W, int64_t rows, int64_t k, const uint16_t *X,
@@ -303,9 +308,26 @@ int bm_set_exact_sgemm_cols(int ncols);
  * tensor-core bound in every mode and is repeatable (the same bits for the same
  * product, mode and GPU).  The workspace (one partial tile per SM and a flag word
  * per epilogue warp) comes from the library's stream-ordered pool like the k-split
- * one; bm_f16_matmul_noalloc never uses this mode.  Returns the previous setting.
+ * one; bm_f16_matmul_noalloc never uses this mode.  An owner waits for the SMs
+ * below it, so the mode is taken only where the occupancy calculator confirms that
+ * one CTA of the product fits on every SM the grid uses; otherwise the product
+ * falls back to whole tiles.  Returns the previous setting.
  */
 int bm_set_stream_k(int mode);
+
+/*
+ * The plan a tensor-core product takes (introspection, no counterpart on the
+ * pages): for a bm_takes_sgemm product of rows x k x ncols on the current device,
+ * under the current bm_set_stream_k mode, or bm_f16_matmul_noalloc's plan when
+ * noalloc != 0.  Writes info[0..5] (host array of 6): 128-row tiles per work
+ * unit (1 or 2), tile columns, k-splits, balanced k ranges (0 or 1), scratch
+ * bytes (split-k partial tiles, or the balanced ranges' slots and flags) and
+ * CTAs.  It launches and allocates nothing.  The plan is the same whatever
+ * bm_set_exact_sgemm_cols says; whether the product reaches the tensor cores at
+ * all follows bm_f16_matmul's path selection.  BM_ERR_INVALID_ARG for sizes the
+ * tensor-core product does not take (rows % 4, k % 8, ncols < 2, k > BM_MAX_K).
+ */
+int bm_tc_plan(int64_t rows, int64_t k, int64_t ncols, int noalloc, int64_t *info);
 
 /* Waits for `stream`, then reads and clears this library's device error word
  * on the current device: BM_OK, BM_ERR_TIMEOUT (a kernel gave up a bounded

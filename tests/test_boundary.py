@@ -227,3 +227,14 @@ def test_mad_and_scale_host_checks(L):
     assert st(L, g, A, 2.0, 0, None) == 0
     assert st(L, g, None, 2.0, 8, None) == 1
     assert st(L, g, A + 3, 2.0, 8, None) == 2
+
+
+def test_tc_plan_host_checks(L):
+    info = (C.c_int64 * 6)()
+    assert st(L, "bm_tc_plan", 4096, 4096, 512, 0, None) == 1      # null info
+    assert st(L, "bm_tc_plan", 13, 4096, 512, 0, info) == 1         # rows % 4 != 0: not a tensor-core product
+    assert st(L, "bm_tc_plan", 4096, 33, 512, 0, info) == 1         # k % 8 != 0
+    assert st(L, "bm_tc_plan", 4096, 4096, 1, 0, info) == 1         # one column
+    assert st(L, "bm_tc_plan", 4096, 65544, 512, 0, info) == 1      # k > BM_MAX_K
+    assert b"tensor-core" in L.bm_last_error()
+
