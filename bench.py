@@ -1,35 +1,36 @@
 #!/usr/bin/env python3
 """Benchmark of the F16-weight products on one GB300 (or N replicas).
 
-Default workload: a SmolLM2-135M-shaped decode step -- 30 layers of
-[fused Q/K/V product (576+192+192 rows x 576), O (576 x 576), fused gate/up
-(2 x 1536 x 576), down (576 x 1536)] then the tied logits (49152 x 576): one
-column, 121 products over 269 MB of f16 weights (more than the 129 MB L2),
-seeded synthetic weights N(0, 0.02) and f32 activations N(0, 1).  Each product
-is one bm_f16_matvec_act call: the f32 activation is rounded to f16 and
-multiplied in the same launch.  The step is captured once as a CUDA graph
+Default workload (the JSON line's `value`): a Llama-3-8B-shaped decode step --
+32 layers of [fused Q/K/V product (4096+1024+1024 rows x 4096), O (4096 x 4096),
+fused gate/up (2 x 14336 x 4096), down (4096 x 14336)] then the output product
+(128256 x 4096): one column, 129 products over 15.0 GB of f16 weights (far more
+than the 129 MB L2), seeded synthetic weights N(0, 0.01) (one layer drawn and
+copied to 32 distinct buffers, so every product streams from HBM) and a distinct
+f32 activation N(0, 1) for every product.  Each product is one
+bm_f16_matvec_act call: the f32 activation is rounded to f16 and multiplied in
+the same launch (k_gemv_stream).  The step is captured once as a CUDA graph
 (programmatic dependent launch on) and replayed; `value` is algorithmic bytes
 per step / time per step.
 
-Extra objects in the same JSON line:
-  roofline     -- the step's kernel (k_gemv_stream) against the measured HBM peak
-  unfused      -- the same step as bm_to_f16 + bm_f16_matvec[_multi]/bm_f16_logits
-                  (242 launches)
-  norm_front_end -- the step with the RMS norm ahead of Q/K/V, gate/up and the
-                  logits fused into those products (bm_f16_matvec_norm)
-  products     -- single products of the Llama-3-8B / Qwen3-0.6B shapes:
-                  decode GB/s and 512-column tensor-core TFLOP/s
-  llama3_8b_decode_step / llama3_8b_prefill_layer -- a whole Llama-3-8B-shaped
-                  decode step (129 products), and one layer's 7 products for a
-                  512-token prefill micro-batch (with and without PDL)
-  e2e          -- the same step through the Python binding without a graph (the
-                  step's calls recorded once by prepare(), replayed each step; and
-                  made through the wrappers each time), with the step's activations
-                  copied from pinned host memory and the logits copied back every step
-  cpu_baseline -- the CPU oracle on this host, full decode steps
+Objects in the same JSON line:
+  roofline     -- the step's only kernel (k_gemv_stream) against the measured HBM peak,
+                  with the DRAM traffic per launch from an ncu launch list
+  e2e          -- the same step end to end: every step the activations are copied
+                  from pinned host memory, the 129 recorded calls are made one C call
+                  each, the logits are copied back and the host waits for them
+  cpu_baseline -- the CPU oracle on this host, on a bounded sample of the same step
+  prefill      -- the second half of the metric: one Llama-3-8B-shaped layer's
+                  products for a 512-token prefill micro-batch on the tensor cores,
+                  TFLOP/s against the measured dense bf16 peak
+  smollm2_135m_decode_step, qwen3_0.6b_decode_step -- the smaller decode steps
+                  (launch-latency-bound), with their unfused and norm-fused variants
+  products     -- single products: one and few columns (HBM GB/s), 512 columns
+                  (TFLOP/s), and the exact fallback and unaligned shapes
+  helpers      -- rms_norm_mul, get_rows, mad and scale
 
 `--impl reference` times the CPU oracle (the only reference that exists for
-this method) on the same workload and prints the same JSON line.
+this method) on the same workload and metric, on a bounded sample of the step.
 """
 from __future__ import annotations
 
@@ -48,77 +49,106 @@ sys.path.insert(0, ROOT)
 
 import synth  # noqa: E402
 
-HIDDEN, FFN, VOCAB, LAYERS = 576, 1536, 49152, 30
-Q_ROWS, KV_ROWS = 9 * 64, 3 * 64
 SEED = 0
-W_SIGMA, A_SIGMA = 0.02, 1.0
+A_SIGMA = 1.0
+
+# The decode steps' shapes.  distinct: every layer's weights drawn on their own
+# (else one layer is drawn and copied to every layer's buffers).
+MODELS = {
+    "smollm2_135m": {"prefix": "smollm2", "hidden": 576, "q": 9 * 64, "kv": 3 * 64, "o_in": 576, "ffn": 1536,
+                     "vocab": 49152, "head": "token_embd", "layers": 30, "sigma": 0.02, "distinct": True},
+    "qwen3_0.6b": {"prefix": "qwen3", "hidden": 1024, "q": 16 * 128, "kv": 8 * 128, "o_in": 16 * 128, "ffn": 3072,
+                   "vocab": 151936, "head": "embd", "layers": 28, "sigma": 0.02, "distinct": False},
+    "llama3_8b": {"prefix": "llama3_8b", "hidden": 4096, "q": 32 * 128, "kv": 8 * 128, "o_in": 32 * 128,
+                  "ffn": 14336, "vocab": 128256, "head": "output", "layers": 32, "sigma": 0.01, "distinct": False},
+}
+HEADLINE = "llama3_8b"
 
 
-# DRAM traffic per launch of the step's kernel, from the ncu launch list of one
-# timed step (profiles/decode_step_smollm2_launches.md), valid only for the kernel
-# source it was measured on (sha256 prefix of k_gemv_stream.cu).
-NCU_TRAFFIC = {"kernel": "k_gemv_stream", "source": "f16_weight_gemv_gb300/csrc/k_gemv_stream.cu",
-               "sha256_16": "78fefbba59017a3a", "bytes_per_launch": 2294604}
+def weight_name(model: str, layer: int, mat: str) -> str:
+    m = MODELS[model]
+    if mat == "head":
+        return "%s.%s" % (m["prefix"], m["head"])
+    return "%s.l%d.%s" % (m["prefix"], layer, mat) if m["distinct"] else "%s.%s" % (m["prefix"], mat)
 
 
-def ncu_traffic():
-    import hashlib
-    try:
-        with open(os.path.join(ROOT, NCU_TRAFFIC["source"]), "rb") as f:
-            sha = hashlib.sha256(f.read()).hexdigest()[:16]
-    except OSError:
-        return None
-    return NCU_TRAFFIC["bytes_per_launch"] if sha == NCU_TRAFFIC["sha256_16"] else None
+def step_plan(model: str = HEADLINE, layers: int | None = None):
+    """The decode step as an ordered list of calls (kind, [(output key, weight name,
+    rows)], k, activation id); kind is 'multi' (one launch over several matrices),
+    'mv' or 'logits'.  Every call has its own activation."""
+    m = MODELS[model]
+    L = m["layers"] if layers is None else layers
+    h, plan, a = m["hidden"], [], 0
+    for i in range(L):
+        def mats(*names):
+            return [("l%d.%s" % (i, n), weight_name(model, i, n), r) for n, r in names]
+        plan.append(("multi", mats(("q", m["q"]), ("k", m["kv"]), ("v", m["kv"])), h, a))
+        plan.append(("mv", mats(("o", h)), m["o_in"], a + 1))
+        plan.append(("multi", mats(("gate", m["ffn"]), ("up", m["ffn"])), h, a + 2))
+        plan.append(("mv", mats(("down", h)), m["ffn"], a + 3))
+        a += 4
+    plan.append(("logits", [("head", weight_name(model, 0, "head"), m["vocab"])], h, a))
+    return plan
+
+
+def act_name(model: str, a: int) -> str:
+    return "%s.act%d" % (MODELS[model]["prefix"], a)
+
+
+def step_bytes(plan, fused=True):
+    """Algorithmic bytes of one step.  Fused: each call reads its f32 activation (4k)
+    and rounds it in the kernel; unfused: a rounding call (6 bytes per element), then
+    the product reads the f16 activation (2k).  Weights 2*rows*k and outputs 4*rows
+    either way; a multi-matrix call reads its activation once."""
+    tot = 0
+    for _, mats, k, _ in plan:
+        tot += sum(2 * r * k + 4 * r for _, _, r in mats) + (4 * k if fused else 6 * k + 2 * k)
+    return tot
+
+
+def weight_bytes(plan):
+    return sum(2 * r * k for _, mats, k, _ in plan for _, _, r in mats)
 
 
 def algorithmic_bytes(rows, k, ncols=1):
     return 2 * rows * k + 2 * k * ncols + 4 * rows * ncols
 
 
-def step_plan():
-    """The decode step as an ordered list of calls: ('round', n, act_id) or
-    ('multi'|'mv'|'logits', [(name, rows)], k, act_id)."""
-    plan = []
-    a = 0
-    for L in range(LAYERS):
-        plan.append(("round", HIDDEN, a))
-        plan.append(("multi", [("l%d.q" % L, Q_ROWS), ("l%d.k" % L, KV_ROWS), ("l%d.v" % L, KV_ROWS)], HIDDEN, a))
-        a += 1
-        plan.append(("round", HIDDEN, a))
-        plan.append(("mv", [("l%d.o" % L, HIDDEN)], HIDDEN, a))
-        a += 1
-        plan.append(("round", HIDDEN, a))
-        plan.append(("multi", [("l%d.gate" % L, FFN), ("l%d.up" % L, FFN)], HIDDEN, a))
-        a += 1
-        plan.append(("round", FFN, a))
-        plan.append(("mv", [("l%d.down" % L, HIDDEN)], FFN, a))
-        a += 1
-    plan.append(("round", HIDDEN, a))
-    plan.append(("logits", [("token_embd", VOCAB)], HIDDEN, a))
-    return plan
+# DRAM traffic of k_gemv_stream per product shape (rows x k, matrices of one launch),
+# from the ncu launch list of a two-layer Llama-3-8B-shaped step (read + write bytes,
+# profiles/decode_step_llama3_8b_launches.md), valid only for the kernel source it was
+# measured on (sha256 prefix of k_gemv_stream.cu).  Shapes per launch do not depend on
+# the number of layers, so the full step's traffic is these, summed over its launches.
+NCU_TRAFFIC = {"kernel": "k_gemv_stream", "source": "f16_weight_gemv_gb300/csrc/k_gemv_stream.cu",
+               "sha256_16": None, "bytes_per_call": {}}
 
 
-def step_bytes(plan, fused=True):
-    """Algorithmic bytes of one step.  Fused: each product call reads its f32
-    activation (4k) and rounds it in the kernel; unfused: a rounding call (6 bytes
-    per element) then the product reads the f16 activation (2k).  Weights 2*rows*k
-    and outputs 4*rows either way; a fused multi-matrix call reads its activation once."""
+def _source_sha16(rel):
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            return hashlib.sha256(f.read()).hexdigest()[:16]
+    except OSError:
+        return None
+
+
+def call_key(mats, k):
+    return "+".join("%dx%d" % (r, k) for _, _, r in mats)
+
+
+def ncu_traffic_per_launch(plan):
+    """Mean DRAM bytes per launch of the step from the recorded per-shape traffic, or
+    None when the kernel changed since (or a shape was not measured)."""
+    t = NCU_TRAFFIC
+    if not t["sha256_16"] or _source_sha16(t["source"]) != t["sha256_16"]:
+        return None
     tot = 0
-    for op in plan:
-        if op[0] == "round":
-            tot += 0 if fused else 6 * op[1]
-        else:
-            k = op[2]
-            tot += sum(2 * r * k + 4 * r for _, r in op[1]) + (4 * k if fused else 2 * k)
-    return tot
-
-
-def act_sizes(plan):
-    sizes = {}
-    for op in plan:
-        if op[0] == "round":
-            sizes[op[2]] = op[1]
-    return sizes
+    for _, mats, k, _ in plan:
+        b = t["bytes_per_call"].get(call_key(mats, k))
+        if b is None:
+            return None
+        tot += b
+    return int(round(tot / len(plan)))
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -138,7 +168,7 @@ class ClockSampler:
     def start(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
-                                          "-i", str(self.index), "-lms", "100"], stdout=subprocess.PIPE,
+                                          "-i", str(self.index), "-lms", "25"], stdout=subprocess.PIPE,
                                          stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -149,9 +179,6 @@ class ClockSampler:
     def _read(self):
         for line in self.proc.stdout:
             self.lines.append((time.time(), line.strip()))
-
-    def mark(self):
-        return time.time()
 
     def stop(self):
         if self.proc is not None:
@@ -171,7 +198,9 @@ class ClockSampler:
                 rows.append((t, float(parts[1]), float(parts[2]), parts[4:9]))
             except ValueError:
                 continue
-        inside = [r for r in rows if t0 - 0.15 <= r[0] <= t1 + 0.15] or rows[-3:]
+        inside = [r for r in rows if t0 - 0.03 <= r[0] <= t1 + 0.03]
+        if len(inside) < 3:  # a short timed region: the samples nearest to it
+            inside = sorted(rows, key=lambda r: abs(r[0] - 0.5 * (t0 + t1)))[:3]
         if not inside:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
         names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
@@ -182,6 +211,174 @@ class ClockSampler:
                     reasons.add(n)
         return {"sm_mhz": float(np.median([r[1] for r in inside])), "sm_max_mhz": max(r[2] for r in inside),
                 "reasons": sorted(reasons), "samples": len(inside)}
+
+
+# ----------------------------------------------------------------------------- decode steps
+
+
+class DecodeStep:
+    """A decode step of `model` resident on the GPU: weights, one f32 activation per
+    call (packed, 32-byte aligned slices), one output per matrix and layer.  With
+    keep_host the host copies of the distinct weights and of the activations stay
+    (for the parity tests)."""
+
+    def __init__(self, bm, torch, dev, model=HEADLINE, layers=None, keep_host=False):
+        self.bm, self.torch, self.model = bm, torch, model
+        spec = MODELS[model]
+        self.plan = step_plan(model, layers)
+        self.host_w = {}
+        dev_by_name = {}
+        for _, mats, k, _ in self.plan:
+            for _, wn, rows in mats:
+                if wn in dev_by_name:
+                    continue
+                w = synth.normal_f16(SEED, wn, spec["sigma"], (rows, k))
+                dev_by_name[wn] = torch.from_numpy(w.view(np.float16)).to(dev)
+                if keep_host:
+                    self.host_w[wn] = w
+        # one layer drawn: every layer gets its own copy (distinct memory, streamed from HBM)
+        self.weights = {}
+        for _, mats, _, _ in self.plan:
+            for key, wn, _ in mats:
+                layer0 = key.startswith("l0.") or key == "head" or spec["distinct"]
+                self.weights[key] = dev_by_name[wn] if layer0 else dev_by_name[wn].clone()
+        del dev_by_name
+        self.offs, o = {}, 0
+        for _, _, k, a in self.plan:
+            self.offs[a] = (o, k)
+            o += (k + 7) // 8 * 8
+        self.act_host = np.zeros(o, dtype=np.float32)
+        for a, (off, k) in self.offs.items():
+            self.act_host[off:off + k] = synth.normal_f32(SEED, act_name(model, a), A_SIGMA, k)
+        self.act = torch.from_numpy(self.act_host).to(dev)
+        self.act_f16 = None
+        self.outs = {key: torch.empty(rows, dtype=torch.float32, device=dev)
+                     for _, mats, _, _ in self.plan for key, _, rows in mats}
+        self.norm_w = torch.from_numpy((1.0 + synth.normal_f32(SEED, "%s.norm" % spec["prefix"], 0.2,
+                                                               spec["hidden"])).astype(np.float32)).to(dev)
+        self.bytes = step_bytes(self.plan, True)
+
+    def activation(self, a):
+        off, k = self.offs[a]
+        return self.act[off:off + k]
+
+    def run(self, s, mode="act"):
+        """mode 'act': one bm_f16_matvec_act per call (the benchmarked step); 'unfused':
+        bm_to_f16, then bm_f16_matvec[_multi] / bm_f16_logits; 'norm': the RMS norm fused
+        ahead of Q/K/V, gate/up and the head (bm_f16_matvec_norm)."""
+        bm = self.bm
+        if mode == "unfused" and self.act_f16 is None:
+            self.act_f16 = self.torch.empty(self.act.numel(), dtype=self.torch.float16, device=self.act.device)
+        for kind, mats, k, a in self.plan:
+            W = [self.weights[key] for key, _, _ in mats]
+            Y = [self.outs[key] for key, _, _ in mats]
+            x = self.activation(a)
+            if mode == "act" or (mode == "norm" and kind == "mv"):
+                bm.bm_f16_matvec_act(W, x, Y, stream=s)
+            elif mode == "norm":
+                bm.bm_f16_matvec_norm(W, x, self.norm_w, 1e-5, Y, stream=s)
+            else:
+                off, _ = self.offs[a]
+                h = self.act_f16[off:off + k]
+                bm.bm_to_f16(x, h, stream=s)
+                if kind == "multi":
+                    bm.bm_f16_matvec_multi(W, h, Y, stream=s)
+                elif kind == "mv":
+                    bm.bm_f16_matvec(W[0], h, Y[0], stream=s)
+                else:
+                    bm.bm_f16_logits(W[0], h.view(1, -1), Y[0].view(1, -1), stream=s)
+
+    def head(self):
+        return self.outs["head"]
+
+
+def capture(torch, stream, fn):
+    """fn() once eagerly (attribute set-up happens outside capture), then captured."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        fn()
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    torch.cuda.synchronize()
+    return g
+
+
+def replay_time(torch, stream, g, steps, warmup, world=1):
+    """ms per replay of graph g: `warmup` untimed replays, then `steps` between CUDA
+    events on the launching stream, a barrier and a synchronize on both sides."""
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            g.replay()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(steps):
+            g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    return e0.elapsed_time(e1) / steps
+
+
+def e2e_time(torch, stream, step, calls, steps):
+    """ms per step end to end: each step copies the step's activations from pinned host
+    memory, makes the step's calls, copies the logits back and waits for them on the
+    host (wall clock over `steps` such steps, after two untimed ones)."""
+    act_pinned = torch.from_numpy(step.act_host).pin_memory()
+    head_host = torch.empty(step.head().numel(), dtype=torch.float32).pin_memory()
+
+    def one():
+        with torch.cuda.stream(stream):
+            step.act.copy_(act_pinned, non_blocking=True)
+            calls()
+            head_host.copy_(step.head(), non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(2):
+        one()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one()
+    return (time.perf_counter() - t0) * 1e3 / steps, int(step.act_host.nbytes), int(head_host.numel() * 4)
+
+
+def decode_side(bm, torch, dev, stream, model, steps=20, variants=True):
+    """A smaller decode step as a side measurement: the fused step (as the headline),
+    and optionally its unfused and norm-fused variants and its end-to-end time."""
+    st = DecodeStep(bm, torch, dev, model)
+    g = capture(torch, stream, lambda: st.run(stream))
+    ms = replay_time(torch, stream, g, steps, 5)
+    res = {"ms_per_step": round(ms, 5), "GB_s": round(st.bytes / ms / 1e6, 1), "launches": len(st.plan),
+           "weight_GB": round(weight_bytes(st.plan) / 1e9, 3),
+           "how": "%d bm_f16_matvec_act calls (rounding fused), CUDA graph, PDL on" % len(st.plan)}
+    if variants:
+        g_u = capture(torch, stream, lambda: st.run(stream, "unfused"))
+        ms_u = replay_time(torch, stream, g_u, steps, 5)
+        unfused_bytes = step_bytes(st.plan, False)
+        res["unfused"] = {"ms_per_step": round(ms_u, 5), "GB_s": round(unfused_bytes / ms_u / 1e6, 1),
+                          "launches": 2 * len(st.plan),
+                          "how": "bm_to_f16 then bm_f16_matvec[_multi] / bm_f16_logits per product"}
+        g_n = capture(torch, stream, lambda: st.run(stream, "norm"))
+        ms_n = replay_time(torch, stream, g_n, steps, 5)
+        nb = st.bytes + 4 * MODELS[model]["hidden"] * sum(1 for op in st.plan if op[0] != "mv")
+        res["norm_front_end"] = {"ms_per_step": round(ms_n, 5), "GB_s": round(nb / ms_n / 1e6, 1),
+                                 "how": "the RMS norm ahead of Q/K/V, gate/up and the head fused into those "
+                                        "launches (bm_f16_matvec_norm)"}
+        prepared = bm.prepare(lambda: st.run(stream))
+        ms_e, h2d, d2h = e2e_time(torch, stream, st, prepared, max(3, min(steps, 30)))
+        res["e2e"] = {"GB_s": round(st.bytes / ms_e / 1e6, 1), "ms_per_step": round(ms_e, 5),
+                      "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                      "how": "recorded calls replayed one C call each; activations in, logits out, host waits"}
+        del g_u, g_n
+    del g, st
+    torch.cuda.empty_cache()
+    return res
 
 
 # ----------------------------------------------------------------------------- GPU arm
@@ -195,163 +392,51 @@ def run_gpu(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     bm.lib()
-    plan = step_plan()
-    tot_bytes, unfused_bytes = step_bytes(plan, True), step_bytes(plan, False)
-
-    # ---- weights and activations (seeded, generated on the host once, then resident)
-    weights = {}
-    for op in plan:
-        if op[0] == "round":
-            continue
-        for name, rows in op[1]:
-            w = synth.normal_f16(SEED, "smollm2." + name, W_SIGMA, (rows, op[2]))
-            weights[name] = torch.from_numpy(w.view(np.float16)).to(dev)
-    sizes = act_sizes(plan)
-    offs, o = {}, 0
-    for a in sorted(sizes):
-        offs[a] = o
-        o += (sizes[a] + 7) // 8 * 8  # 32-byte aligned slices
-    act_host = np.zeros(o, dtype=np.float32)
-    for a in sorted(sizes):
-        act_host[offs[a]:offs[a] + sizes[a]] = synth.normal_f32(SEED, "smollm2.act%d" % a, A_SIGMA, sizes[a])
-    act_f32 = torch.from_numpy(act_host).to(dev)
-    act_f16 = torch.empty(o, dtype=torch.float16, device=dev)
-    outs = {}
-    for op in plan:
-        if op[0] != "round":
-            for name, rows in op[1]:
-                outs[name] = torch.empty(rows, dtype=torch.float32, device=dev)
-
     stream = torch.cuda.Stream(device=dev)
     # The weights are constants: programmatic dependent launch lets each product start
     # copying its weights while the kernel ahead of it is still running.
     bm.bm_set_pdl(not args.no_pdl)
 
-    norm_w = {k: torch.from_numpy((1.0 + synth.normal_f32(SEED, "smollm2.norm%d" % k, 0.2, k))
-                                  .astype(np.float32)).to(dev) for k in (HIDDEN,)}
-
-    def run_step(s, fused=True, norm=False):
-        for op in plan:
-            if op[0] == "round":
-                if not fused:
-                    a = op[2]
-                    bm.bm_to_f16(act_f32[offs[a]:offs[a] + op[1]], act_f16[offs[a]:offs[a] + op[1]], stream=s)
-                continue
-            kind, mats, k, a = op
-            if norm and kind in ("multi", "logits"):
-                # the norm ahead of Q/K/V, of gate/up and of the logits, fused into the product
-                bm.bm_f16_matvec_norm([weights[n] for n, _ in mats], act_f32[offs[a]:offs[a] + k], norm_w[k], 1e-5,
-                                      [outs[n] for n, _ in mats], stream=s)
-                continue
-            if fused:
-                bm.bm_f16_matvec_act([weights[n] for n, _ in mats], act_f32[offs[a]:offs[a] + k],
-                                     [outs[n] for n, _ in mats], stream=s)
-                continue
-            x = act_f16[offs[a]:offs[a] + k]
-            if kind == "multi":
-                bm.bm_f16_matvec_multi([weights[n] for n, _ in mats], x, [outs[n] for n, _ in mats], stream=s)
-            elif kind == "mv":
-                bm.bm_f16_matvec(weights[mats[0][0]], x, outs[mats[0][0]], stream=s)
-            else:
-                bm.bm_f16_logits(weights[mats[0][0]], x.view(1, -1), outs[mats[0][0]].view(1, -1), stream=s)
-
-    launches_per_step = sum(1 for op in plan if op[0] != "round")
-
-    def capture(fused, norm=False):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(stream):
-            run_step(stream, fused, norm)  # warm (attribute setup happens outside capture)
-        torch.cuda.synchronize()
-        with torch.cuda.graph(g, stream=stream):
-            run_step(stream, fused, norm)
-        torch.cuda.synchronize()
-        return g
-
-    g_step = capture(True)
-    g_unfused = capture(False)
-    g_norm = capture(True, True)
-
-    def timed(g, steps, warmup):
-        for _ in range(warmup):
-            g.replay()
-        torch.cuda.synchronize()
-        if world > 1:
-            torch.distributed.barrier()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            e0.record(stream)
-            for _ in range(steps):
-                g.replay()
-            e1.record(stream)
-        torch.cuda.synchronize()
-        if world > 1:
-            torch.distributed.barrier()
-        return e0.elapsed_time(e1) / steps  # ms per step
+    step = DecodeStep(bm, torch, dev, HEADLINE, args.decode_layers)
+    g_step = capture(torch, stream, lambda: step.run(stream))
 
     clocks = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ else
                           int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local_rank]))
     clocks.start()
     time.sleep(0.3)
     t_begin = time.time()
-    ms = timed(g_step, args.steps, args.warmup)
+    ms = replay_time(torch, stream, g_step, args.steps, args.warmup, world)
     t_end = time.time()
-    ms_unfused = timed(g_unfused, max(args.steps, 20), args.warmup)
-    ms_norm = timed(g_norm, max(args.steps, 20), args.warmup)
+    time.sleep(0.1)
     clk = clocks.summary(t_begin, t_end)
     clocks.stop()
-
     if world > 1:
         t = torch.tensor([ms], device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         ms = float(t.item())
 
-    # ---- end to end through the binding: pinned H2D of the step's activations, eager
-    # calls, D2H of the logits, every step
-    act_pinned = torch.from_numpy(act_host).pin_memory()
-    logits_host = torch.empty(VOCAB, dtype=torch.float32).pin_memory()
-    e2e_steps = max(3, min(args.steps, 50))
+    # ---- end to end through the binding: the step's 129 calls recorded once by prepare()
+    # (arguments checked and marshalled once), then every step: activations in from pinned
+    # host memory, one C call per product, logits out, the host waits for them
+    e2e_steps = max(3, min(args.steps, 30))
+    prepared = bm.prepare(lambda: step.run(stream))
+    ms_e2e, h2d, d2h = e2e_time(torch, stream, step, prepared, e2e_steps)
+    pg = prepared.graph(stream)
+    ms_e2e_graph, _, _ = e2e_time(torch, stream, step, pg, e2e_steps)
+    ms_e2e_eager, _, _ = e2e_time(torch, stream, step, lambda: step.run(stream), e2e_steps)
+    del pg, prepared, g_step
 
-    # the step's 121 calls recorded once through the binding's prepare(): each replay is
-    # one C call per product (the same entry points, pointers and stream)
-    prepared = bm.prepare(lambda: run_step(stream))
-
-    def e2e_step(calls):
-        with torch.cuda.stream(stream):
-            act_f32.copy_(act_pinned, non_blocking=True)
-            calls()
-            logits_host.copy_(outs["token_embd"], non_blocking=True)
-
-    def e2e_time(calls):
-        for _ in range(2):
-            e2e_step(calls)
-        torch.cuda.synchronize()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(e2e_steps):
-            e2e_step(calls)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        return e0.elapsed_time(e1) / e2e_steps
-
-    prepared_graph = prepared.graph(stream)
-    ms_e2e = e2e_time(prepared_graph)
-    ms_e2e_replay = e2e_time(prepared)
-    ms_e2e_eager = e2e_time(lambda: run_step(stream))
-
-    result = {
-        "ms": ms, "ms_unfused": ms_unfused, "ms_norm": ms_norm, "ms_e2e": ms_e2e, "ms_e2e_replay": ms_e2e_replay,
-        "ms_e2e_eager": ms_e2e_eager, "tot_bytes": tot_bytes,
-        "unfused_bytes": unfused_bytes, "launches_per_step": launches_per_step, "clocks": clk,
-        "h2d": int(act_host.nbytes), "d2h": int(VOCAB * 4),
-    }
+    result = {"ms": ms, "ms_e2e": ms_e2e, "ms_e2e_graph": ms_e2e_graph, "ms_e2e_eager": ms_e2e_eager,
+              "tot_bytes": step.bytes, "weight_bytes": weight_bytes(step.plan), "launches_per_step": len(step.plan),
+              "plan": step.plan, "clocks": clk, "h2d": h2d, "d2h": d2h}
+    del step
+    torch.cuda.empty_cache()
     if rank == 0 and not args.no_products:
-        result["products"] = bench_products(bm, dev, stream, torch)
-        result["llama3_8b_decode_step"] = bench_llama_decode(bm, dev, stream, torch)
-        result["llama3_8b_prefill_layer"] = bench_llama_prefill(bm, dev, stream, torch)
-        result["qwen3_0.6b_decode_step"] = bench_qwen3_decode(bm, dev, stream, torch)
+        result["prefill"] = bench_llama_prefill(bm, dev, stream, torch)
+        result["smollm2_135m_decode_step"] = decode_side(bm, torch, dev, stream, "smollm2_135m")
+        result["qwen3_0.6b_decode_step"] = decode_side(bm, torch, dev, stream, "qwen3_0.6b", variants=False)
         result["qwen3_0.6b_prefill_layer"] = bench_qwen3_prefill(bm, dev, stream, torch)
+        result["products"] = bench_products(bm, dev, stream, torch)
         result["helpers"] = bench_helpers(bm, dev, stream, torch)
     return result
 
@@ -359,13 +444,7 @@ def run_gpu(args, rank, world, local_rank):
 def graph_time(torch, stream, fn, reps=3, pre=None):
     """Capture fn() once as a CUDA graph; median ms of `reps` replays (pre() runs
     before each replay, outside the timed events)."""
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(stream):
-        fn()
-    torch.cuda.synchronize()
-    with torch.cuda.graph(g, stream=stream):
-        fn()
-    torch.cuda.synchronize()
+    g = capture(torch, stream, fn)
     ts = []
     for _ in range(reps):
         with torch.cuda.stream(stream):
@@ -379,6 +458,148 @@ def graph_time(torch, stream, fn, reps=3, pre=None):
         torch.cuda.synchronize()
         ts.append(e0.elapsed_time(e1))
     return float(np.median(ts))
+
+
+class PrefillLayer:
+    """One Llama-3-8B-shaped layer's products for a prefill micro-batch of `n` tokens,
+    resident on the GPU: Q/K/V/O (4096, 1024, 1024, 4096 rows x 4096), gate and up
+    (14336 x 4096) and down (4096 x 14336), weights N(0, 0.01); the normed activations
+    x (f32 [n][4096]) and the FFN activation xf (f32 [n][14336], a synthetic stand-in for
+    the SwiGLU output) N(0, 1), each rounded to f16 by bm_to_f16 inside the step.  7
+    tensor-core products and 2 rounding kernels per step (plus a reduction after each
+    product that splits k).  The layer's 436 MB of weights exceed L2, so replays stream
+    them from HBM."""
+
+    HID, FFN, KV = 4096, 14336, 1024
+    SHAPES = [("q", 4096, 4096), ("k", 1024, 4096), ("v", 1024, 4096), ("o", 4096, 4096), ("gate", 14336, 4096),
+              ("up", 14336, 4096), ("down", 4096, 14336)]
+
+    def __init__(self, bm, torch, dev, n=512, keep_host=False):
+        self.bm, self.torch, self.n = bm, torch, n
+        self.host = {}
+        self.W = {}
+        for nm, r, c in self.SHAPES:
+            w = synth.normal_f16(SEED, "llama3_8b." + nm, 0.01, (r, c))
+            self.W[nm] = torch.from_numpy(w.view(np.float16)).to(dev)
+            if keep_host:
+                self.host[nm] = w
+        xh = synth.normal_f32(SEED, "llama3_8b.prefill_x", 1.0, (n, self.HID))
+        fh = synth.normal_f32(SEED, "llama3_8b.prefill_ffn", 1.0, (n, self.FFN))
+        if keep_host:
+            self.host["x"], self.host["xf"] = xh, fh
+        self.x = torch.from_numpy(xh).to(dev)
+        self.xf = torch.from_numpy(fh).to(dev)
+        self.h = torch.empty((n, self.HID), dtype=torch.float16, device=dev)
+        self.hd = torch.empty((n, self.FFN), dtype=torch.float16, device=dev)
+        self.Y = {nm: torch.empty((n, r), dtype=torch.float32, device=dev) for nm, r, _ in self.SHAPES}
+        self.flops = 2.0 * n * sum(r * c for _, r, c in self.SHAPES)
+        self._cat = None
+
+    def run(self, s, variant="multi"):
+        """variant 'separate': 7 bm_f16_matmul calls; 'multi': Q/K/V and gate/up each one
+        bm_f16_matmul_multi launch (the separate matrices share the activation); 'concat':
+        Q/K/V and gate/up stored as one matrix each ([6144][4096] and [28672][4096]), whose
+        outputs a caller reads as row ranges of each column."""
+        bm, W, Y = self.bm, self.W, self.Y
+        bm.bm_to_f16(self.x, self.h, stream=s)
+        if variant == "separate":
+            for nm in ("q", "k", "v", "o", "gate", "up"):
+                bm.bm_f16_matmul(W[nm], self.h, Y=Y[nm], stream=s)
+        elif variant == "multi":
+            bm.bm_f16_matmul_multi([W["q"], W["k"], W["v"]], self.h, [Y["q"], Y["k"], Y["v"]], stream=s)
+            bm.bm_f16_matmul(W["o"], self.h, Y=Y["o"], stream=s)
+            bm.bm_f16_matmul_multi([W["gate"], W["up"]], self.h, [Y["gate"], Y["up"]], stream=s)
+        else:
+            if self._cat is None:
+                t = self.torch
+                Wqkv = t.cat([W["q"], W["k"], W["v"]], 0)
+                Wgu = t.cat([W["gate"], W["up"]], 0)
+                self._cat = (Wqkv, Wgu, t.empty((self.n, Wqkv.shape[0]), dtype=t.float32, device=Wqkv.device),
+                             t.empty((self.n, Wgu.shape[0]), dtype=t.float32, device=Wqkv.device))
+            Wqkv, Wgu, Yqkv, Ygu = self._cat
+            bm.bm_f16_matmul(Wqkv, self.h, Y=Yqkv, stream=s)
+            bm.bm_f16_matmul(W["o"], self.h, Y=Y["o"], stream=s)
+            bm.bm_f16_matmul(Wgu, self.h, Y=Ygu, stream=s)
+        bm.bm_to_f16(self.xf, self.hd, stream=s)
+        bm.bm_f16_matmul(W["down"], self.hd, Y=Y["down"], stream=s)
+
+
+def bench_llama_prefill(bm, dev, stream, torch, reps=10):
+    """The prefill half of the metric: PrefillLayer at 512 tokens as one CUDA graph, with
+    Q/K/V and gate/up through bm_f16_matmul_multi and programmatic dependent launch (the
+    `value`), and the other variants beside it."""
+    layer = PrefillLayer(bm, torch, dev)
+    old = bm.bm_set_pdl(True)
+    try:
+        ms = graph_time(torch, stream, lambda: layer.run(stream, "multi"), reps=reps)
+        ms_sep = graph_time(torch, stream, lambda: layer.run(stream, "separate"), reps=reps)
+        ms_cat = graph_time(torch, stream, lambda: layer.run(stream, "concat"), reps=reps)
+        bm.bm_set_pdl(False)
+        ms_plain = graph_time(torch, stream, lambda: layer.run(stream, "multi"), reps=reps)
+    finally:
+        bm.bm_set_pdl(old)
+    tf = lambda t: round(layer.flops / t / 1e9, 1)  # noqa: E731
+    res = {"workload": "llama3_8b_prefill_layer", "tokens": layer.n, "ms_per_step": round(ms, 4),
+           "TFLOP_s": tf(ms), "flop_per_step": layer.flops,
+           "how": "one layer's 7 products at 512 columns (Q/K/V and gate/up through bm_f16_matmul_multi) plus 2 "
+                  "rounding kernels, CUDA graph, PDL on; median of %d replays, weights (436 MB) larger than L2" % reps,
+           "separate": {"ms_per_step": round(ms_sep, 4), "TFLOP_s": tf(ms_sep),
+                        "how": "7 bm_f16_matmul calls, PDL on"},
+           "concatenated_weights": {"ms_per_step": round(ms_cat, 4), "TFLOP_s": tf(ms_cat),
+                                    "how": "Q/K/V and gate/up each stored as one matrix: 4 products, PDL on"},
+           "without_pdl": {"ms_per_step": round(ms_plain, 4), "TFLOP_s": tf(ms_plain)}}
+    # the products one by one (each a graph of one call after an L2 flush by a read)
+    flush_buf = torch.ones(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    sink = torch.zeros((), dtype=torch.float32, device=dev)
+    per = []
+    for nm, r, c in PrefillLayer.SHAPES:
+        X = layer.hd if nm == "down" else layer.h
+        t = graph_time(torch, stream, lambda: bm.bm_f16_matmul(layer.W[nm], X, Y=layer.Y[nm], stream=stream),
+                       reps=5, pre=lambda: sink.copy_(flush_buf.sum()))
+        per.append({"product": nm, "rows": r, "k": c, "us": round(t * 1e3, 2),
+                    "TFLOP_s": round(2.0 * r * c * layer.n / t / 1e9, 1), "plan": bm.bm_tc_plan(r, c, layer.n)})
+    res["products"] = per
+    del layer, flush_buf
+    torch.cuda.empty_cache()
+    return res
+
+
+def bench_qwen3_prefill(bm, dev, stream, torch, reps=10):
+    """A Qwen3-0.6B-shaped prefill micro-batch of 512 tokens through one layer's products,
+    with Q/K/V and gate/up stored as one matrix each ([4096][1024] and [6144][1024]), then
+    O (1024 x 2048) and down (1024 x 3072), plus the two roundings: one CUDA graph, PDL on.
+    One layer's weights (31 MB) sit in L2, so this measures the tensor path with hot weights."""
+    hid, q, kv, ffn, n = 1024, 2048, 1024, 3072, 512
+    Wqkv = torch.from_numpy(synth.normal_f16(SEED, "qwen3.qkv", 0.02, (q + 2 * kv, hid)).view(np.float16)).to(dev)
+    Wo = torch.from_numpy(synth.normal_f16(SEED, "qwen3.o", 0.02, (hid, q)).view(np.float16)).to(dev)
+    Wgu = torch.from_numpy(synth.normal_f16(SEED, "qwen3.gu", 0.02, (2 * ffn, hid)).view(np.float16)).to(dev)
+    Wd = torch.from_numpy(synth.normal_f16(SEED, "qwen3.down", 0.02, (hid, ffn)).view(np.float16)).to(dev)
+    x = torch.from_numpy(synth.normal_f32(SEED, "qwen3.prefill_x", 1.0, (n, hid))).to(dev)
+    xo = torch.from_numpy(synth.normal_f16(SEED, "qwen3.prefill_o", 1.0, (n, q)).view(np.float16)).to(dev)
+    xf = torch.from_numpy(synth.normal_f32(SEED, "qwen3.prefill_f", 1.0, (n, ffn))).to(dev)
+    h = torch.empty((n, hid), dtype=torch.float16, device=dev)
+    hf = torch.empty((n, ffn), dtype=torch.float16, device=dev)
+    Yqkv = torch.empty((n, q + 2 * kv), dtype=torch.float32, device=dev)
+    Yo = torch.empty((n, hid), dtype=torch.float32, device=dev)
+    Ygu = torch.empty((n, 2 * ffn), dtype=torch.float32, device=dev)
+    Yd = torch.empty((n, hid), dtype=torch.float32, device=dev)
+    flops = 2.0 * n * hid * (q + 2 * kv + q + 2 * ffn + ffn)
+
+    def step():
+        bm.bm_to_f16(x, h, stream=stream)
+        bm.bm_f16_matmul(Wqkv, h, Y=Yqkv, stream=stream)
+        bm.bm_f16_matmul(Wo, xo, Y=Yo, stream=stream)
+        bm.bm_f16_matmul(Wgu, h, Y=Ygu, stream=stream)
+        bm.bm_to_f16(xf, hf, stream=stream)
+        bm.bm_f16_matmul(Wd, hf, Y=Yd, stream=stream)
+
+    old = bm.bm_set_pdl(True)
+    try:
+        ms = graph_time(torch, stream, step, reps=reps)
+    finally:
+        bm.bm_set_pdl(old)
+    return {"tokens": n, "ms_per_step": round(ms, 4), "TFLOP_s": round(flops / ms / 1e9, 1),
+            "how": "one layer: Q/K/V and gate/up as one matrix each, O, down, 2 roundings; CUDA graph, PDL on"}
 
 
 def bench_products(bm, dev, stream, torch):
@@ -445,101 +666,39 @@ def bench_products(bm, dev, stream, torch):
         out.append({"product": name, "rows": rows, "k": k, "ncols": 512, "ms": round(ms, 5),
                     "TFLOP_s": round(tf, 1), "GB_s": round(algorithmic_bytes(rows, k, 512) / ms / 1e6, 1)})
         del W, x, y, Y, reps
+    out.extend(bench_fallback(bm, dev, stream, torch))
     return out
 
 
-def bench_llama_decode(bm, dev, stream, torch, steps=10):
-    """A Llama-3-8B-shaped decode step: 32 layers of [fused Q/K/V (4096+1024+1024 x
-    4096), O (4096 x 4096), fused gate/up (2 x 14336 x 4096), down (4096 x 14336)]
-    then the output product (128256 x 4096): 129 bm_f16_matvec_act calls over 15 GB
-    of f16 weights N(0, 0.01).  One layer's weights are drawn and copied to all 32
-    layers (distinct memory: every product still streams from HBM)."""
-    hid, ffn, kv, vocab, layers = 4096, 14336, 1024, 128256, 32
-    base = {n: torch.from_numpy(synth.normal_f16(SEED, "llama3_8b." + n, 0.01, (r, c)).view(np.float16)).to(dev)
-            for n, r, c in [("q", hid, hid), ("k", kv, hid), ("v", kv, hid), ("o", hid, hid), ("gate", ffn, hid),
-                            ("up", ffn, hid), ("down", hid, ffn)]}
-    lw = [{n: (t if L == 0 else t.clone()) for n, t in base.items()} for L in range(layers)]
-    out_w = torch.from_numpy(synth.normal_f16(SEED, "llama3_8b.output", 0.01, (vocab, hid)).view(np.float16)).to(dev)
-    xa = torch.from_numpy(synth.normal_f32(SEED, "llama3_8b.act", 1.0, hid)).to(dev)
-    xf = torch.from_numpy(synth.normal_f32(SEED, "llama3_8b.act_ffn", 1.0, ffn)).to(dev)
-    ys = {n: torch.empty(t.shape[0], dtype=torch.float32, device=dev) for n, t in base.items()}
-    logits = torch.empty(vocab, dtype=torch.float32, device=dev)
-    nbytes = 0
-    for n, t in base.items():
-        nbytes += layers * (2 * t.numel() + 4 * t.shape[0])
-    nbytes += layers * 4 * (hid + hid + hid + ffn) + 2 * vocab * hid + 4 * vocab + 4 * hid
+def bench_fallback(bm, dev, stream, torch):
+    """The exact vec_dot kernels off the tinyBLAS path: shapes that fail takes_sgemm
+    (13 rows, k % 8 != 0) at 512 columns, and one-column rows of k % 8 != 0 (not
+    16-byte aligned, so the lane-per-chain kernel with 2-byte loads), each a graph of
+    back-to-back launches cycling through weight replicas larger than twice the L2
+    where the weights are large; GB/s of algorithmic bytes against the HBM peak."""
+    out = []
+    for name, rows, k, nc in (("fallback.13x1536", 13, 1536, 512), ("fallback.4096x33", 4096, 33, 512),
+                              ("fallback.12x4097", 12, 4097, 512), ("unaligned.14336x4097", 14336, 4097, 1),
+                              ("unaligned.4096x14335", 4096, 14335, 1)):
+        W = torch.from_numpy(synth.normal_f16(SEED, name, 0.02, (rows, k)).view(np.float16)).to(dev)
+        X = torch.from_numpy(synth.normal_f16(SEED, name + ".x", 1.0, (nc, k)).view(np.float16)).to(dev)
+        Y = torch.empty((nc, rows), dtype=torch.float32, device=dev)
+        nrep = max(1, min(16, -(-2 * 129 * 2 ** 20 // (2 * rows * k))))
+        reps = [W] + [W.clone() for _ in range(nrep - 1)]
+        launches = max(8, 2 * nrep)
 
-    def step():
-        for L in range(layers):
-            w = lw[L]
-            bm.bm_f16_matvec_act([w["q"], w["k"], w["v"]], xa, [ys["q"], ys["k"], ys["v"]], stream=stream)
-            bm.bm_f16_matvec_act([w["o"]], xa, [ys["o"]], stream=stream)
-            bm.bm_f16_matvec_act([w["gate"], w["up"]], xa, [ys["gate"], ys["up"]], stream=stream)
-            bm.bm_f16_matvec_act([w["down"]], xf, [ys["down"]], stream=stream)
-        bm.bm_f16_matvec_act([out_w], xa, [logits], stream=stream)
+        def chain():
+            for i in range(launches):
+                bm.bm_f16_matmul(reps[i % nrep], X, Y, stream=stream)
 
-    norms = [torch.from_numpy((1.0 + synth.normal_f32(SEED, "llama3_8b.norm%d" % i, 0.2, hid)).astype(np.float32))
-             .to(dev) for i in range(2 * layers + 1)]
-
-    def step_norm():
-        # the same step with the RMS norm ahead of Q/K/V, gate/up and the output product
-        # fused into those launches (each reads its norm weight, 4 * 4096 bytes, too)
-        for L in range(layers):
-            w = lw[L]
-            bm.bm_f16_matvec_norm([w["q"], w["k"], w["v"]], xa, norms[2 * L], 1e-5, [ys["q"], ys["k"], ys["v"]],
-                                  stream=stream)
-            bm.bm_f16_matvec_act([w["o"]], xa, [ys["o"]], stream=stream)
-            bm.bm_f16_matvec_norm([w["gate"], w["up"]], xa, norms[2 * L + 1], 1e-5, [ys["gate"], ys["up"]],
-                                  stream=stream)
-            bm.bm_f16_matvec_act([w["down"]], xf, [ys["down"]], stream=stream)
-        bm.bm_f16_matvec_norm([out_w], xa, norms[-1], 1e-5, [logits], stream=stream)
-
-    ms = graph_time(torch, stream, step, reps=steps)
-    ms_norm = graph_time(torch, stream, step_norm, reps=steps)
-    res = {"ms_per_step": round(ms, 4), "GB_s": round(nbytes / ms / 1e6, 1), "weight_GB": round(
-        (sum(t.numel() for t in base.values()) * layers + out_w.numel()) * 2 / 1e9, 3), "launches": 4 * layers + 1,
-        "with_norm_front_end": {"ms_per_step": round(ms_norm, 4),
-                                "GB_s": round((nbytes + 4 * hid * (2 * layers + 1)) / ms_norm / 1e6, 1),
-                                "how": "bm_f16_matvec_norm for Q/K/V, gate/up and the output product"}}
-    del lw, out_w, base, norms
-    return res
-
-
-def bench_qwen3_decode(bm, dev, stream, torch, steps=10):
-    """A Qwen3-0.6B-shaped decode step: 28 layers of [fused Q/K/V (2048+1024+1024 x 1024),
-    O (1024 x 2048), fused gate/up (2 x 3072 x 1024), down (1024 x 3072)] then the tied
-    logits (151936 x 1024): 113 bm_f16_matvec_act calls over 1.19 GB of f16 weights
-    N(0, 0.02), one layer drawn and copied to 28 distinct buffers."""
-    hid, q, kv, ffn, vocab, layers = 1024, 2048, 1024, 3072, 151936, 28
-    base = {n: torch.from_numpy(synth.normal_f16(SEED, "qwen3." + n, 0.02, (r, c)).view(np.float16)).to(dev)
-            for n, r, c in [("q", q, hid), ("k", kv, hid), ("v", kv, hid), ("o", hid, q), ("gate", ffn, hid),
-                            ("up", ffn, hid), ("down", hid, ffn)]}
-    lw = [{n: (t if L == 0 else t.clone()) for n, t in base.items()} for L in range(layers)]
-    emb = torch.from_numpy(synth.normal_f16(SEED, "qwen3.embd", 0.02, (vocab, hid)).view(np.float16)).to(dev)
-    xa = torch.from_numpy(synth.normal_f32(SEED, "qwen3.act", 1.0, hid)).to(dev)
-    xo = torch.from_numpy(synth.normal_f32(SEED, "qwen3.act_o", 1.0, q)).to(dev)
-    xf = torch.from_numpy(synth.normal_f32(SEED, "qwen3.act_ffn", 1.0, ffn)).to(dev)
-    ys = {n: torch.empty(t.shape[0], dtype=torch.float32, device=dev) for n, t in base.items()}
-    logits = torch.empty(vocab, dtype=torch.float32, device=dev)
-    nbytes = 0
-    for n, t in base.items():
-        nbytes += layers * (2 * t.numel() + 4 * t.shape[0])
-    nbytes += layers * 4 * (hid + q + hid + ffn) + 2 * vocab * hid + 4 * vocab + 4 * hid
-
-    def step():
-        for L in range(layers):
-            w = lw[L]
-            bm.bm_f16_matvec_act([w["q"], w["k"], w["v"]], xa, [ys["q"], ys["k"], ys["v"]], stream=stream)
-            bm.bm_f16_matvec_act([w["o"]], xo, [ys["o"]], stream=stream)
-            bm.bm_f16_matvec_act([w["gate"], w["up"]], xa, [ys["gate"], ys["up"]], stream=stream)
-            bm.bm_f16_matvec_act([w["down"]], xf, [ys["down"]], stream=stream)
-        bm.bm_f16_matvec_act([emb], xa, [logits], stream=stream)
-
-    ms = graph_time(torch, stream, step, reps=steps)
-    res = {"ms_per_step": round(ms, 4), "GB_s": round(nbytes / ms / 1e6, 1), "weight_GB": round(
-        (sum(t.numel() for t in base.values()) * layers + emb.numel()) * 2 / 1e9, 3), "launches": 4 * layers + 1}
-    del lw, emb, base
-    return res
+        ms = graph_time(torch, stream, chain) / launches
+        out.append({"product": name, "rows": rows, "k": k, "ncols": nc, "ms": round(ms, 5),
+                    "GB_s": round(algorithmic_bytes(rows, k, nc) / ms / 1e6, 1),
+                    "TFLOP_s": round(2.0 * rows * k * nc / ms / 1e9, 3),
+                    "path": "vec_dot bit-exact (lane per chain)",
+                    "how": "%d back-to-back launches over %d weight replicas, PDL" % (launches, nrep)})
+        del W, X, Y, reps
+    return out
 
 
 def bench_helpers(bm, dev, stream, torch, launches=8):
@@ -578,144 +737,42 @@ def bench_helpers(bm, dev, stream, torch, launches=8):
     return out
 
 
-def bench_qwen3_prefill(bm, dev, stream, torch, reps=10):
-    """A Qwen3-0.6B-shaped prefill micro-batch of 512 tokens through one layer's products,
-    with Q/K/V and gate/up stored as one matrix each ([4096][1024] and [6144][1024]), then
-    O (1024 x 2048) and down (1024 x 3072), plus the two roundings: one CUDA graph, PDL on.
-    One layer's weights (31 MB) sit in L2, so this measures the tensor path with hot weights."""
-    hid, q, kv, ffn, n = 1024, 2048, 1024, 3072, 512
-    Wqkv = torch.from_numpy(synth.normal_f16(SEED, "qwen3.qkv", 0.02, (q + 2 * kv, hid)).view(np.float16)).to(dev)
-    Wo = torch.from_numpy(synth.normal_f16(SEED, "qwen3.o", 0.02, (hid, q)).view(np.float16)).to(dev)
-    Wgu = torch.from_numpy(synth.normal_f16(SEED, "qwen3.gu", 0.02, (2 * ffn, hid)).view(np.float16)).to(dev)
-    Wd = torch.from_numpy(synth.normal_f16(SEED, "qwen3.down", 0.02, (hid, ffn)).view(np.float16)).to(dev)
-    x = torch.from_numpy(synth.normal_f32(SEED, "qwen3.prefill_x", 1.0, (n, hid))).to(dev)
-    xo = torch.from_numpy(synth.normal_f16(SEED, "qwen3.prefill_o", 1.0, (n, q)).view(np.float16)).to(dev)
-    xf = torch.from_numpy(synth.normal_f32(SEED, "qwen3.prefill_f", 1.0, (n, ffn))).to(dev)
-    h = torch.empty((n, hid), dtype=torch.float16, device=dev)
-    hf = torch.empty((n, ffn), dtype=torch.float16, device=dev)
-    Yqkv = torch.empty((n, q + 2 * kv), dtype=torch.float32, device=dev)
-    Yo = torch.empty((n, hid), dtype=torch.float32, device=dev)
-    Ygu = torch.empty((n, 2 * ffn), dtype=torch.float32, device=dev)
-    Yd = torch.empty((n, hid), dtype=torch.float32, device=dev)
-    flops = 2.0 * n * hid * (q + 2 * kv + q + 2 * ffn + ffn)
-
-    def step():
-        bm.bm_to_f16(x, h, stream=stream)
-        bm.bm_f16_matmul(Wqkv, h, Y=Yqkv, stream=stream)
-        bm.bm_f16_matmul(Wo, xo, Y=Yo, stream=stream)
-        bm.bm_f16_matmul(Wgu, h, Y=Ygu, stream=stream)
-        bm.bm_to_f16(xf, hf, stream=stream)
-        bm.bm_f16_matmul(Wd, hf, Y=Yd, stream=stream)
-
-    old = bm.bm_set_pdl(True)
-    try:
-        ms = graph_time(torch, stream, step, reps=reps)
-    finally:
-        bm.bm_set_pdl(old)
-    return {"tokens": n, "ms_per_step": round(ms, 4), "TFLOP_s": round(flops / ms / 1e9, 1),
-            "how": "one layer: Q/K/V and gate/up as one matrix each, O, down, 2 roundings; CUDA graph, PDL on"}
-
-
-def bench_llama_prefill(bm, dev, stream, torch, reps=10):
-    """A Llama-3-8B-shaped prefill micro-batch of 512 tokens through one layer's products:
-    the rounding of the normed activations, Q/K/V/O (4096, 1024, 1024, 4096 rows x 4096),
-    gate and up (14336 x 4096), the rounding of the FFN activation and down (4096 x 14336):
-    7 tensor-core products and 2 rounding kernels per step (plus a reduction after each
-    product that splits k), one CUDA graph, with and without programmatic dependent launch.
-    The layer's 436 MB of weights exceed L2, so replays stream them from HBM."""
-    hid, ffn, kv, n = 4096, 14336, 1024, 512
-    shapes = [("q", hid, hid), ("k", kv, hid), ("v", kv, hid), ("o", hid, hid), ("gate", ffn, hid),
-              ("up", ffn, hid), ("down", hid, ffn)]
-    W = {nm: torch.from_numpy(synth.normal_f16(SEED, "llama3_8b." + nm, 0.01, (r, c)).view(np.float16)).to(dev)
-         for nm, r, c in shapes}
-    x = torch.from_numpy(synth.normal_f32(SEED, "llama3_8b.prefill_x", 1.0, (n, hid))).to(dev)
-    h = torch.empty((n, hid), dtype=torch.float16, device=dev)
-    Y = {nm: torch.empty((n, r), dtype=torch.float32, device=dev) for nm, r, _ in shapes}
-    hd = torch.empty((n, ffn), dtype=torch.float16, device=dev)
-    flops = 2.0 * n * sum(r * c for _, r, c in shapes)
-
-    def step():
-        bm.bm_to_f16(x, h, stream=stream)
-        for nm in ("q", "k", "v", "o", "gate", "up"):
-            bm.bm_f16_matmul(W[nm], h, Y=Y[nm], stream=stream)
-        bm.bm_to_f16(Y["gate"], hd, stream=stream)
-        bm.bm_f16_matmul(W["down"], hd, Y=Y["down"], stream=stream)
-
-    # The same layer with Q/K/V and gate/up stored as one matrix each ([6144][4096] and
-    # [28672][4096]): two products instead of five.  Every element is still its own row's
-    # product (the path follows the concatenated shape, which takes_sgemm the same way),
-    # and a caller reads Q, K, V (or gate, up) as row ranges of each output column.
-    Wqkv = torch.cat([W["q"], W["k"], W["v"]], 0)
-    Wgu = torch.cat([W["gate"], W["up"]], 0)
-    Yqkv = torch.empty((n, Wqkv.shape[0]), dtype=torch.float32, device=dev)
-    Ygu = torch.empty((n, Wgu.shape[0]), dtype=torch.float32, device=dev)
-
-    def step_fused():
-        bm.bm_to_f16(x, h, stream=stream)
-        bm.bm_f16_matmul(Wqkv, h, Y=Yqkv, stream=stream)
-        bm.bm_f16_matmul(W["o"], h, Y=Y["o"], stream=stream)
-        bm.bm_f16_matmul(Wgu, h, Y=Ygu, stream=stream)
-        bm.bm_to_f16(Y["gate"], hd, stream=stream)  # stand-in FFN activation, same shape as in step()
-        bm.bm_f16_matmul(W["down"], hd, Y=Y["down"], stream=stream)
-
-    def step_multi():
-        # the same with the separate matrices: bm_f16_matmul_multi shares one launch
-        bm.bm_to_f16(x, h, stream=stream)
-        bm.bm_f16_matmul_multi([W["q"], W["k"], W["v"]], h, [Y["q"], Y["k"], Y["v"]], stream=stream)
-        bm.bm_f16_matmul(W["o"], h, Y=Y["o"], stream=stream)
-        bm.bm_f16_matmul_multi([W["gate"], W["up"]], h, [Y["gate"], Y["up"]], stream=stream)
-        bm.bm_to_f16(Y["gate"], hd, stream=stream)
-        bm.bm_f16_matmul(W["down"], hd, Y=Y["down"], stream=stream)
-
-    old = bm.bm_set_pdl(False)
-    try:
-        ms_plain = graph_time(torch, stream, step, reps=reps)
-        bm.bm_set_pdl(True)
-        ms_pdl = graph_time(torch, stream, step, reps=reps)
-        ms_fused = graph_time(torch, stream, step_fused, reps=reps)
-        ms_multi = graph_time(torch, stream, step_multi, reps=reps)
-    finally:
-        bm.bm_set_pdl(old)
-    res = {"tokens": n, "ms_per_step": round(ms_pdl, 4), "TFLOP_s": round(flops / ms_pdl / 1e9, 1),
-           "ms_per_step_without_pdl": round(ms_plain, 4), "TFLOP_s_without_pdl": round(flops / ms_plain / 1e9, 1),
-           "how": "one layer's 7 products at 512 columns plus 2 rounding kernels, CUDA graph, PDL on / off",
-           "concatenated_weights": {"ms_per_step": round(ms_fused, 4), "TFLOP_s": round(flops / ms_fused / 1e9, 1),
-                                    "how": "Q/K/V and gate/up each stored as one matrix: 4 products, PDL on"},
-           "multi": {"ms_per_step": round(ms_multi, 4), "TFLOP_s": round(flops / ms_multi / 1e9, 1),
-                     "how": "separate matrices, Q/K/V and gate/up through bm_f16_matmul_multi, PDL on"}}
-    del W, Y, Wqkv, Wgu, Yqkv, Ygu
-    return res
-
-
 # ----------------------------------------------------------------------------- CPU oracle
 
 
-def oracle_step_runner():
-    """The decode step on the CPU oracle: returns (run_one_step, bytes_per_step)."""
+def oracle_sample_runner(model=HEADLINE):
+    """A bounded sample of the decode step on the CPU oracle: one layer's four calls (every
+    layer has the same shapes) and 1/L of the head's rows, with the step's own weights and
+    activations.  Returns (run_one_sample, bytes_per_sample, threads, description)."""
     import oracle
 
-    plan = step_plan()
-    tot_bytes = step_bytes(plan, True)  # the same byte count the GPU arm's value uses
+    spec = MODELS[model]
+    L = spec["layers"]
+    plan = step_plan(model)
+    layer0 = plan[:4]
+    head = plan[-1]
+    hk, hrows = head[2], -(-head[1][0][2] // L)
     weights = {}
-    for op in plan:
-        if op[0] != "round":
-            for name, rows in op[1]:
-                weights[name] = synth.normal_f16(SEED, "smollm2." + name, W_SIGMA, (rows, op[2]))
-    acts = {a: synth.normal_f32(SEED, "smollm2.act%d" % a, A_SIGMA, n) for a, n in act_sizes(plan).items()}
+    for _, mats, k, _ in layer0:
+        for _, wn, rows in mats:
+            weights[wn] = synth.normal_f16(SEED, wn, spec["sigma"], (rows, k))
+    hw = synth.normal_f16(SEED, head[1][0][1], spec["sigma"], (hrows, hk))  # the head's first rows (counter-based)
+    acts = {a: synth.normal_f32(SEED, act_name(model, a), A_SIGMA, k) for _, _, k, a in layer0 + [head]}
+    nbytes = step_bytes(layer0, True) + 2 * hrows * hk + 4 * hrows + 4 * hk
 
     def run():
-        h = {}
-        for op in plan:
-            if op[0] == "round":
-                h[op[2]] = oracle.to_f16(acts[op[2]])
-            elif op[0] == "multi":
-                oracle.matvec_multi([weights[n] for n, _ in op[1]], h[op[3]])
-            elif op[0] == "mv":
-                oracle.matvec(weights[op[1][0][0]], h[op[3]])
+        for kind, mats, k, a in layer0:
+            h = oracle.to_f16(acts[a])
+            if kind == "multi":
+                oracle.matvec_multi([weights[wn] for _, wn, _ in mats], h)
             else:
-                oracle.matmul(weights[op[1][0][0]], h[op[3]][None, :])
+                oracle.matvec(weights[mats[0][1]], h)
+        oracle.matvec(hw, oracle.to_f16(acts[head[3]]))
 
-    return run, tot_bytes, oracle.threads()
+    desc = ("one layer's 4 calls (Q/K/V, O, gate/up, down; %.0f MB of f16 weights) and %d of the %d head rows "
+            "(1/%d) of the %s decode step, activations rounded by the oracle" %
+            (weight_bytes(layer0) / 1e6, hrows, head[1][0][2], L, model))
+    return run, nbytes, oracle.threads(), desc
 
 
 def host_cpu():
@@ -735,7 +792,7 @@ def host_cpu():
 
 def cpu_baseline(budget_s=10.0, budget_1core_s=4.0):
     import oracle
-    run, nbytes, cores = oracle_step_runner()
+    run, nbytes, cores, desc = oracle_sample_runner()
 
     def timed(budget):
         run()
@@ -774,29 +831,28 @@ def cpu_baseline(budget_s=10.0, budget_1core_s=4.0):
             entry["TFLOP_s"] = round(2.0 * rows * k * nc / full_s / 1e12, 5)
         products.append(entry)
     return {"value": round(nbytes * n / dt / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-            "sample": "%d full SmolLM2-135M decode steps (30 layers + logits, 269 MB of f16 weights each) "
-                      "in %.1f s on the host" % (n, dt),
+            "sample": "%d repetitions in %.1f s on the host of %s" % (n, dt, desc),
             "value_1core": round(nbytes * n1 / dt1 / 1e9, 4),
-            "sample_1core": "%d full steps in %.1f s on one core" % (n1, dt1), "host": host_cpu(),
+            "sample_1core": "%d repetitions in %.1f s on one core" % (n1, dt1), "host": host_cpu(),
             "products": products}
 
 
-def step_config(world, no_pdl):
-    """The workload description both arms print (the reference arm runs it on the host)."""
-    return {"workload": "smollm2_135m_decode_step", "layers": LAYERS, "hidden": HIDDEN, "ffn": FFN,
-            "q_rows": Q_ROWS, "kv_rows": KV_ROWS, "vocab": VOCAB, "ncols": 1, "seed": SEED,
-            "weight_bytes": int(sum(2 * rows * op[2] for op in step_plan() if op[0] != "round"
-                                    for _, rows in op[1])),
-            "l2": "inputs larger than L2 (269 MB of weights per step, cyclic)",
-            "parallelism": "replicas" if world > 1 else "single GPU", "graph": "CUDA graph of the step",
-            "pdl": not no_pdl}
+def step_config(model=HEADLINE, layers=None):
+    """The workload both arms measure (a description of the data, not of how it runs)."""
+    spec = MODELS[model]
+    plan = step_plan(model, layers)
+    return {"workload": "%s_decode_step" % model, "layers": spec["layers"] if layers is None else layers,
+            "hidden": spec["hidden"], "q_rows": spec["q"], "kv_rows": spec["kv"], "ffn": spec["ffn"],
+            "vocab": spec["vocab"], "ncols": 1, "calls_per_step": len(plan), "seed": SEED,
+            "weight_sigma": spec["sigma"], "activation_sigma": A_SIGMA, "weight_bytes": weight_bytes(plan),
+            "algorithmic_bytes_per_step": step_bytes(plan, True)}
 
 
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
-    run, nbytes, cores = oracle_step_runner()
+    run, nbytes, cores, desc = oracle_sample_runner()
     for _ in range(args.warmup):
         run()
     t0 = time.perf_counter()
@@ -805,21 +861,24 @@ def run_reference(args):
     dt = time.perf_counter() - t0
     ms = dt * 1e3 / args.steps
     value = nbytes / (ms / 1e3) / 1e9
+    cfg = step_config()
+    cfg.update({"runs_on": "host CPU cores (OpenMP over output rows)", "l2": None,
+                "step_sample": "each step is a bounded sample: " + desc})
     line = {
-        "impl": "reference", "metric": "decode F16 GEMV HBM GB/s (SmolLM2-135M decode step)",
+        "impl": "reference", "metric": "decode F16 GEMV HBM GB/s (Llama-3-8B-shaped decode step)",
         "value": round(value, 4), "unit": "GB/s", "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f16 weights, f32 accumulate", "data": "synthetic",
-        "config": step_config(1, False),
+        "dtype": "f16 weights and activations, f32 accumulate (vec_dot bits)", "data": "synthetic",
+        "config": cfg,
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-                         "sample": "%d full decode steps after %d warm-up" % (args.steps, args.warmup)},
+                         "sample": "%d steps after %d warm-up, each %s" % (args.steps, args.warmup, desc)},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
     return 0
 
 
-# ----------------------------------------------------------------------------- main
+# ----------------------------------------------------------------------------- profile modes
 
 
 def run_single(spec: str, reps: int):
@@ -832,7 +891,7 @@ def run_single(spec: str, reps: int):
     __graft_entry__.build()
     rows, k, ncols = (int(v) for v in spec.lower().split("x"))
     dev = torch.device("cuda", 0)
-    W = torch.from_numpy(synth.normal_f16(SEED, "single.w", W_SIGMA, (rows, k)).view(np.float16)).to(dev)
+    W = torch.from_numpy(synth.normal_f16(SEED, "single.w", 0.02, (rows, k)).view(np.float16)).to(dev)
     X = torch.from_numpy(synth.normal_f16(SEED, "single.x", A_SIGMA, (ncols, k)).view(np.float16)).to(dev)
     Y = torch.empty((ncols, rows), dtype=torch.float32, device=dev)
     for _ in range(reps):
@@ -842,6 +901,29 @@ def run_single(spec: str, reps: int):
             bm.bm_f16_matmul(W, X, Y)
     torch.cuda.synchronize()
     print(json.dumps({"single": spec, "reps": reps, "status": bm.bm_device_status()}))
+    return 0
+
+
+def run_decode(spec: str, reps: int):
+    """MODEL:LAYERS -- that decode step with LAYERS layers (and the head), eagerly, `reps`
+    times with programmatic dependent launch on (for profilers; prints nothing timed).
+    Each product's shape is the full step's, so its per-launch counters are too."""
+    import torch
+
+    import __graft_entry__
+    import f16_weight_gemv_gb300 as bm
+
+    __graft_entry__.build()
+    model, layers = spec.split(":")
+    dev = torch.device("cuda", 0)
+    bm.bm_set_pdl(True)
+    step = DecodeStep(bm, torch, dev, model, int(layers))
+    s = torch.cuda.current_stream()
+    for _ in range(reps):
+        step.run(s)
+    torch.cuda.synchronize()
+    print(json.dumps({"decode": spec, "launches_per_step": len(step.plan), "reps": reps,
+                      "keys": [call_key(m, k) for _, m, k, _ in step.plan], "status": bm.bm_device_status()}))
     return 0
 
 
@@ -867,12 +949,12 @@ def run_helper(name: str, reps: int):
         g = torch.rand(4096, device=dev, generator=gen) + 0.5
         y = torch.empty_like(x)
         h = torch.empty(512, 4096, dtype=torch.float16, device=dev)
-        call = lambda: bm.bm_rms_norm_mul(x, g, 1e-5, y, h)
+        call = lambda: bm.bm_rms_norm_mul(x, g, 1e-5, y, h)  # noqa: E731
     elif name == "get_rows":
         E = (torch.randn(128256, 4096, device=dev, generator=gen) * 0.01).to(torch.float16)
         ids = torch.randint(0, 128256, (512,), device=dev, dtype=torch.int32, generator=gen)
         out = torch.empty(512, 4096, dtype=torch.float32, device=dev)
-        call = lambda: bm.bm_f16_get_rows(E, ids, out)
+        call = lambda: bm.bm_f16_get_rows(E, ids, out)  # noqa: E731
     else:
         raise SystemExit("unknown helper " + name)
     for _ in range(reps):
@@ -883,8 +965,9 @@ def run_helper(name: str, reps: int):
 
 
 def run_prefill(reps: int):
-    """The Llama-3-8B-shaped prefill layer (bench_llama_prefill), eagerly, `reps` times with
-    programmatic dependent launch on (for profilers; prints nothing timed)."""
+    """The Llama-3-8B-shaped prefill layer (PrefillLayer, bm_f16_matmul_multi variant),
+    eagerly, `reps` times with programmatic dependent launch on (for profilers; prints
+    nothing timed)."""
     import torch
 
     import __graft_entry__
@@ -892,30 +975,23 @@ def run_prefill(reps: int):
 
     __graft_entry__.build()
     dev = torch.device("cuda", 0)
-    hid, ffn, kv, n = 4096, 14336, 1024, 512
-    shapes = [("q", hid, hid), ("k", kv, hid), ("v", kv, hid), ("o", hid, hid), ("gate", ffn, hid),
-              ("up", ffn, hid), ("down", hid, ffn)]
-    W = {nm: torch.from_numpy(synth.normal_f16(SEED, "llama3_8b." + nm, 0.01, (r, c)).view(np.float16)).to(dev)
-         for nm, r, c in shapes}
-    x = torch.from_numpy(synth.normal_f32(SEED, "llama3_8b.prefill_x", 1.0, (n, hid))).to(dev)
-    h = torch.empty((n, hid), dtype=torch.float16, device=dev)
-    Y = {nm: torch.empty((n, r), dtype=torch.float32, device=dev) for nm, r, _ in shapes}
-    hd = torch.empty((n, ffn), dtype=torch.float16, device=dev)
+    layer = PrefillLayer(bm, torch, dev)
     bm.bm_set_pdl(True)
+    s = torch.cuda.current_stream()
     for _ in range(reps):
-        bm.bm_to_f16(x, h)
-        for nm in ("q", "k", "v", "o", "gate", "up"):
-            bm.bm_f16_matmul(W[nm], h, Y=Y[nm])
-        bm.bm_to_f16(Y["gate"], hd)
-        bm.bm_f16_matmul(W["down"], hd, Y=Y["down"])
+        layer.run(s, "multi")
     torch.cuda.synchronize()
     print(json.dumps({"prefill": "llama3_8b layer, 512 tokens", "reps": reps, "status": bm.bm_device_status()}))
     return 0
 
 
+# ----------------------------------------------------------------------------- main
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--single", default=None, help="profile mode: run one product ROWSxKxNCOLS --reps times")
+    ap.add_argument("--decode", default=None, help="profile mode: run the decode step MODEL:LAYERS --reps times")
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--prefill", action="store_true", help="profile mode: run the Llama-3-8B prefill layer --reps times")
     ap.add_argument("--helper", default=None, choices=["mad", "scale", "norm", "get_rows"],
@@ -924,7 +1000,8 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--no-products", action="store_true")
+    ap.add_argument("--decode-layers", type=int, default=None, help=argparse.SUPPRESS)
+    ap.add_argument("--no-products", action="store_true", help="the headline objects only")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-pdl", action="store_true", help="launch without programmatic dependent launch")
     args = ap.parse_args()
@@ -934,6 +1011,8 @@ def main():
         return run_reference(args)
     if args.single:
         return run_single(args.single, args.reps)
+    if args.decode:
+        return run_decode(args.decode, args.reps)
     if args.prefill:
         return run_prefill(args.reps)
     if args.helper:
@@ -959,82 +1038,86 @@ def main():
     if rank != 0:
         return 0
 
-    gpu_name = torch.cuda.get_device_name()
     peaks = {}
     try:
         peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
     except (OSError, ValueError):
         pass
     hbm_peak = float(peaks.get("hbm_gbs", 6800.0))
-    peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
+    hbm_src = "measured (MEASURED_PEAKS.json hbm_gbs)" if "hbm_gbs" in peaks else "fallback 6.8 TB/s"
+    tc_peak = float(peaks.get("bf16_tflops", 1900.0))
+    tc_src = ("measured (MEASURED_PEAKS.json bf16_tflops, burst: the layer is timed alone); f16 and bf16 run at "
+              "the same dense rate" if "bf16_tflops" in peaks else "fallback 1.9 PFLOP/s")
     value = r["tot_bytes"] * world / (r["ms"] / 1e3) / 1e9
     achieved = r["tot_bytes"] / (r["ms"] / 1e3) / 1e9
+    layers = args.decode_layers
+    cfg = step_config(HEADLINE, layers)
+    cfg.update({"l2": "inputs larger than L2: %.1f GB of weights per step, read once per step" %
+                      (r["weight_bytes"] / 1e9),
+                "parallelism": "replicas" if world > 1 else "single GPU", "graph": "CUDA graph of the step",
+                "pdl": not args.no_pdl})
+    gb = lambda ms: round(r["tot_bytes"] / (ms / 1e3) / 1e9, 2)  # noqa: E731
     line = {
-        "metric": "decode F16 GEMV HBM GB/s (SmolLM2-135M decode step)",
+        "metric": "decode F16 GEMV HBM GB/s (Llama-3-8B-shaped decode step)",
         "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(r["ms"], 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f16 weights and activations, f32 accumulate (vec_dot bits)", "data": "synthetic",
-        "config": step_config(world, args.no_pdl),
+        "config": cfg,
         "pct_of_hbm_peak": round(100.0 * value / world / hbm_peak, 2),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
-                     "frac": round(achieved / hbm_peak, 4), "traffic": ncu_traffic(),
+                     "frac": round(achieved / hbm_peak, 4), "traffic": ncu_traffic_per_launch(r["plan"]),
                      "traffic_unit": "bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)",
                      "algorithmic_bytes_per_launch": int(r["tot_bytes"] / r["launches_per_step"]),
-                     "kernel": "k_gemv_stream (rounding + one-column GEMV)", "peak_source": peak_src,
+                     "kernel": "k_gemv_stream (rounding + one-column GEMV)", "peak_source": hbm_src,
                      "launches_per_step": r["launches_per_step"],
                      "how": "the step's only kernel: algorithmic bytes of its launches / CUDA-event time of the "
-                            "step graph on the launch stream"},
-        "unfused": {"ms_per_step": round(r["ms_unfused"], 5),
-                    "value": round(r["unfused_bytes"] / (r["ms_unfused"] / 1e3) / 1e9, 2),
-                    "launches_per_step": 2 * r["launches_per_step"],
-                    "how": "bm_to_f16 then bm_f16_matvec[_multi] / bm_f16_logits per product"},
-        "norm_front_end": {"ms_per_step": round(r["ms_norm"], 5),
-                           "value": round((r["tot_bytes"] + 4 * HIDDEN * (2 * LAYERS + 1)) / (r["ms_norm"] / 1e3) / 1e9,
-                                          2),
-                           "how": "the step with the RMS norm (rms_norm then mul) ahead of Q/K/V, gate/up and the "
-                                  "logits fused into those launches (bm_f16_matvec_norm)"},
+                            "step graph's replays on the launch stream"},
         "gpu_launches": r["launches_per_step"] * args.steps,
         "clocks": r["clocks"],
-        "e2e": {"value": round(r["tot_bytes"] / (r["ms_e2e"] / 1e3) / 1e9, 2), "unit": "GB/s",
-                "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
-                "how": "the step's calls through the Python binding, recorded once with prepare(), captured "
-                       "with Prepared.graph() and launched every step; pinned host activations in, logits out, "
-                       "every step",
-                "replay_value": round(r["tot_bytes"] / (r["ms_e2e_replay"] / 1e3) / 1e9, 2),
-                "replay_how": "the same recorded calls replayed one C call per product (no graph)",
-                "eager_value": round(r["tot_bytes"] / (r["ms_e2e_eager"] / 1e3) / 1e9, 2),
+        "e2e": {"value": gb(r["ms_e2e"]), "unit": "GB/s", "h2d_bytes_per_step": r["h2d"],
+                "d2h_bytes_per_step": r["d2h"], "ms_per_step": round(r["ms_e2e"], 5),
+                "how": "every step: the step's f32 activations copied from pinned host memory, the 129 calls "
+                       "recorded once by the binding's prepare() made one C call each, the logits copied back to "
+                       "pinned host memory and waited for on the host; wall clock",
+                "graph_value": gb(r["ms_e2e_graph"]),
+                "graph_how": "the same with the recorded calls captured once as a CUDA graph (Prepared.graph())",
+                "eager_value": gb(r["ms_e2e_eager"]),
                 "eager_how": "the same with every call made through the wrappers (argument checks each time)"},
-        "device": gpu_name,
+        "device": torch.cuda.get_device_name(),
     }
-    if "llama3_8b_decode_step" in r:
-        r["llama3_8b_decode_step"]["pct_hbm"] = round(100.0 * r["llama3_8b_decode_step"]["GB_s"] / hbm_peak, 1)
-        line["llama3_8b_decode_step"] = r["llama3_8b_decode_step"]
-    if "qwen3_0.6b_decode_step" in r:
-        r["qwen3_0.6b_decode_step"]["pct_hbm"] = round(100.0 * r["qwen3_0.6b_decode_step"]["GB_s"] / hbm_peak, 1)
-        line["qwen3_0.6b_decode_step"] = r["qwen3_0.6b_decode_step"]
+    if "prefill" in r:
+        pf = r["prefill"]
+        line["prefill"] = {
+            "metric": "prefill GEMM TFLOP/s (% of dense FP16 peak)", "value": pf["TFLOP_s"], "unit": "TFLOP/s",
+            "pct_of_peak": round(100.0 * pf["TFLOP_s"] / tc_peak, 1),
+            "roofline": {"bound": "tensor", "achieved": pf["TFLOP_s"], "peak": tc_peak, "unit": "TFLOP/s",
+                         "frac": round(pf["TFLOP_s"] / tc_peak, 4), "traffic": None,
+                         "kernel": "k_gemm_tc (tcgen05 + TMA + TMEM)", "peak_source": tc_src,
+                         "how": "the layer's algorithmic flops / CUDA-event time of the whole layer graph, which also "
+                                "holds the two rounding kernels and the split-k reductions: a lower bound on the "
+                                "tensor-core kernel's own rate"},
+            **pf}
+        for p in pf["products"]:
+            p["pct_of_peak"] = round(100.0 * p["TFLOP_s"] / tc_peak, 1)
+    for key in ("smollm2_135m_decode_step", "qwen3_0.6b_decode_step"):
+        if key in r:
+            r[key]["pct_hbm"] = round(100.0 * r[key]["GB_s"] / hbm_peak, 1)
+            line[key] = r[key]
+    if "qwen3_0.6b_prefill_layer" in r:
+        pq = r["qwen3_0.6b_prefill_layer"]
+        pq["pct_bf16_dense_peak"] = round(100.0 * pq["TFLOP_s"] / tc_peak, 1)
+        line["qwen3_0.6b_prefill_layer"] = pq
     if "helpers" in r:
         for p in r["helpers"]:
             p["pct_hbm"] = round(100.0 * p["GB_s"] / hbm_peak, 1)
         line["helpers"] = r["helpers"]
-    if "qwen3_0.6b_prefill_layer" in r:
-        pq = r["qwen3_0.6b_prefill_layer"]
-        pq["pct_bf16_dense_peak"] = round(100.0 * pq["TFLOP_s"] / float(peaks.get("bf16_tflops", 1900.0)), 1)
-        line["qwen3_0.6b_prefill_layer"] = pq
-    if "llama3_8b_prefill_layer" in r:
-        pf = r["llama3_8b_prefill_layer"]
-        pk = float(peaks.get("bf16_tflops", 1900.0))
-        pf["pct_bf16_dense_peak"] = round(100.0 * pf["TFLOP_s"] / pk, 1)
-        for key in ("multi", "concatenated_weights"):
-            if key in pf:
-                pf[key]["pct_bf16_dense_peak"] = round(100.0 * pf[key]["TFLOP_s"] / pk, 1)
-        line["llama3_8b_prefill_layer"] = pf
     if "products" in r:
         line["products"] = r["products"]
         for p in r["products"]:
-            if p["ncols"] <= 64:
+            if p["ncols"] <= 64 or "path" in p and "vec_dot" in p["path"]:
                 p["pct_hbm"] = round(100.0 * p["GB_s"] / hbm_peak, 1)
             else:
-                p["pct_bf16_dense_peak"] = round(100.0 * p["TFLOP_s"] / float(peaks.get("bf16_tflops", 1900.0)), 1)
+                p["pct_bf16_dense_peak"] = round(100.0 * p["TFLOP_s"] / tc_peak, 1)
     if not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline()
     print(json.dumps(line), flush=True)
