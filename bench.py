@@ -120,7 +120,24 @@ def algorithmic_bytes(rows, k, ncols=1):
 # measured on (sha256 prefix of k_gemv_stream.cu).  Shapes per launch do not depend on
 # the number of layers, so the full step's traffic is these, summed over its launches.
 NCU_TRAFFIC = {"kernel": "k_gemv_stream", "source": "f16_weight_gemv_gb300/csrc/k_gemv_stream.cu",
-               "sha256_16": None, "bytes_per_call": {}}
+               "sha256_16": "78fefbba59017a3a",
+               "bytes_per_call": {"4096x4096+1024x4096+1024x4096": 50418048, "4096x4096": 33640064,
+                                  "14336x4096+14336x4096": 235057536, "4096x14336": 117673728,
+                                  "128256x4096": 1051344896}}
+
+
+# DRAM traffic of the prefill layer's four k_gemm_tc launches (Q/K/V, O, gate/up, down; read +
+# write bytes), from the ncu launch list in profiles/prefill_layer_llama3_8b_launches.md, valid
+# only for the kernel source it was measured on.
+PREFILL_TRAFFIC = {"kernel": "k_gemm_tc", "source": "f16_weight_gemv_gb300/csrc/k_gemm_tc.cu",
+                   "sha256_16": "ada03cc1911f3a90", "bytes_per_launch": [54724096, 37835264, 281087744, 132340480]}
+
+
+def prefill_traffic_per_launch():
+    t = PREFILL_TRAFFIC
+    if not t["sha256_16"] or _source_sha16(t["source"]) != t["sha256_16"]:
+        return None
+    return int(round(sum(t["bytes_per_launch"]) / len(t["bytes_per_launch"])))
 
 
 def _source_sha16(rel):
@@ -1091,7 +1108,12 @@ def main():
             "metric": "prefill GEMM TFLOP/s (% of dense FP16 peak)", "value": pf["TFLOP_s"], "unit": "TFLOP/s",
             "pct_of_peak": round(100.0 * pf["TFLOP_s"] / tc_peak, 1),
             "roofline": {"bound": "tensor", "achieved": pf["TFLOP_s"], "peak": tc_peak, "unit": "TFLOP/s",
-                         "frac": round(pf["TFLOP_s"] / tc_peak, 4), "traffic": None,
+                         "frac": round(pf["TFLOP_s"] / tc_peak, 4), "traffic": prefill_traffic_per_launch(),
+                         "traffic_unit": "bytes per k_gemm_tc launch of the layer (ncu dram__bytes_read.sum + "
+                                         "dram__bytes_write.sum, mean of its 4 launches)",
+                         "algorithmic_bytes_per_launch": int(round(sum(
+                             2 * r * k + 2 * k * 512 + 4 * r * 512 for r, k in
+                             ((6144, 4096), (4096, 4096), (28672, 4096), (4096, 14336))) / 4)),
                          "kernel": "k_gemm_tc (tcgen05 + TMA + TMEM)", "peak_source": tc_src,
                          "how": "the layer's algorithmic flops / CUDA-event time of the whole layer graph, which also "
                                 "holds the two rounding kernels and the split-k reductions: a lower bound on the "
