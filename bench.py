@@ -712,7 +712,7 @@ def bench_fallback(bm, dev, stream, torch):
         out.append({"product": name, "rows": rows, "k": k, "ncols": nc, "ms": round(ms, 5),
                     "GB_s": round(algorithmic_bytes(rows, k, nc) / ms / 1e6, 1),
                     "TFLOP_s": round(2.0 * rows * k * nc / ms / 1e9, 3),
-                    "path": "vec_dot bit-exact (lane per chain)",
+                    "path": "vec_dot bit-exact (lane per chain)" if nc > 1 else "vec_dot bit-exact (bulk-copied aligned windows)",
                     "how": "%d back-to-back launches over %d weight replicas, PDL" % (launches, nrep)})
         del W, X, Y, reps
     return out

@@ -60,6 +60,9 @@ struct ActNorm {
 // non-null, receives the rounded activation.
 int launch_gemv_stream(const VecdotJob &job, const float *x_f32, uint16_t *h_out, cudaStream_t s,
                        const DeviceInfo &dev, const ActNorm *nrm = nullptr);
+// One column, rows not 16-byte aligned (k % 8 != 0): each row's k-slices streamed by
+// 1-D bulk copies of their 16-byte-aligned windows (job.X 16-byte aligned).
+int launch_gemv_bulk(const VecdotJob &job, cudaStream_t s, const DeviceInfo &dev);
 // rms_norm then mul of nrows rows of k values (out and/or h; out may equal x).
 int launch_rms_norm(const float *x, const float *g, int64_t nrows, int64_t k, float eps, float *out, uint16_t *h,
                     cudaStream_t s, const DeviceInfo &dev);

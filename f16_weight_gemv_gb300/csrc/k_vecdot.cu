@@ -12,11 +12,12 @@
 // give identical bits.  No split of a chain is ever made; the thread layout
 // decides only who computes a chain, never its order.
 //
-// This file holds the lane-per-chain kernel, used for rows whose k % 8 != 0 (not
-// 16-byte aligned, so not TMA-able) and for the multi-column vec_dot fallback:
+// This file holds the lane-per-chain kernel of the multi-column vec_dot fallback:
 // lane c of a warp owns chain c (element 32s + c) for a tile of R rows x C
-// columns, with 2-byte loads; the reduction is five warp shuffles per output.
-// One-column products with k % 8 == 0 go to k_gemv_stream.cu.
+// columns, with 2-byte loads; the reduction is five warp shuffles per output, and
+// lane q*R + i stores output (row i, column q), so a warp's stores are runs of
+// consecutive rows.  One-column products go to k_gemv_stream.cu (k % 8 == 0) and
+// k_gemv_bulk.cu (rows not 16-byte aligned).
 #include "../../include/bm.h"
 #include "bm_internal.h"
 
@@ -135,10 +136,10 @@ __global__ void __launch_bounds__(kThreads) k_vecdot_lanes(const __grid_constant
             v += __shfl_xor_sync(kFull, v, 1);
             v += __shfl_xor_sync(kFull, v, 2);
             v = __shfl_sync(kFull, v, 0);
-            if (lane == i * C + q) mine = v;
+            if (lane == q * R + i) mine = v;
         }
     if (lane < R * C) {
-        const int i = lane / C, q = lane % C;
+        const int i = lane % R, q = lane / R;
         const int64_t r = r0 + i, c = c0 + q;
         if (r < rows && c < ncols) {
             const float out = add_tail(mine, job.W[m] + r * k, job.X + c * k, nsteps << 5, k);
@@ -181,7 +182,7 @@ int launch_vecdot_1col(const VecdotJob &job_in, cudaStream_t s, const DeviceInfo
 {
     VecdotJob job = job_in;
     job.ncols = 1;
-    if (job.k % 8 != 0) return launch_lanes<8, 1>(job, s);
+    if (job.k % 8 != 0) return launch_gemv_bulk(job, s, dev);
     return launch_gemv_stream(job, nullptr, nullptr, s, dev);
 }
 

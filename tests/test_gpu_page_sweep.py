@@ -75,3 +75,18 @@ def test_tinyblas_bits_on_every_k_multiple_of_8(bm, rows):
     bits (f16.md, Design notes, "sgemm_dot") at every k % 8 == 0 from 8 to 1536."""
     n_exact, n_bound = sweep(bm, rows, range(8, 1537, 8), 8)
     assert n_bound == 0 and n_exact > 0
+
+
+def test_unaligned_rows_every_small_shape(bm):
+    """One column, rows not 16-byte aligned (k % 8 != 0): every row count 1..16 and every
+    such k from 9 to 100, so every offset of a row from its 16-byte boundary and the
+    matrix's last, clamped window occur; vec_dot's bits (f16.md, Design notes, "vec_dot")."""
+    import torch
+    for rows in range(1, 17):
+        for k in (k for k in range(9, 101) if k % 8):
+            W = synth.normal_f16(0, "unaligned.w.%d.%d" % (rows, k), 0.02, (rows, k))
+            x = oracle.to_f16(synth.normal_f32(0, "unaligned.x.%d" % k, 1.0, k))
+            y = torch.full((rows,), float("nan"), dtype=torch.float32, device="cuda")
+            bm.bm_f16_matvec(to_dev(W), to_dev(x), y)
+            assert np.array_equal(y.cpu().numpy().view(np.uint32), oracle.matvec(W, x).view(np.uint32)), (rows, k)
+    assert bm.bm_device_status() == 0
