@@ -305,6 +305,12 @@ class DecodeStep:
                 else:
                     bm.bm_f16_logits(W[0], h.view(1, -1), Y[0].view(1, -1), stream=s)
 
+    def record(self):
+        """The step's calls recorded as one launch (bm_step_create): the same products, in
+        the same order, with the same bits as run()."""
+        return self.bm.bm_step_create([([self.weights[key] for key, _, _ in mats], self.activation(a),
+                                        [self.outs[key] for key, _, _ in mats]) for _, mats, _, a in self.plan])
+
     def head(self):
         return self.outs["head"]
 
@@ -365,15 +371,40 @@ def e2e_time(torch, stream, step, calls, steps):
     return (time.perf_counter() - t0) * 1e3 / steps, int(step.act_host.nbytes), int(head_host.numel() * 4)
 
 
+def one_launch_time(torch, stream, st, steps, warmup=3):
+    """ms per run of the step recorded as one launch (bm_step_create / bm_step_run):
+    CUDA events on the launching stream around `steps` runs."""
+    step = st.record()
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            step.run(stream)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(steps):
+            step.run(stream)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    step.close()
+    return e0.elapsed_time(e1) / steps
+
+
 def decode_side(bm, torch, dev, stream, model, steps=20, variants=True):
     """A smaller decode step as a side measurement: the fused step (as the headline),
-    and optionally its unfused and norm-fused variants and its end-to-end time."""
+    the same calls recorded as one launch, and optionally its unfused and norm-fused
+    variants and its end-to-end time."""
     st = DecodeStep(bm, torch, dev, model)
     g = capture(torch, stream, lambda: st.run(stream))
     ms = replay_time(torch, stream, g, steps, 5)
+    ms1 = one_launch_time(torch, stream, st, steps)
     res = {"ms_per_step": round(ms, 5), "GB_s": round(st.bytes / ms / 1e6, 1), "launches": len(st.plan),
            "weight_GB": round(weight_bytes(st.plan) / 1e9, 3),
-           "how": "%d bm_f16_matvec_act calls (rounding fused), CUDA graph, PDL on" % len(st.plan)}
+           "how": "%d bm_f16_matvec_act calls (rounding fused), CUDA graph, PDL on" % len(st.plan),
+           "one_launch": {"ms_per_step": round(ms1, 5), "GB_s": round(st.bytes / ms1 / 1e6, 1),
+                          "how": "the same calls recorded once (bm_step_create) and run as one cooperative launch "
+                                 "(bm_step_run), each call waiting on the device for every earlier call"}}
     if variants:
         g_u = capture(torch, stream, lambda: st.run(stream, "unfused"))
         ms_u = replay_time(torch, stream, g_u, steps, 5)
@@ -442,8 +473,9 @@ def run_gpu(args, rank, world, local_rank):
     ms_e2e_graph, _, _ = e2e_time(torch, stream, step, pg, e2e_steps)
     ms_e2e_eager, _, _ = e2e_time(torch, stream, step, lambda: step.run(stream), e2e_steps)
     del pg, prepared, g_step
+    ms_one = one_launch_time(torch, stream, step, max(3, min(args.steps, 20)))
 
-    result = {"ms": ms, "ms_e2e": ms_e2e, "ms_e2e_graph": ms_e2e_graph, "ms_e2e_eager": ms_e2e_eager,
+    result = {"ms": ms, "ms_e2e": ms_e2e, "ms_e2e_graph": ms_e2e_graph, "ms_e2e_eager": ms_e2e_eager, "ms_one": ms_one,
               "tot_bytes": step.bytes, "weight_bytes": weight_bytes(step.plan), "launches_per_step": len(step.plan),
               "plan": step.plan, "clocks": clk, "h2d": h2d, "d2h": d2h}
     del step
@@ -1100,6 +1132,9 @@ def main():
                 "graph_how": "the same with the recorded calls captured once as a CUDA graph (Prepared.graph())",
                 "eager_value": gb(r["ms_e2e_eager"]),
                 "eager_how": "the same with every call made through the wrappers (argument checks each time)"},
+        "one_launch": {"ms_per_step": round(r["ms_one"], 5), "GB_s": gb(r["ms_one"]),
+                       "how": "the same 129 calls recorded once (bm_step_create) and run as one cooperative launch "
+                              "(bm_step_run), each call waiting on the device for every earlier call; CUDA events"},
         "device": torch.cuda.get_device_name(),
     }
     if "prefill" in r:

@@ -20,12 +20,21 @@ from . import _build
 __all__ = [
     "BmError", "lib", "bm_to_f16", "bm_f16_matvec", "bm_f16_matvec_multi", "bm_f16_matvec_act", "bm_f16_matvec_norm", "bm_rms_norm_mul", "bm_f16_matmul", "bm_f16_matmul_multi", "bm_f16_matmul_noalloc",
     "bm_f16_logits", "bm_f16_get_rows", "bm_f16_mad", "bm_f16_scale", "bm_takes_sgemm", "bm_device_status", "bm_status_string", "bm_last_error",
-    "bm_selftest_wait_timeout", "bm_set_pdl", "prepare", "Prepared", "PreparedGraph", "bm_set_exact_sgemm_cols", "bm_set_stream_k", "bm_tc_plan", "EXPORTS",
+    "bm_selftest_wait_timeout", "bm_set_pdl", "prepare", "Prepared", "PreparedGraph", "bm_set_exact_sgemm_cols", "bm_set_stream_k", "bm_tc_plan", "bm_step_create", "bm_step_run", "bm_step_destroy", "Step",
+    "MatvecCall", "EXPORTS",
     "BM_MAX_K",
 ]
 
 BM_OK, BM_ERR_INVALID_ARG, BM_ERR_ALIGNMENT, BM_ERR_UNSUPPORTED_DEVICE, BM_ERR_CUDA, BM_ERR_TIMEOUT = range(6)
 BM_MAX_K = 65536
+
+
+
+class MatvecCall(C.Structure):
+    """bm_matvec_call of include/bm.h."""
+    _fields_ = [("nmat", C.c_int), ("W", C.c_void_p * 4), ("rows", C.c_int64 * 4), ("k", C.c_int64),
+                ("x", C.c_void_p), ("y", C.c_void_p * 4)]
+
 
 # Every symbol include/bm.h declares, with (restype, argtypes).
 _vp, _i64, _i = C.c_void_p, C.c_int64, C.c_int
@@ -47,6 +56,9 @@ EXPORTS = {
     "bm_takes_sgemm": (_i, [_i64, _i64, _i64]),
     "bm_device_status": (_i, [_vp]),
     "bm_tc_plan": (_i, [_i64, _i64, _i64, _i, C.POINTER(_i64)]),
+    "bm_step_create": (_i, [C.POINTER(MatvecCall), _i, C.POINTER(_vp)]),
+    "bm_step_run": (_i, [_vp, _vp]),
+    "bm_step_destroy": (_i, [_vp]),
     "bm_set_pdl": (_i, [_i]),
     "bm_set_exact_sgemm_cols": (_i, [_i]),
     "bm_set_stream_k": (_i, [_i]),
@@ -274,6 +286,68 @@ def bm_f16_matvec_act(Ws, x: torch.Tensor, ys=None, h: torch.Tensor | None = Non
     hp = _dev(h, "h", _F16_LIKE) if h is not None else None
     _call("bm_f16_matvec_act", n, wp, rows, k, _dev(x, "x", (torch.float32,)), hp, yp, _stream(stream))
     return ys
+
+
+class Step:
+    """A recorded decode step (bm_step_create): run() launches all its calls at once.
+    Holds the tensors the calls point into; close() (or garbage collection) frees it."""
+
+    def __init__(self, handle, tensors):
+        self._h = handle
+        self._tensors = tuple(tensors)
+
+    def run(self, stream=None):
+        if not self._h:
+            raise ValueError("the step is closed")
+        _check(lib().bm_step_run(self._h, _stream(stream)), "bm_step_run")
+
+    __call__ = run
+
+    def close(self):
+        if self._h:
+            lib().bm_step_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def bm_step_create(calls) -> Step:
+    """Records a decode step: `calls` is a list of (Ws, x, ys) as for bm_f16_matvec_act
+    (f32 activation x, up to four f16 matrices Ws sharing it, their f32 outputs ys)."""
+    arr = (MatvecCall * max(len(calls), 1))()
+    keep = []
+    for i, (Ws, x, ys) in enumerate(calls):
+        if len(Ws) != len(ys) or not 1 <= len(Ws) <= 4:
+            raise ValueError("call %d: one output per matrix, 1..4 matrices" % i)
+        k = x.numel()
+        c = arr[i]
+        c.nmat = len(Ws)
+        c.k = k
+        c.x = _dev(x, "x", (torch.float32,))
+        keep.append(x)
+        for m, (W, y) in enumerate(zip(Ws, ys)):
+            r, kk = _wk(W)
+            if kk != k or y.numel() != r:
+                raise ValueError("call %d: shape mismatch" % i)
+            c.W[m] = _dev(W, "W", _F16_LIKE)
+            c.rows[m] = r
+            c.y[m] = _dev(y, "y", (torch.float32,))
+            keep += [W, y]
+    h = C.c_void_p()
+    _check(lib().bm_step_create(arr, len(calls), C.byref(h)), "bm_step_create")
+    return Step(h.value, keep)
+
+
+def bm_step_run(step: Step, stream=None):
+    step.run(stream)
+
+
+def bm_step_destroy(step: Step):
+    step.close()
 
 
 def bm_f16_matvec_norm(Ws, x: torch.Tensor, g: torch.Tensor, eps: float, ys=None, n_out=None,

@@ -371,6 +371,73 @@ int bm_f16_matvec_norm(int nmat, const uint16_t *const *W, const int64_t *rows, 
     return act_products("bm_f16_matvec_norm", nmat, W, rows, k, x, &nrm, h, y, stream);
 }
 
+int bm_step_create(const bm_matvec_call *calls, int ncalls, bm_step **step)
+{
+    clear_error();
+    if (!step) return fail(BM_ERR_INVALID_ARG, "bm_step_create: null step");
+    *step = nullptr;
+    if (!calls || ncalls < 1 || ncalls > 65535)
+        return fail(BM_ERR_INVALID_ARG, "bm_step_create: ncalls = %d outside 1..65535 (or null calls)", ncalls);
+    for (int i = 0; i < ncalls; i++) {
+        const bm_matvec_call &c = calls[i];
+        if (c.nmat < 1 || c.nmat > 4)
+            return fail(BM_ERR_INVALID_ARG, "bm_step_create: call %d: nmat = %d outside 1..4", i, c.nmat);
+        if (c.k < 8 || c.k > BM_MAX_K || c.k % 8 != 0)
+            return fail(BM_ERR_INVALID_ARG, "bm_step_create: call %d: k = %lld (need 8 <= k <= %d, k %% 8 == 0)", i,
+                        (long long)c.k, BM_MAX_K);
+        if (!c.x) return fail(BM_ERR_INVALID_ARG, "bm_step_create: call %d: null activation", i);
+        if (!aligned(c.x, 16)) return fail(BM_ERR_ALIGNMENT, "bm_step_create: call %d: x must be 16-byte aligned", i);
+        for (int m = 0; m < c.nmat; m++) {
+            if (c.rows[m] > 0x7fffffffLL)
+                return fail(BM_ERR_INVALID_ARG, "bm_step_create: call %d: rows must be below 2^31", i);
+            int st = check_matrix_args("bm_step_create", c.W[m], c.rows[m], c.k,
+                                       reinterpret_cast<const uint16_t *>(c.x), 1, c.y[m]);
+            if (st != BM_OK) return st;
+            if (c.rows[m] == 0) continue;
+            if (overlap(c.y[m], c.rows[m] * 4, c.x, c.k * 4))
+                return fail(BM_ERR_INVALID_ARG, "bm_step_create: call %d: output %d overlaps the activation", i, m);
+            for (int q = 0; q < m; q++)
+                if (c.rows[q] > 0 && (overlap(c.y[m], c.rows[m] * 4, c.y[q], c.rows[q] * 4) ||
+                                      overlap(c.y[m], c.rows[m] * 4, c.W[q], c.rows[q] * c.k * 2) ||
+                                      overlap(c.y[q], c.rows[q] * 4, c.W[m], c.rows[m] * c.k * 2)))
+                    return fail(BM_ERR_INVALID_ARG, "bm_step_create: call %d: output %d overlaps an input or output",
+                                i, m);
+        }
+    }
+    // no call writes into any call's weights (the weights of later calls stream early)
+    for (int i = 0; i < ncalls; i++)
+        for (int m = 0; m < calls[i].nmat; m++) {
+            if (calls[i].rows[m] == 0) continue;
+            for (int j = 0; j < ncalls; j++)
+                for (int q = 0; q < calls[j].nmat; q++)
+                    if (calls[j].rows[q] > 0 && overlap(calls[i].y[m], calls[i].rows[m] * 4, calls[j].W[q],
+                                                        calls[j].rows[q] * calls[j].k * 2))
+                        return fail(BM_ERR_INVALID_ARG, "bm_step_create: call %d writes into call %d's weights", i, j);
+        }
+    int st;
+    DeviceInfo dev;
+    if (!current_device(&dev, &st)) return st;
+    void *h = nullptr;
+    st = step_create(calls, ncalls, dev, &h);
+    if (st != BM_OK) return st;
+    *step = static_cast<bm_step *>(h);
+    return BM_OK;
+}
+
+int bm_step_run(const bm_step *step, bm_stream_t stream)
+{
+    clear_error();
+    if (!step) return fail(BM_ERR_INVALID_ARG, "bm_step_run: null step");
+    return step_run(const_cast<bm_step *>(step), reinterpret_cast<cudaStream_t>(stream));
+}
+
+int bm_step_destroy(bm_step *step)
+{
+    clear_error();
+    step_destroy(step);
+    return BM_OK;
+}
+
 int bm_rms_norm_mul(const float *x, const float *g, int64_t nrows, int64_t k, float eps, float *out, uint16_t *h,
                     bm_stream_t stream)
 {

@@ -4,6 +4,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "../../include/bm.h"
+
 namespace bm {
 
 // Per-device facts read once.
@@ -97,6 +99,11 @@ int launch_gemm_tc_withheld(const uint16_t *W, int64_t rows, int64_t k, const ui
 // Rows of an f16 table widened to f32 (ids checked on the device).
 int launch_get_rows(const uint16_t *E, int64_t vocab, int64_t hidden, const int32_t *ids, int64_t n, float *out,
                     cudaStream_t s, const DeviceInfo &dev);
+// A recorded decode step (bm_step_create / bm_step_run / bm_step_destroy); the calls are
+// validated by the caller.
+int step_create(const bm_matvec_call *calls, int ncalls, const DeviceInfo &dev, void **out);
+int step_run(void *step, cudaStream_t s);
+void step_destroy(void *step);
 // Waits for `s` and reads/clears the device error word of the tensor-core kernels.
 int read_device_error(cudaStream_t s);
 

@@ -107,6 +107,50 @@ int bm_f16_matvec_act(int nmat, const uint16_t *const *W, const int64_t *rows, i
                       const float *x, uint16_t *h, float *const *y, bm_stream_t stream);
 
 /*
+ * A decode step's one-column products, recorded once and run as one launch (no
+ * counterpart on the pages, which run each product as its own pool pass: a
+ * schedule of this library for f16.md's one-column products).  Each call is
+ * bm_f16_matvec_act's -- the f32 activation x rounded to f16, then multiplied
+ * by up to four matrices sharing it, every output row ggml_vec_dot_f16 bit for
+ * bit -- and bm_step_run gives exactly the bits that making the calls in order
+ * with bm_f16_matvec_act gives.  A call may read what an earlier call of the
+ * step wrote: its activation is read only once every earlier call's outputs
+ * are written (the kernel waits, on the device, between calls).  What one
+ * launch buys: the weights of the next calls stream while a call finishes or
+ * waits, and no launch gaps.
+ *   calls[i].nmat 1..4; W[m] device f16[rows[m]][k], 16-byte aligned, rows[m] in
+ *   0 .. 2^31-1 (0: skipped); 8 <= k <= BM_MAX_K and k % 8 == 0 (rows are streamed
+ *   as 16-byte-aligned boxes; other k: bm_f16_matvec_act); x device f32[k],
+ *   16-byte aligned; y[m] device f32[rows[m]], 4-byte aligned.  Within a call no
+ *   output overlaps an input or another output; across calls outputs may be
+ *   later calls' activations (or be overwritten by later calls), never weights.
+ *   1 <= ncalls <= 65535.
+ * bm_step_create validates every call, encodes the weights' tensor maps and
+ * copies the call table to the current device (the step's only allocation, freed
+ * by bm_step_destroy), and synchronises the device once.  The pointers are kept:
+ * the same memory is read and written by every run, with whatever it holds then.
+ * bm_step_run launches the step on `stream` (asynchronous; one cooperative launch
+ * of two CTAs per SM, which must all be resident: BM_ERR_CUDA if the device
+ * cannot hold them).  Runs of one step must not overlap on the GPU (they share
+ * the step's device counter); runs of different steps may.  After a run whose
+ * bm_device_status is BM_ERR_TIMEOUT the step must be destroyed and recorded
+ * again.  bm_step_destroy frees the step (NULL is allowed); the step's device
+ * must still exist.
+ */
+typedef struct bm_matvec_call {
+    int nmat;
+    const uint16_t *W[4];
+    int64_t rows[4];
+    int64_t k;
+    const float *x;
+    float *y[4];
+} bm_matvec_call;
+typedef struct bm_step bm_step;
+int bm_step_create(const bm_matvec_call *calls, int ncalls, bm_step **step);
+int bm_step_run(const bm_step *step, bm_stream_t stream);
+int bm_step_destroy(bm_step *step);
+
+/*
  * rms_norm then mul of f32 rows by an f32 norm weight (page forward.md,
  * "Technical usage", "Other public pieces": the sum of squares in double, no
  * FMA; "Design notes", step three: the first RMS norm with its weight gives

@@ -238,3 +238,33 @@ def test_tc_plan_host_checks(L):
     assert st(L, "bm_tc_plan", 4096, 65544, 512, 0, info) == 1      # k > BM_MAX_K
     assert b"tensor-core" in L.bm_last_error()
 
+
+
+def test_step_create_host_checks(L):
+    import f16_weight_gemv_gb300 as bm
+    calls = (bm.MatvecCall * 2)()
+    out = C.c_void_p()
+    assert st(L, "bm_step_create", calls, 1, None) == 1          # null step
+    assert st(L, "bm_step_create", calls, 0, C.byref(out)) == 1  # no calls
+    c = calls[0]
+    c.nmat, c.k, c.x = 1, 4096, A + 2 ** 26
+    c.W[0], c.rows[0], c.y[0] = A, 64, A + 2 ** 27
+    c.nmat = 5
+    assert st(L, "bm_step_create", calls, 1, C.byref(out)) == 1  # nmat outside 1..4
+    c.nmat, c.k = 1, 4097
+    assert st(L, "bm_step_create", calls, 1, C.byref(out)) == 1  # k % 8 != 0
+    c.k, c.x = 4096, A + 2 ** 26 + 4
+    assert st(L, "bm_step_create", calls, 1, C.byref(out)) == 2  # x not 16-byte aligned
+    c.x, c.y[0] = A + 2 ** 26, A + 64                             # output inside W
+    assert st(L, "bm_step_create", calls, 1, C.byref(out)) == 1
+    c.y[0] = A + 2 ** 27
+    d = calls[1]
+    d.nmat, d.k, d.x = 1, 4096, A + 2 ** 26
+    d.W[0], d.rows[0], d.y[0] = A + 2 ** 28, 64, A + 2 ** 28 + 128  # call 1 writes into its own weights
+    assert st(L, "bm_step_create", calls, 2, C.byref(out)) == 1
+    d.y[0] = A + 128                                               # call 1 writes into call 0's weights
+    assert st(L, "bm_step_create", calls, 2, C.byref(out)) == 1
+    assert b"weights" in L.bm_last_error()
+    assert out.value is None
+    assert st(L, "bm_step_run", None, None) == 1
+    assert st(L, "bm_step_destroy", None) == 0
