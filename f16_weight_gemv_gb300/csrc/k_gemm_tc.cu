@@ -872,13 +872,31 @@ constexpr double kKblockUs[3] = {0.0, 0.45, 0.80};
 constexpr double kReduceFixedUs = 2.0;
 constexpr double kReduceBytesPerUs = 6.0e6;
 
+// Tiles of 64 columns or fewer: a k-block's time depends on how many SMs stream at
+// once.  One SM takes at least kNarrowKblockUs per k-block; all the busy SMs together
+// draw their weight tiles from HBM at about kNarrowHbmBytesPerUs.  Measured on GB300
+// at 8 to 64 columns over 32 to 224 row tiles and 1 to 8 splits: 0.32-0.35 us with
+// up to 112 SMs streaming, 0.40 us with 128, 0.47 us with all 152.  (A partial wave
+// of 112 row tiles unsplit then beats four splits of three waves and the reduction.)
+constexpr double kNarrowKblockUs = 0.33;
+constexpr double kNarrowHbmBytesPerUs = 5.3e6;
+
 // Predicted time of a plan in microseconds: waves x (k-blocks per unit x the time of
 // a k-block), plus, with S > 1, the reduction kernel.
 double plan_us(int64_t units_per_split, int64_t tiles128, int num_kb, int bn, int mt, int s, int ctas, int64_t rows,
                int64_t ncols)
 {
-    const double waves = std::ceil((double)units_per_split * s / ctas);
-    double us = waves * std::ceil((double)num_kb / s) * kKblockUs[mt];
+    double us;
+    if (bn <= 64) {
+        const int64_t units = units_per_split * s, full = units / ctas, rest = units % ctas;
+        auto kblock_us = [&](int64_t busy) {
+            return std::max(kNarrowKblockUs, (double)busy * mt * kTileABytes / kNarrowHbmBytesPerUs);
+        };
+        us = std::ceil((double)num_kb / s) * ((double)full * kblock_us(ctas) + (rest ? kblock_us(rest) : 0.0));
+    } else {
+        const double waves = std::ceil((double)units_per_split * s / ctas);
+        us = waves * std::ceil((double)num_kb / s) * kKblockUs[mt];
+    }
     if (s > 1)
         us += kReduceFixedUs + ((double)tiles128 * s * bn * kBM * 4.0 + (double)rows * ncols * 4.0) / kReduceBytesPerUs;
     return us;
@@ -1067,7 +1085,13 @@ int plan_gemm(Plan *pl, int nmat, const int64_t *rows, int64_t k, int64_t ncols,
             const int stage_b = mt * kTileABytes + bw * kBK * 2;
             const int ring_b = std::min(kMaxStages, (dev.max_smem_optin - 2048) / stage_b) * stage_b;
             const int64_t per_col = std::min<int64_t>(dev.sm_count / nt, units_rows * p.num_kb);  // CTAs per column
-            if (sk_mode != 0 && ring_b >= kEpiWarps * kOwnerDepth * 4096 && per_col >= 1) {
+            // Where the planner is free to choose, tiles of 64 columns or fewer never take
+            // balanced ranges: measured 10-30 % slower than whole tiles on the Llama-3-8B
+            // shapes at 8-64 columns, and up to twice as slow on products of a few MB
+            // (2048 x 1024, 3072 x 576 and 576 x 576 at 8-16 columns: 12-14 us against
+            // 6.8-7.5 us for whole tiles with k-splits).
+            const bool sk_ok = sk_mode == 1 || (sk_mode == -1 && bw > 64);
+            if (sk_ok && ring_b >= kEpiWarps * kOwnerDepth * 4096 && per_col >= 1) {
                 const int nbuf = 2 * mt * pow2_at_least(bw) <= 512 ? 2 : 1;
                 const bool many_waves = tiles >= 3 * (int64_t)dev.sm_count && bw == 256;  // measured there only
                 const double us = plan_sk_us(units_rows, p.num_kb, bw, mt, (int)per_col, nt, nbuf, many_waves);

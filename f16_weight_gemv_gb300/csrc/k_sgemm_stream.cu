@@ -26,13 +26,17 @@
 //     warps, not over lanes of one warp (measured);
 //   - two convert warps, alternating slots, widen a slot's X boxes to f32 once they
 //     have landed and signal the slot; the products then read f32 operands only;
-//   - eight consumer warps.  Lane 4*rs + lp of warp w holds row rs of each of the
-//     warp's R groups and chains 2lp, 2lp+1 of every column: 2*R*NCP accumulators.
-//     Each 8-element step reads 4 bytes of each of its R rows (eight rows per warp
-//     and group: one conflict-free wavefront by the swizzle), widens them once, and
-//     for each column reads 8 bytes of widened X (four addresses per warp), which
-//     then feed R rows from registers through paired f32 FMAs (fma.rn.f32x2: chains
-//     2lp and 2lp+1).  Every operand is an exactly widened f16, so every product is
+//   - eight consumer warps in CS column sets (CS = 1 or 2) of 8/CS warps; warp w
+//     takes columns (w % CS) * NCP/CS .. of R groups of the sub-block.  Lane
+//     4*rs + lp holds row rs of each of its warp's R groups and chains 2lp, 2lp+1 of
+//     each of the warp's columns: 2*R*NCP/CS accumulators.  Each 8-element step
+//     reads 4 bytes of each of its R rows (eight rows per warp and group: one
+//     conflict-free wavefront by the swizzle), widens them once, and for each of its
+//     columns reads 8 bytes of widened X (four addresses per warp), which then feed
+//     R rows from registers through paired f32 FMAs (fma.rn.f32x2: chains 2lp and
+//     2lp+1).  The launch picks R and CS from the groups a CTA owns and the columns:
+//     with a few groups per CTA (Llama Q: 3-4) a single column set would leave most
+//     warps idle while the busy ones wait on their loads.  Every operand is an exactly widened f16, so every product is
 //     exact and every FMA rounds once, as tinyBLAS's does.  (The mixed-precision
 //     f16 x f16 + f32 FMA would give the same bits but issues at half the f32 FMA
 //     rate, which a kernel doing up to 8 FMAs per weight element cannot afford.)
@@ -79,10 +83,13 @@ constexpr unsigned long long kTimeoutNs = 2000000000ull;
 // 1 KB swizzle periods so that column c of every box is swizzle row c % 8.
 __host__ __device__ constexpr uint32_t x16_slot(int ncp) { return ncp <= 8 ? 1024u : 2048u; }
 
-// Rows per consumer thread: each widened X value feeds R rows from registers, each
-// widened weight value feeds all NCP columns (2 * R * NCP <= 32 accumulators keep
-// the 576-thread CTA within its registers).
-constexpr int kRowsPerThread = 2;
+// Consumer layouts (R groups per warp, CS column sets): each widened X value feeds R
+// rows from registers, each widened weight value the warp's NCP/CS columns; at most
+// 2 * R * NCP / CS <= 32 accumulators keep the 576-thread CTA within its registers.
+struct Layout {
+    int R, CS;
+};
+constexpr Layout kLayouts[] = {{2, 1}, {1, 2}, {2, 2}, {3, 2}};
 
 struct SgemmJob {
     CUtensorMap wmap;  // W as [rows][k] 16-bit elements, box 64 x 8, 128-byte swizzle
@@ -162,9 +169,10 @@ __device__ __forceinline__ void walk(const SgemmJob &job, int64_t glo, int64_t g
     }
 }
 
-template <int NCP, int R>
+template <int NCP, int R, int CS>
 __global__ void __launch_bounds__(kThreads, 1) k_sgemm_stream(const __grid_constant__ SgemmJob job)
 {
+    constexpr int CW = NCP / CS;  // columns per warp
     constexpr uint32_t kX16Slot = x16_slot(NCP);
     constexpr uint32_t kX16BoxBytes = NCP * 128u;
     constexpr uint32_t kX32Block = NCP * 256u;
@@ -274,7 +282,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_sgemm_stream(const __grid_const
         dev::pdl_wait();  // output writes follow the kernel ahead
         const int lp = lane & 3;   // chains 2*lp and 2*lp + 1
         const int rs = lane >> 2;  // row within each of the warp's R groups
-        float acc[R][NCP][2];
+        const int c0 = (warp % CS) * CW;  // the warp's first column
+        const int wg = warp / CS;         // the warp's place in its column set
+        float acc[R][CW][2];
         walk(job, glo, ghi, [&](int t, int64_t g, int ng, int kc0, int nb, bool last) {
             const int slot = t % S;
             const uint32_t ph = (uint32_t)(t / S) & 1u;
@@ -282,22 +292,22 @@ __global__ void __launch_bounds__(kThreads, 1) k_sgemm_stream(const __grid_const
 #pragma unroll
                 for (int j = 0; j < R; j++)
 #pragma unroll
-                    for (int c = 0; c < NCP; c++) acc[j][c][0] = acc[j][c][1] = 0.0f;
+                    for (int c = 0; c < CW; c++) acc[j][c][0] = acc[j][c][1] = 0.0f;
             }
             if (!dev::mbar_wait_warp(dev::smem_u32(&wfull_bar[slot]), ph, abort_v, job.timeout_ns, job.err) ||
                 !dev::mbar_wait_warp(dev::smem_u32(&xready_bar[slot]), ph, abort_v, job.timeout_ns, job.err))
                 return false;
             const uint8_t *stage = smem + (size_t)slot * job.slot_bytes;
-            const int nact = min(R, ng - warp * R);  // groups of this warp in the sub-block (warp-uniform)
+            const int nact = min(R, ng - wg * R);  // groups of this warp in the sub-block (warp-uniform)
             if (nact > 0) {
-                // row rs of group warp*R + j: box (warp*R + j)*bps + b, 128-byte row rs, word lp of a chunk
-                const uint8_t *wrow = stage + (size_t)(warp * R * bps) * kWBoxBytes + rs * 128 + 4 * lp;
-                const uint8_t *x32 = stage + job.x32_off + 8 * lp;
+                // row rs of group wg*R + j: box (wg*R + j)*bps + b, 128-byte row rs, word lp of a chunk
+                const uint8_t *wrow = stage + (size_t)(wg * R * bps) * kWBoxBytes + rs * 128 + 4 * lp;
+                const uint8_t *x32 = stage + job.x32_off + c0 * 256 + 8 * lp;
                 const int nst = min(8 * bps, (job.k - kc0) >> 3);  // 8-element steps in this slice
                 for (int b = 0; b * 8 < nst; b++) {
                     const uint8_t *wb = wrow + b * kWBoxBytes;
                     const uint8_t *xb = x32 + b * kX32Block;
-                    // one 8-element step: R weight words, NCP widened X pairs, R * NCP paired FMAs
+                    // one 8-element step: R weight words, CW widened X pairs, R * CW paired FMAs
                     auto step = [&](int c8) {
                         float w[R][2];
 #pragma unroll
@@ -309,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_sgemm_stream(const __grid_const
                             widen2(w[j][0], w[j][1], h);
                         }
 #pragma unroll
-                        for (int c = 0; c < NCP; c++) {
+                        for (int c = 0; c < CW; c++) {
                             const float2 x = *reinterpret_cast<const float2 *>(xb + c * 256 + c8 * 32);
 #pragma unroll
                             for (int j = 0; j < R; j++) fma_x2(acc[j][c][0], acc[j][c][1], w[j][0], w[j][1], x.x, x.y);
@@ -329,16 +339,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_sgemm_stream(const __grid_const
                 // brings the other pair: ((l0+l4)+(l2+l6))+((l1+l5)+(l3+l7)) in every lane of the row.
 #pragma unroll
                 for (int j = 0; j < R; j++) {
-                    const int64_t row = (g + warp * R + j) * kGroupRows + rs;
+                    const int64_t row = (g + wg * R + j) * kGroupRows + rs;
                     const bool mine = j < nact && row < job.rows;
 #pragma unroll
-                    for (int c = 0; c < NCP; c++) {
+                    for (int c = 0; c < CW; c++) {
                         const float s0 = acc[j][c][0] + __shfl_xor_sync(0xffffffffu, acc[j][c][0], 2);
                         const float s1 = acc[j][c][1] + __shfl_xor_sync(0xffffffffu, acc[j][c][1], 2);
                         const float o0 = __shfl_xor_sync(0xffffffffu, s0, 1);
                         const float o1 = __shfl_xor_sync(0xffffffffu, s1, 1);
                         const float y = (lp & 1) ? (o0 + s0) + (o1 + s1) : (s0 + o0) + (s1 + o1);
-                        if (mine && lp == (c & 3) && c < job.ncols) job.Y[(int64_t)c * job.rows + row] = y;
+                        const int col = c0 + c;
+                        if (mine && lp == (col & 3) && col < job.ncols) job.Y[(int64_t)col * job.rows + row] = y;
                     }
                 }
             }
@@ -393,21 +404,36 @@ bool make_map(CUtensorMap *map, const uint16_t *base, int64_t outer, int64_t k, 
 }
 
 constexpr int kMaxDevices = 64;
-std::once_flag g_attr_once[kMaxDevices][5];
+constexpr int kNumLayouts = sizeof(kLayouts) / sizeof(kLayouts[0]);
+std::once_flag g_attr_once[kMaxDevices][5][kNumLayouts];
 
-template <int NCP>
-int launch_ncp(SgemmJob &job, cudaStream_t s, const DeviceInfo &dev)
+// The consumer layout for a CTA of `gpc` groups and NCP columns, as measured on GB300
+// (Llama-3-8B and Qwen3 shapes at 2-8 columns, chains of launches over weights larger
+// than L2; every layout gives the same bits):
+//   - up to 4 groups (Q, down: 3-4): two column sets, one group per warp (21-31 % faster
+//     than one column set at 2-4 columns), two groups per warp at 6-8 columns (39-42 %);
+//   - 5 to 12 groups (Q/K/V: 5-6, gate: 12): two column sets, three groups per warp,
+//     except gate-like CTAs of 9-12 groups at 2 columns, where one column set is 2 %
+//     faster;
+//   - 13 or more (gate/up: 24, the output product: 105): one column set, two groups
+//     per warp (the others measured 1-40 % slower).
+int pick_layout(int64_t gpc, int ncp)
 {
-    constexpr int R = kRowsPerThread;
-    auto kern = k_sgemm_stream<NCP, R>;
+    if (gpc <= 4) return ncp <= 4 ? 1 : 2;
+    if (gpc <= 12) return gpc >= 9 && ncp == 2 ? 0 : 3;
+    return 0;
+}
+
+template <int NCP, int LI>
+int launch_layout(SgemmJob &job, int64_t grid, int64_t groups_per_cta, cudaStream_t s, const DeviceInfo &dev)
+{
+    constexpr int R = kLayouts[LI].R, CS = kLayouts[LI].CS;
+    auto kern = k_sgemm_stream<NCP, R, CS>;
     // One CTA per SM.  The slot layout follows the groups a CTA owns: a sub-block of
-    // up to 8*R groups, and as many 64-element blocks per slot as keep its weight boxes
-    // within 32; then as many slots as shared memory holds, so that the most weight
-    // bytes are in flight.
-    const int64_t G = job.groups;
-    const int64_t grid = std::min<int64_t>((int64_t)dev.sm_count, G);
-    const int64_t groups_per_cta = (G + grid - 1) / grid;
-    job.sub = (int)std::min<int64_t>(kConsumerWarps * R, groups_per_cta);
+    // up to 8/CS*R groups, and as many 64-element blocks per slot as keep its weight
+    // boxes within 32; then as many slots as shared memory holds, so that the most
+    // weight bytes are in flight.
+    job.sub = (int)std::min<int64_t>(kConsumerWarps / CS * R, groups_per_cta);
     job.bps = std::max(1, std::min(kMaxBlocks, kMaxWBoxes / job.sub));
     job.x16_off = (uint32_t)(job.sub * job.bps) * kWBoxBytes;
     job.x32_off = job.x16_off + (uint32_t)job.bps * x16_slot(NCP);
@@ -421,7 +447,7 @@ int launch_ncp(SgemmJob &job, cudaStream_t s, const DeviceInfo &dev)
 
     int dev_id = 0;
     cudaGetDevice(&dev_id);
-    std::call_once(g_attr_once[dev_id & (kMaxDevices - 1)][NCP / 2], [&] {
+    std::call_once(g_attr_once[dev_id & (kMaxDevices - 1)][NCP / 2][LI], [&] {
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, dev.max_smem_optin - 1024);
     });
 
@@ -438,6 +464,20 @@ int launch_ncp(SgemmJob &job, cudaStream_t s, const DeviceInfo &dev)
     cudaError_t e = cudaLaunchKernelEx(&cfg, kern, job);
     if (e != cudaSuccess) return fail(BM_ERR_CUDA, "sgemm stream: launch failed: %s", cudaGetErrorString(e));
     return BM_OK;
+}
+
+template <int NCP>
+int launch_ncp(SgemmJob &job, cudaStream_t s, const DeviceInfo &dev)
+{
+    const int64_t G = job.groups;
+    const int64_t grid = std::min<int64_t>((int64_t)dev.sm_count, G);
+    const int64_t groups_per_cta = (G + grid - 1) / grid;
+    switch (pick_layout(groups_per_cta, NCP)) {
+    case 0: return launch_layout<NCP, 0>(job, grid, groups_per_cta, s, dev);
+    case 1: return launch_layout<NCP, 1>(job, grid, groups_per_cta, s, dev);
+    case 2: return launch_layout<NCP, 2>(job, grid, groups_per_cta, s, dev);
+    default: return launch_layout<NCP, 3>(job, grid, groups_per_cta, s, dev);
+    }
 }
 
 }  // namespace

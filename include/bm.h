@@ -346,8 +346,8 @@ int bm_set_exact_sgemm_cols(int ncols);
  * The k-blocks of all tiles of a product are cut into equal ranges, one per SM;
  * a tile shared by several SMs is finished by the SM holding its last k-block,
  * which adds the other pieces in k order.  mode -1 (default): used where the
- * library's time model predicts it clearly faster than whole tiles or k-splits;
- * 0: never; 1: wherever it applies (at least one SM per column tile of the
+ * library's time model predicts it clearly faster than whole tiles or k-splits,
+ * never for products of 64 columns or fewer (measured slower there); 0: never; 1: wherever it applies (at least one SM per column tile of the
  * product).  Any other value counts as its sign.  The result stays within the
  * tensor-core bound in every mode and is repeatable (the same bits for the same
  * product, mode and GPU).  The workspace (one partial tile per SM and a flag word

@@ -6,6 +6,8 @@
   launch, replayed; every output of the step bit for bit against the oracle
   (page f16.md, Design notes, "vec_dot"; forward.md, Advantages, "Shared activations").
 - Llama-3-8B and Qwen3-0.6B one-column products at full size, every row bit for bit.
+- Llama-3-8B products at 2-64 columns (decode batches) at full size, every element:
+  the exact kernel's bits, the tensor cores within the bound.
 - The 512-column tensor-core products at full size, EVERY element within
   4e-6 * sum|w*a| of tinyBLAS's element (f16.md, Design notes, "sgemm_dot"), into
   NaN-filled outputs, in the plan the library chooses and again with balanced k
@@ -101,6 +103,18 @@ class Reference:
         assert not bad.any(), "%s: %d elements outside the bound, worst ratio %.3g" % (
             what, int(bad.sum()), float((err / np.maximum(self.bound, 1e-300)).max()))
 
+    def check_cols(self, Y, nc, what):
+        """The first nc columns (a product over X[:nc]) within the bound."""
+        got = Y.detach().cpu().numpy().astype(np.float64)
+        assert np.isfinite(got).all(), what + ": an element was never written (NaN left)"
+        err = np.abs(got - self.ref[:nc])
+        bad = err > self.bound[:nc]
+        assert not bad.any(), "%s: %d elements outside the bound" % (what, int(bad.sum()))
+
+    def bits_cols(self, nc):
+        """tinyBLAS's bits of the first nc columns (the oracle's f32 result)."""
+        return self.ref[:nc].astype(np.float32).view(np.uint32)
+
 
 _prefill_refs = {}
 
@@ -158,6 +172,45 @@ def test_full_size_512_columns_every_element(bm, name, rows, k):
             bm.bm_set_stream_k(old)
     assert bm.bm_device_status() == 0
     assert plans[1]["balanced"] == 1, plans  # the forced mode really ran balanced k ranges
+
+
+FEW = [("q", 4096, 4096), ("gate", 14336, 4096), ("down", 4096, 14336), ("qkv", 6144, 4096)]
+
+
+@pytest.mark.parametrize("name,rows,k", FEW)
+def test_full_size_few_columns_every_element(bm, name, rows, k):
+    """Decode-batch widths of the Llama-3-8B products at full size, every element into
+    NaN-filled outputs, twice: 2 and 3 columns on the exact CUDA-core kernel, tinyBLAS's
+    bits (f16.md, Design notes, "sgemm_dot"; 3 columns with bm_set_exact_sgemm_cols(8)),
+    in the consumer layout its launch picks for these row counts; 8, 16 and 64 columns on
+    the tensor cores within the bound, where Q and down split k (partials summed in split
+    order by the reduction kernel)."""
+    import torch
+    if name == "qkv":
+        W, X = other_inputs("llama3_8b.qkv", rows, k)
+        ref = Reference(W, X[:64])
+    else:
+        ref = prefill_reference(name)
+    dW, dX = to_dev(ref.W), to_dev(ref.X)
+    plans = {}
+    for nc, exact in ((2, 2), (3, 8), (8, 2), (16, 2), (64, 2)):
+        old = bm.bm_set_exact_sgemm_cols(exact)
+        try:
+            Xn = dX[:nc].contiguous()
+            if nc > exact:
+                plans[nc] = bm.bm_tc_plan(rows, k, nc)
+            for _ in range(2):  # twice: the second launch finds the first one's workspace contents
+                Y = torch.full((nc, rows), float("nan"), dtype=torch.float32, device="cuda")
+                bm.bm_f16_matmul(dW, Xn, Y)
+                if nc <= exact:
+                    assert np.array_equal(bits32(Y), ref.bits_cols(nc)), (name, nc)
+                else:
+                    ref.check_cols(Y, nc, "%s x %d columns, plan %s" % (name, nc, plans[nc]))
+        finally:
+            bm.bm_set_exact_sgemm_cols(old)
+    assert bm.bm_device_status() == 0
+    if name in ("q", "down"):
+        assert all(p["splits"] > 1 for p in plans.values()), plans  # the split-k path ran
 
 
 @pytest.mark.parametrize("variant", ["multi", "separate", "concat"])
