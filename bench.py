@@ -130,7 +130,7 @@ NCU_TRAFFIC = {"kernel": "k_gemv_stream", "source": "f16_weight_gemv_gb300/csrc/
 # write bytes), from the ncu launch list in profiles/prefill_layer_llama3_8b_launches.md, valid
 # only for the kernel source it was measured on.
 PREFILL_TRAFFIC = {"kernel": "k_gemm_tc", "source": "f16_weight_gemv_gb300/csrc/k_gemm_tc.cu",
-                   "sha256_16": "ada03cc1911f3a90", "bytes_per_launch": [54724096, 37835264, 281087744, 132340480]}
+                   "sha256_16": "c52fe893d3def690", "bytes_per_launch": [54795264, 37834496, 281310976, 132292096]}
 
 
 def prefill_traffic_per_launch():
