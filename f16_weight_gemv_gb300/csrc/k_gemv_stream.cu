@@ -17,29 +17,28 @@
 // Layout on the GPU.  Each matrix's rows are cut into groups of 8; the groups
 // of all (up to four) matrices are split evenly between the CTAs (CTA b owns
 // groups [G*b/n, G*(b+1)/n)), so every SM streams the same number of rows at any
-// product size.  A CTA walks its groups in sub-blocks of up to eight groups of
+// product size.  A CTA walks its groups in sub-blocks of up to four groups of
 // one matrix, and each sub-block in k-slices: a stage holds up to 32 TMA boxes
-// of 8 rows x 64 elements, floor(32 / groups) boxes per group (slices of 256 to
-// 2048 elements; with 3, 5 or 6 groups the stage is fuller than with a power of
-// two per group: Q/K/V-sized products measured 7 % faster).  The boxes of a stage are issued in
-// parallel by 16 threads in four producer warps, two TMA instructions each (one
-// issuing thread cannot keep HBM busy with 1 KB boxes; issue spreads best across
-// warps), each thread arriving on the stage's barrier with its own byte count.
-// Boxes are stored with the
+// of 8 rows x 64 elements, floor(32 / groups) boxes per group (slices of 512 to
+// 2048 elements; with 3 groups the stage is fuller than with a power of two per
+// group).  The boxes of a stage are issued in parallel by 16 threads in four
+// producer warps, two TMA instructions each (one issuing thread cannot keep HBM
+// busy with 1 KB boxes; issue spreads best across warps), each thread arriving on
+// the stage's barrier with its own byte count.  Boxes are stored with the
 // 128-byte swizzle (16-byte chunk c of row r lands at chunk c ^ (r % 8)).  Rows
-// past the matrix and columns past k are zero-filled and never used.  Consumer
-// warp w owns group w of the sub-block: four threads per row, thread j holding
-// accumulator j (chains 8j..8j+7) and reading the 16 bytes at element 32s + 8j
-// of each step, the activation's matching 16 bytes as a broadcast.  Lanes
-// 4t..4t+3 serve row (t >> 1) | ((t & 1) << 2), so the two rows of every
-// 8-lane phase differ in bit 2 and their swizzled chunks fall in disjoint
-// banks.  The reduction is two xor-shuffles across the row's four threads,
-// then the lane pairs in registers.  A CTA of at most four groups (the short
-// products of a decode step: Q, O, down, Q/K/V) would leave most consumer warps
-// without rows that way; it takes eight threads per row instead, each holding
-// half an accumulator (chains 4q..4q+3, 8-byte reads), two warps per group: the
-// same chains in the same order, reduced by the same additions (the partners of
-// accumulator j^2 and j^1, then the high lanes, then the horizontal adds).
+// past the matrix and columns past k are zero-filled and never used.  Two
+// consumer warps serve each group, eight threads per row: thread q holds lanes
+// 4(q & 1) .. +3 of accumulator q >> 1 (chains 4q..4q+3) and reads the 8 bytes at
+// element 32s + 4q of each step, the activation's matching 8 bytes as a
+// broadcast.  Warp w serves four rows of group w / 2, lanes 8r..8r+7 row
+// (r >> 1) | ((w & 1) << 1) | ((r & 1) << 2), so the two rows of every 16-lane
+// phase differ in bit 2 and their swizzled chunks fall in disjoint banks.  The
+// reduction is three xor-shuffles across the row's eight threads (the partners
+// holding accumulator j^2, then j^1, then the high four lanes), then the two
+// horizontal adds in registers.  Eight threads per row keep every consumer warp
+// busy in CTAs of one or two groups (the short products of a decode step) and
+// measured faster than four threads per row, each holding a whole accumulator,
+// on the long products too.
 //
 // Programmatic dependent launch: the producer issues its first ring's worth of
 // weight copies at once -- the weights are not written by the kernel ahead of
@@ -69,12 +68,9 @@ constexpr int kIssuersPerWarp = 4;  // lanes of a producer warp that issue TMA c
 constexpr int kIssuers = kProducerWarps * kIssuersPerWarp;
 constexpr int kThreads = 32 * (kConsumerWarps + kProducerWarps);
 constexpr int kGroupRows = 8;                   // rows per TMA box
-// Consumer layouts: TPR threads per row.  TPR = 4: a warp holds 8 rows (one group), a
-// sub-block up to 8 groups.  TPR = 8: a warp holds 4 rows, two warps a group, a
-// sub-block up to 4 groups -- for CTAs of few groups, where the 4-thread layout left
-// most consumer warps without rows.
-template <int TPR>
-__host__ __device__ constexpr int groups_per_block() { return kConsumerWarps * 4 / TPR; }
+constexpr int kThreadsPerRow = 8;                                      // each holds 4 of a row's 32 chains
+constexpr int kRowsPerWarp = 32 / kThreadsPerRow;                      // 4
+constexpr int kGroupsPerBlock = kConsumerWarps * kRowsPerWarp / kGroupRows;  // sub-block: 4 groups, 2 warps each
 constexpr int kBoxCols = 64;                    // 128 bytes: one swizzle row
 constexpr uint32_t kBoxBytes = kGroupRows * kBoxCols * 2;  // 1 KB
 constexpr int kBoxesPerStage = 32;
@@ -128,15 +124,6 @@ __device__ __forceinline__ void fma2(float &a0, float &a1, uint32_t w, uint32_t 
         : "r"(w), "r"(x));
 }
 
-// Lanes l = 0..7 of one accumulator: elements 8j + l of a step.
-__device__ __forceinline__ void fma8(float (&acc)[8], const uint4 &w, const uint4 &x)
-{
-    fma2(acc[0], acc[1], w.x, x.x);
-    fma2(acc[2], acc[3], w.y, x.y);
-    fma2(acc[4], acc[5], w.z, x.z);
-    fma2(acc[6], acc[7], w.w, x.w);
-}
-
 // Lanes 4h .. 4h+3 of one accumulator: elements 8j + 4h .. 8j + 4h + 3 of a step.
 __device__ __forceinline__ void fma4(float (&acc)[4], const uint2 &w, const uint2 &x)
 {
@@ -174,10 +161,8 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
 // Named barrier of the eight consumer warps (the producer warp never joins it).
 __device__ __forceinline__ void consumers_sync() { asm volatile("bar.sync 1, %0;" ::"n"(32 * kConsumerWarps)); }
 
-template <int TPR>
 __global__ void __launch_bounds__(kThreads, 2) k_gemv_stream(const __grid_constant__ StreamJob job)
 {
-    constexpr int kGroupsPerBlock = groups_per_block<TPR>();
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[kMaxStages];
     __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
@@ -351,22 +336,18 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv_stream(const __grid_consta
         }
         consumers_sync();
 
-        // TPR = 4: thread j of a row holds accumulator j (chains 8j..8j+7) and reads the 16
-        // bytes at element 32s + 8j; lanes 4t..4t+3 serve row (t >> 1) | ((t & 1) << 2).
-        // TPR = 8: thread q of a row holds lanes 4(q & 1) .. +3 of accumulator q >> 1 (chains
-        // 4q..4q+3) and reads the 8 bytes at element 32s + 4q; warp w serves rows of group
-        // w / 2, lanes 8r..8r+7 row (r >> 1) | ((w & 1) << 1) | ((r & 1) << 2).  Either way
-        // the two rows of a shared-memory phase differ in bit 2, so their swizzled chunks
+        // Thread q of a row holds lanes 4(q & 1) .. +3 of accumulator j = q >> 1 (chains
+        // 4q..4q+3) and reads the 8 bytes at element 32s + 4q; warp w serves 4 rows of group
+        // w / 2, lanes 8r..8r+7 row (r >> 1) | ((w & 1) << 1) | ((r & 1) << 2), so the two
+        // rows of a 16-lane shared-memory phase differ in bit 2 and their swizzled chunks
         // fall in disjoint banks.
-        const int tq = lane % TPR;                                  // thread within the row
-        const int tr = lane / TPR;                                  // row slot within the warp
-        const int gw = TPR == 4 ? warp : warp >> 1;                 // the warp's group in the sub-block
-        const int rho = TPR == 4 ? (tr >> 1) | ((tr & 1) << 2)
-                                 : (tr >> 1) | ((warp & 1) << 1) | ((tr & 1) << 2);  // row in the group
-        const int j = TPR == 4 ? tq : tq >> 1;                      // accumulator
-        const int hq = TPR == 4 ? 0 : tq & 1;                       // half of it (TPR = 8)
-        const uint4 *x4 = reinterpret_cast<const uint4 *>(xs) + j;  // TPR 4: x[32s + 8j] at x4[4s]
-        const uint2 *x2 = reinterpret_cast<const uint2 *>(xs) + tq; // TPR 8: x[32s + 4q] at x2[8s]
+        const int tq = lane % kThreadsPerRow;                       // thread within the row
+        const int tr = lane / kThreadsPerRow;                       // row slot within the warp
+        const int gw = warp >> 1;                                   // the warp's group in the sub-block
+        const int rho = (tr >> 1) | ((warp & 1) << 1) | ((tr & 1) << 2);  // row in the group
+        const int j = tq >> 1;                                      // accumulator
+        const int hq = tq & 1;                                      // its half
+        const uint2 *x2 = reinterpret_cast<const uint2 *>(xs) + tq; // x[32s + 4q] at x2[8s]
         bool ok = true;
         int t = 0;
         for (int g = glo; g < ghi && ok;) {
@@ -387,10 +368,9 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv_stream(const __grid_consta
             const int sw = bpg * kBoxCols;
             const int row = (g_in_m + gw) * kGroupRows + rho;  // this thread's row (< 2^31)
             const bool active = gw < ng;                                       // warp-uniform
-            constexpr int NA = 32 / TPR;  // accumulator lanes held per thread
-            float acc[NA];
+            float acc[4];  // lanes 4hq .. 4hq+3 of accumulator j
 #pragma unroll
-            for (int e = 0; e < NA; e++) acc[e] = 0.0f;
+            for (int e = 0; e < 4; e++) acc[e] = 0.0f;
             for (int sl = 0; sl < nslices; sl++, t++) {
                 const int slot = t % S;
                 const uint32_t ph = (uint32_t)(t / S) & 1u;
@@ -408,55 +388,32 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv_stream(const __grid_consta
                     for (; s + 2 <= nst; s += 2) {  // one 64-element box: two steps
                         const uint8_t *bx = rbase + (s >> 1) * kBoxBytes;
                         const int S0 = kc0 / 32 + s;
-                        if constexpr (TPR == 4) {
-                            const uint4 w0 = *reinterpret_cast<const uint4 *>(bx + ((j) ^ rho) * 16);
-                            const uint4 w1 = *reinterpret_cast<const uint4 *>(bx + ((4 + j) ^ rho) * 16);
-                            fma8(acc, w0, x4[4 * S0]);
-                            fma8(acc, w1, x4[4 * S0 + 4]);
-                        } else {
-                            const uint2 w0 = *reinterpret_cast<const uint2 *>(bx + ((j) ^ rho) * 16 + hq * 8);
-                            const uint2 w1 = *reinterpret_cast<const uint2 *>(bx + ((4 + j) ^ rho) * 16 + hq * 8);
-                            fma4(acc, w0, x2[8 * S0]);
-                            fma4(acc, w1, x2[8 * S0 + 8]);
-                        }
+                        const uint2 w0 = *reinterpret_cast<const uint2 *>(bx + ((j) ^ rho) * 16 + hq * 8);
+                        const uint2 w1 = *reinterpret_cast<const uint2 *>(bx + ((4 + j) ^ rho) * 16 + hq * 8);
+                        fma4(acc, w0, x2[8 * S0]);
+                        fma4(acc, w1, x2[8 * S0 + 8]);
                     }
                     if (s < nst) {
                         const uint8_t *bx = rbase + (s >> 1) * kBoxBytes;
                         const int S0 = kc0 / 32 + s;
-                        if constexpr (TPR == 4) {
-                            const uint4 w0 = *reinterpret_cast<const uint4 *>(bx + ((j) ^ rho) * 16);
-                            fma8(acc, w0, x4[4 * S0]);
-                        } else {
-                            const uint2 w0 = *reinterpret_cast<const uint2 *>(bx + ((j) ^ rho) * 16 + hq * 8);
-                            fma4(acc, w0, x2[8 * S0]);
-                        }
+                        const uint2 w0 = *reinterpret_cast<const uint2 *>(bx + ((j) ^ rho) * 16 + hq * 8);
+                        fma4(acc, w0, x2[8 * S0]);
                     }
                 }
                 if (sl == nslices - 1) {
-                    // (a0 + a2) + (a1 + a3) lane by lane: the partners holding accumulator j^2,
-                    // then j^1, at the same lanes; then low four lanes + high four lanes, then
-                    // the two horizontal adds.  The thread holding accumulator 0 (lanes 0-3
-                    // with TPR = 8) ends with the row's sum.
-                    float red;
-                    if constexpr (TPR == 4) {
+                    // (a0 + a2) + (a1 + a3) lane by lane: the partners holding accumulator j^2
+                    // (thread q^4), then j^1 (q^2), at the same lanes; then low four lanes + high
+                    // four lanes (q^1), then the two horizontal adds.  Thread 0 of the row, lanes
+                    // 0-3 of accumulator 0, ends with the row's sum.
 #pragma unroll
-                        for (int e = 0; e < 8; e++) acc[e] += __shfl_xor_sync(kFull, acc[e], 2);
+                    for (int e = 0; e < 4; e++) acc[e] += __shfl_xor_sync(kFull, acc[e], 4);
 #pragma unroll
-                        for (int e = 0; e < 8; e++) acc[e] += __shfl_xor_sync(kFull, acc[e], 1);
-                        const float t0 = acc[0] + acc[4], t1 = acc[1] + acc[5], t2 = acc[2] + acc[6],
-                                    t3 = acc[3] + acc[7];
-                        red = (t0 + t1) + (t2 + t3);
-                    } else {
+                    for (int e = 0; e < 4; e++) acc[e] += __shfl_xor_sync(kFull, acc[e], 2);
+                    float hi[4];
 #pragma unroll
-                        for (int e = 0; e < 4; e++) acc[e] += __shfl_xor_sync(kFull, acc[e], 4);
-#pragma unroll
-                        for (int e = 0; e < 4; e++) acc[e] += __shfl_xor_sync(kFull, acc[e], 2);
-                        float hi[4];
-#pragma unroll
-                        for (int e = 0; e < 4; e++) hi[e] = __shfl_xor_sync(kFull, acc[e], 1);
-                        const float t0 = acc[0] + hi[0], t1 = acc[1] + hi[1], t2 = acc[2] + hi[2], t3 = acc[3] + hi[3];
-                        red = (t0 + t1) + (t2 + t3);
-                    }
+                    for (int e = 0; e < 4; e++) hi[e] = __shfl_xor_sync(kFull, acc[e], 1);
+                    const float t0 = acc[0] + hi[0], t1 = acc[1] + hi[1], t2 = acc[2] + hi[2], t3 = acc[3] + hi[3];
+                    const float red = (t0 + t1) + (t2 + t3);
                     if (active && tq == 0 && row < job.rows[m]) {
                         float out = red;
                         if (32 * nsteps < k) {
@@ -552,7 +509,7 @@ bool row_map_cached(CUtensorMap *map, const uint16_t *W, int64_t rows, int64_t k
 }
 
 constexpr int kMaxDevices = 64;
-std::once_flag g_attr_once[kMaxDevices][2];
+std::once_flag g_attr_once[kMaxDevices];
 
 }  // namespace
 
@@ -606,14 +563,12 @@ int launch_gemv_stream(const VecdotJob &vj, const float *x_f32, uint16_t *h_out,
     const int stages = (int)std::min<int64_t>(want, room);
     job.stages = stages;
     const size_t smem = xbytes + (size_t)stages * kStageBytes + 1024;
-    // CTAs of up to 4 groups take 8 threads per row, so every consumer warp has rows.
-    const bool tpr8 = (G + grid - 1) / grid <= groups_per_block<8>();
-    auto kern = tpr8 ? k_gemv_stream<8> : k_gemv_stream<4>;
 
     int dev_id = 0;
     cudaGetDevice(&dev_id);
-    std::call_once(g_attr_once[dev_id & (kMaxDevices - 1)][tpr8 ? 1 : 0], [&] {
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, dev.max_smem_optin - 1024);
+    std::call_once(g_attr_once[dev_id & (kMaxDevices - 1)], [&] {
+        cudaFuncSetAttribute(k_gemv_stream, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             dev.max_smem_optin - 1024);
     });
 
     cudaLaunchConfig_t cfg{};
@@ -626,7 +581,7 @@ int launch_gemv_stream(const VecdotJob &vj, const float *x_f32, uint16_t *h_out,
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl_enabled() ? 1 : 0;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, job);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, k_gemv_stream, job);
     if (e != cudaSuccess) return fail(BM_ERR_CUDA, "vec_dot (stream): launch failed: %s", cudaGetErrorString(e));
     return BM_OK;
 }
