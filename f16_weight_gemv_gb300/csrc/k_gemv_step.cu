@@ -4,9 +4,10 @@
 // nearest-even (page "docs/modules/f16.md", Design notes, "Activation"), then
 // multiplied by up to four matrices, ggml_vec_dot_f16 per row, bit for bit
 // (Design notes, "vec_dot": 32 chains, (a0+a2)+(a1+a3), low + high, two
-// horizontal adds, the k%32 tail in double).  The rows, chains, TMA boxes,
-// lane map and reduction are those of k_gemv_stream.cu, so every output has the
-// bits the separate calls give.
+// horizontal adds, the k%32 tail in double).  The chains, TMA boxes and reduction
+// order are those of k_gemv_stream.cu, so every output has the bits the separate
+// calls give; the consumers here keep four threads per row (thread j holding
+// accumulator j, 16-byte reads, one warp per group).
 //
 // What differs is the schedule.  One persistent grid (two CTAs per SM, launched
 // cooperatively so that all of them are resident) walks the calls in order.  The
