@@ -35,10 +35,12 @@
 // phase differ in bit 2 and their swizzled chunks fall in disjoint banks.  The
 // reduction is three xor-shuffles across the row's eight threads (the partners
 // holding accumulator j^2, then j^1, then the high four lanes), then the two
-// horizontal adds in registers.  Eight threads per row keep every consumer warp
-// busy in CTAs of one or two groups (the short products of a decode step) and
-// measured faster than four threads per row, each holding a whole accumulator,
-// on the long products too.
+// horizontal adds in registers.  Eight threads per row measured faster than four
+// (each holding a whole accumulator) on every product; CTAs of one or two groups of
+// rows up to 4096 elements (the short products of a decode step) take sixteen, two
+// chains and 4 bytes per step each, four warps per group, rows w % 4 and w % 4 + 4
+// of group w / 4 in warp w, the reduction starting at the partner of accumulator
+// j^2 (xor 8), so that every consumer warp has rows.
 //
 // Programmatic dependent launch: the producer issues its first ring's worth of
 // weight copies at once -- the weights are not written by the kernel ahead of
@@ -68,9 +70,12 @@ constexpr int kIssuersPerWarp = 4;  // lanes of a producer warp that issue TMA c
 constexpr int kIssuers = kProducerWarps * kIssuersPerWarp;
 constexpr int kThreads = 32 * (kConsumerWarps + kProducerWarps);
 constexpr int kGroupRows = 8;                   // rows per TMA box
-constexpr int kThreadsPerRow = 8;                                      // each holds 4 of a row's 32 chains
-constexpr int kRowsPerWarp = 32 / kThreadsPerRow;                      // 4
-constexpr int kGroupsPerBlock = kConsumerWarps * kRowsPerWarp / kGroupRows;  // sub-block: 4 groups, 2 warps each
+// Consumer layouts: TPR threads per row, each holding 32 / TPR of the row's 32 chains.
+// TPR = 8: 4 rows per warp, two warps a group, sub-blocks of up to 4 groups.  TPR = 16
+// (CTAs of one or two groups of short rows): 2 rows per warp, four warps a group,
+// sub-blocks of up to 2 groups, so every consumer warp has rows.
+template <int TPR>
+__host__ __device__ constexpr int groups_per_block() { return kConsumerWarps * (32 / TPR) / kGroupRows; }
 constexpr int kBoxCols = 64;                    // 128 bytes: one swizzle row
 constexpr uint32_t kBoxBytes = kGroupRows * kBoxCols * 2;  // 1 KB
 constexpr int kBoxesPerStage = 32;
@@ -131,6 +136,18 @@ __device__ __forceinline__ void fma4(float (&acc)[4], const uint2 &w, const uint
     fma2(acc[2], acc[3], w.y, x.y);
 }
 
+// A thread's chains of one step from its bytes of W and x: 4 chains (8 bytes, TPR 8) or
+// 2 chains (4 bytes, TPR 16).
+template <int TPR>
+__device__ __forceinline__ void fma_step(float (&acc)[32 / TPR], const uint8_t *w, const uint16_t *x)
+{
+    if constexpr (TPR == 8) {
+        fma4(acc, *reinterpret_cast<const uint2 *>(w), *reinterpret_cast<const uint2 *>(x));
+    } else {
+        fma2(acc[0], acc[1], *reinterpret_cast<const uint32_t *>(w), *reinterpret_cast<const uint32_t *>(x));
+    }
+}
+
 __device__ __forceinline__ float widen(uint16_t h) { return __half2float(__ushort_as_half(h)); }
 
 __device__ __forceinline__ uint32_t pack_rn(float lo, float hi)
@@ -161,8 +178,11 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
 // Named barrier of the eight consumer warps (the producer warp never joins it).
 __device__ __forceinline__ void consumers_sync() { asm volatile("bar.sync 1, %0;" ::"n"(32 * kConsumerWarps)); }
 
+template <int TPR>
 __global__ void __launch_bounds__(kThreads, 2) k_gemv_stream(const __grid_constant__ StreamJob job)
 {
+    constexpr int kGroupsPerBlock = groups_per_block<TPR>();
+    constexpr int kChains = 32 / TPR;  // chains per thread
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[kMaxStages];
     __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
@@ -336,18 +356,21 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv_stream(const __grid_consta
         }
         consumers_sync();
 
-        // Thread q of a row holds lanes 4(q & 1) .. +3 of accumulator j = q >> 1 (chains
-        // 4q..4q+3) and reads the 8 bytes at element 32s + 4q; warp w serves 4 rows of group
-        // w / 2, lanes 8r..8r+7 row (r >> 1) | ((w & 1) << 1) | ((r & 1) << 2), so the two
-        // rows of a 16-lane shared-memory phase differ in bit 2 and their swizzled chunks
-        // fall in disjoint banks.
-        const int tq = lane % kThreadsPerRow;                       // thread within the row
-        const int tr = lane / kThreadsPerRow;                       // row slot within the warp
-        const int gw = warp >> 1;                                   // the warp's group in the sub-block
-        const int rho = (tr >> 1) | ((warp & 1) << 1) | ((tr & 1) << 2);  // row in the group
-        const int j = tq >> 1;                                      // accumulator
-        const int hq = tq & 1;                                      // its half
-        const uint2 *x2 = reinterpret_cast<const uint2 *>(xs) + tq; // x[32s + 4q] at x2[8s]
+        // Thread q of a row holds chains c = C q .. C q + C - 1 (C = 32 / TPR): lanes
+        // c % 8 .. of accumulator j = c / 8; it reads the 2C bytes at element 32s + C q.
+        // TPR = 8: warp w serves 4 rows of group w / 2, lanes 8r..8r+7 row
+        // (r >> 1) | ((w & 1) << 1) | ((r & 1) << 2).  TPR = 16: warp w serves rows w % 4 and
+        // w % 4 + 4 of group w / 4 (lanes 0-15, 16-31).  Either way the two rows of a
+        // shared-memory phase differ in bit 2, so their swizzled chunks fall in disjoint
+        // banks.
+        const int tq = lane % TPR;                                  // thread within the row
+        const int tr = lane / TPR;                                  // row slot within the warp
+        const int gw = TPR == 8 ? warp >> 1 : warp >> 2;            // the warp's group in the sub-block
+        const int rho = TPR == 8 ? (tr >> 1) | ((warp & 1) << 1) | ((tr & 1) << 2)
+                                 : (warp & 3) | (tr << 2);           // row in the group
+        const int j = tq * kChains / 8;                             // accumulator
+        const int lb = 2 * ((tq * kChains) % 8);                    // byte of its first lane in a chunk
+        const uint16_t *xq = xs + tq * kChains;                     // x[32s + C q] at xq[32 s]
         bool ok = true;
         int t = 0;
         for (int g = glo; g < ghi && ok;) {
@@ -368,9 +391,9 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv_stream(const __grid_consta
             const int sw = bpg * kBoxCols;
             const int row = (g_in_m + gw) * kGroupRows + rho;  // this thread's row (< 2^31)
             const bool active = gw < ng;                                       // warp-uniform
-            float acc[4];  // lanes 4hq .. 4hq+3 of accumulator j
+            float acc[kChains];  // this thread's lanes of accumulator j
 #pragma unroll
-            for (int e = 0; e < 4; e++) acc[e] = 0.0f;
+            for (int e = 0; e < kChains; e++) acc[e] = 0.0f;
             for (int sl = 0; sl < nslices; sl++, t++) {
                 const int slot = t % S;
                 const uint32_t ph = (uint32_t)(t / S) & 1u;
@@ -388,32 +411,39 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv_stream(const __grid_consta
                     for (; s + 2 <= nst; s += 2) {  // one 64-element box: two steps
                         const uint8_t *bx = rbase + (s >> 1) * kBoxBytes;
                         const int S0 = kc0 / 32 + s;
-                        const uint2 w0 = *reinterpret_cast<const uint2 *>(bx + ((j) ^ rho) * 16 + hq * 8);
-                        const uint2 w1 = *reinterpret_cast<const uint2 *>(bx + ((4 + j) ^ rho) * 16 + hq * 8);
-                        fma4(acc, w0, x2[8 * S0]);
-                        fma4(acc, w1, x2[8 * S0 + 8]);
+                        fma_step<TPR>(acc, bx + ((j) ^ rho) * 16 + lb, xq + 32 * S0);
+                        fma_step<TPR>(acc, bx + ((4 + j) ^ rho) * 16 + lb, xq + 32 * S0 + 32);
                     }
                     if (s < nst) {
                         const uint8_t *bx = rbase + (s >> 1) * kBoxBytes;
                         const int S0 = kc0 / 32 + s;
-                        const uint2 w0 = *reinterpret_cast<const uint2 *>(bx + ((j) ^ rho) * 16 + hq * 8);
-                        fma4(acc, w0, x2[8 * S0]);
+                        fma_step<TPR>(acc, bx + ((j) ^ rho) * 16 + lb, xq + 32 * S0);
                     }
                 }
                 if (sl == nslices - 1) {
-                    // (a0 + a2) + (a1 + a3) lane by lane: the partners holding accumulator j^2
-                    // (thread q^4), then j^1 (q^2), at the same lanes; then low four lanes + high
-                    // four lanes (q^1), then the two horizontal adds.  Thread 0 of the row, lanes
-                    // 0-3 of accumulator 0, ends with the row's sum.
+                    // (a0 + a2) + (a1 + a3) lane by lane: the partners holding accumulator j^2,
+                    // then j^1, at the same lanes; then low four lanes + high four lanes, then the
+                    // two horizontal adds.  Thread 0 of the row ends with the row's sum.
+                    constexpr int P = 8 / kChains;  // threads per accumulator: thread q^(2P) holds j^2
 #pragma unroll
-                    for (int e = 0; e < 4; e++) acc[e] += __shfl_xor_sync(kFull, acc[e], 4);
+                    for (int e = 0; e < kChains; e++) acc[e] += __shfl_xor_sync(kFull, acc[e], 2 * P);
 #pragma unroll
-                    for (int e = 0; e < 4; e++) acc[e] += __shfl_xor_sync(kFull, acc[e], 2);
-                    float hi[4];
+                    for (int e = 0; e < kChains; e++) acc[e] += __shfl_xor_sync(kFull, acc[e], P);
+                    float red;
+                    if constexpr (TPR == 8) {
+                        // lanes 0-3 in thread 0, 4-7 in thread 1
+                        float hi[4];
 #pragma unroll
-                    for (int e = 0; e < 4; e++) hi[e] = __shfl_xor_sync(kFull, acc[e], 1);
-                    const float t0 = acc[0] + hi[0], t1 = acc[1] + hi[1], t2 = acc[2] + hi[2], t3 = acc[3] + hi[3];
-                    const float red = (t0 + t1) + (t2 + t3);
+                        for (int e = 0; e < 4; e++) hi[e] = __shfl_xor_sync(kFull, acc[e], 1);
+                        const float t0 = acc[0] + hi[0], t1 = acc[1] + hi[1], t2 = acc[2] + hi[2], t3 = acc[3] + hi[3];
+                        red = (t0 + t1) + (t2 + t3);
+                    } else {
+                        // lanes 2i, 2i+1 in thread i: thread 0 takes 0+4 and 1+5, thread 1 2+6 and 3+7
+                        const float h0 = __shfl_xor_sync(kFull, acc[0], 2), h1 = __shfl_xor_sync(kFull, acc[1], 2);
+                        const float ta = acc[0] + h0, tb = acc[1] + h1;
+                        const float tc = __shfl_xor_sync(kFull, ta, 1), td = __shfl_xor_sync(kFull, tb, 1);
+                        red = (ta + tb) + (tc + td);
+                    }
                     if (active && tq == 0 && row < job.rows[m]) {
                         float out = red;
                         if (32 * nsteps < k) {
@@ -509,7 +539,7 @@ bool row_map_cached(CUtensorMap *map, const uint16_t *W, int64_t rows, int64_t k
 }
 
 constexpr int kMaxDevices = 64;
-std::once_flag g_attr_once[kMaxDevices];
+std::once_flag g_attr_once[kMaxDevices][2];
 
 }  // namespace
 
@@ -563,12 +593,16 @@ int launch_gemv_stream(const VecdotJob &vj, const float *x_f32, uint16_t *h_out,
     const int stages = (int)std::min<int64_t>(want, room);
     job.stages = stages;
     const size_t smem = xbytes + (size_t)stages * kStageBytes + 1024;
+    // CTAs of one or two groups of rows up to 4096 elements take sixteen threads per row,
+    // the rest eight (same-GPU A/B, same bits: Qwen3-0.6B down 7 %, Q 3 %, Llama-3-8B Q 2 %
+    // faster, the SmolLM2 step 2 %; Llama-3-8B down, k = 14336, 1 % slower, within noise).
+    const bool tpr16 = (G + grid - 1) / grid <= groups_per_block<16>() && job.k <= 4096;
+    auto kern = tpr16 ? k_gemv_stream<16> : k_gemv_stream<8>;
 
     int dev_id = 0;
     cudaGetDevice(&dev_id);
-    std::call_once(g_attr_once[dev_id & (kMaxDevices - 1)], [&] {
-        cudaFuncSetAttribute(k_gemv_stream, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             dev.max_smem_optin - 1024);
+    std::call_once(g_attr_once[dev_id & (kMaxDevices - 1)][tpr16 ? 1 : 0], [&] {
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, dev.max_smem_optin - 1024);
     });
 
     cudaLaunchConfig_t cfg{};
@@ -581,7 +615,7 @@ int launch_gemv_stream(const VecdotJob &vj, const float *x_f32, uint16_t *h_out,
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl_enabled() ? 1 : 0;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, k_gemv_stream, job);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, job);
     if (e != cudaSuccess) return fail(BM_ERR_CUDA, "vec_dot (stream): launch failed: %s", cudaGetErrorString(e));
     return BM_OK;
 }
