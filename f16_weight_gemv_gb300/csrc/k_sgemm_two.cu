@@ -1,0 +1,403 @@
+// k_sgemm_two.cu -- two-column products on tinyBLAS's path, bit for bit, streamed the
+// way the one-column kernel streams (k_gemv_stream.cu): rows % 4 == 0, k % 8 == 0.
+//
+// Page "docs/modules/f16.md" (Design notes, "sgemm_dot"): every output
+// Y[c*rows + r] is eight f32 chains -- lane l adds W[r][8t+l] * X[c][8t+l] in
+// increasing t, from +0 -- folded as ((l0+l4)+(l2+l6))+((l1+l5)+(l3+l7)).  The FMA
+// here is the mixed-precision one (fma.rn.f32.f16: f16 operands taken at their exact
+// values, one rounding to f32), which is tinyBLAS's step since the product of two
+// f16 values is exact in f32.
+//
+// Two columns are the product of a two-token decode step, and like one column they
+// are bound by streaming W from HBM.  So this kernel keeps the one-column kernel's
+// machinery and changes only the arithmetic: the 8-row groups of W are split evenly
+// between two CTAs per SM; a CTA walks its groups in sub-blocks and k-slices whose
+// stage holds up to 32 TMA boxes of 8 rows x 64 elements (128-byte swizzle: 16-byte
+// chunk c of row r at chunk c ^ (r % 8)), floor(32 / groups) boxes per group; sixteen
+// lanes of four producer warps issue a stage's boxes, each arriving on the stage's
+// barrier with its own byte count, the weight copies starting before
+// griddepcontrol.wait.  Both activation columns (f16, 4k bytes) are staged once per
+// CTA after the wait.
+//
+// Consumers (eight warps), TPR threads per row:
+//   - TPR = 4: a warp holds one group (8 rows); thread p of a row holds lanes 2p and
+//     2p+1 of both columns' chains and reads, per 8-element step, the 4 bytes at
+//     element 8t + 2p of its row (the row's 16-byte chunk t % 8; the eight rows of a
+//     warp read eight distinct swizzled chunks, one conflict-free wavefront) and the
+//     matching 4 bytes of each column (broadcast);
+//   - TPR = 8 (CTAs of one or two groups, which the 4-thread layout would leave
+//     mostly idle): a warp holds 4 rows, two warps a group; thread l holds lane l of
+//     both columns and reads 2 bytes per step.
+// The fold: xor-shuffles over the row's threads in the order of the page's sum
+// (the partner holding lane l^4, then l^2 (lane pairs), then l^1).
+//
+// Every mbarrier wait is bounded; on a give-up the CTA records BM_ERR_TIMEOUT, drains
+// the copies it issued (bounded) and exits.
+#include "../../include/bm.h"
+#include "bm_device.cuh"
+#include "bm_internal.h"
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <mutex>
+
+namespace bm {
+namespace {
+
+constexpr int kConsumerWarps = 8;
+constexpr int kProducerWarps = 4;
+constexpr int kIssuersPerWarp = 4;
+constexpr int kIssuers = kProducerWarps * kIssuersPerWarp;
+constexpr int kThreads = 32 * (kConsumerWarps + kProducerWarps);
+constexpr int kGroupRows = 8;
+constexpr int kBoxCols = 64;  // 128 bytes: one swizzle row
+constexpr uint32_t kBoxBytes = kGroupRows * kBoxCols * 2;  // 1 KB
+constexpr int kBoxesPerStage = 32;
+constexpr uint32_t kStageBytes = kBoxesPerStage * kBoxBytes;  // 32 KB
+constexpr int kMaxStages = 8;
+constexpr unsigned long long kTimeoutNs = 2000000000ull;
+constexpr unsigned kFull = 0xffffffffu;
+
+template <int TPR>
+__host__ __device__ constexpr int groups_per_block() { return kConsumerWarps * (32 / TPR) / kGroupRows; }
+
+// floor(32 / ng) boxes per group for ng = 1..8, as a byte table.
+__host__ __device__ __forceinline__ int boxes_per_group(int ng)
+{
+    return (int)((0x04040506080A1020ull >> (8 * (ng - 1))) & 0xffu);
+}
+
+struct TwoJob {
+    CUtensorMap map;  // W as [rows][k] 16-bit elements, box 64 x 8, 128-byte swizzle
+    const uint16_t *X;  // [2][k] f16, 16-byte aligned
+    float *Y;           // [2][rows]
+    int rows;
+    int groups;  // ceil(rows / 8)
+    int k;
+    int stages;
+    unsigned int *err;
+    unsigned long long timeout_ns;
+};
+
+// a0 += w.lo * x.lo, a1 += w.hi * x.hi, each rounded once to f32 (exact f16 products).
+__device__ __forceinline__ void fma2(float &a0, float &a1, uint32_t w, uint32_t x)
+{
+    asm("{\n\t.reg .b16 wl, wh, xl, xh;\n\t"
+        "mov.b32 {wl, wh}, %2;\n\t"
+        "mov.b32 {xl, xh}, %3;\n\t"
+        "fma.rn.f32.f16 %0, wl, xl, %0;\n\t"
+        "fma.rn.f32.f16 %1, wh, xh, %1;\n\t}"
+        : "+f"(a0), "+f"(a1)
+        : "r"(w), "r"(x));
+}
+
+// a += w * x, rounded once to f32.
+__device__ __forceinline__ void fma1(float &a, uint16_t w, uint16_t x)
+{
+    asm("fma.rn.f32.f16 %0, %1, %2, %0;" : "+f"(a) : "h"(w), "h"(x));
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int32_t c0, int32_t c1,
+                                            uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+        "[%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void consumers_sync() { asm volatile("bar.sync 1, %0;" ::"n"(32 * kConsumerWarps)); }
+
+template <int TPR>
+__global__ void __launch_bounds__(kThreads, 2) k_sgemm_two(const __grid_constant__ TwoJob job)
+{
+    constexpr int kGroupsPerBlock = groups_per_block<TPR>();
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t full_bar[kMaxStages];
+    __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
+    __shared__ int abort_flag;
+    __shared__ int issued_slot;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int k = job.k;
+    const int S = job.stages;
+    const uint32_t xbytes = (uint32_t)((4 * k + 1023) / 1024 * 1024);  // both columns, f16
+    uint8_t *smem = smem_raw + ((1024u - (dev::smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint16_t *xs = reinterpret_cast<uint16_t *>(smem);  // X[0][0..k), then X[1][0..k)
+    const uint32_t ring_u = dev::smem_u32(smem) + xbytes;
+    volatile int *abort_v = &abort_flag;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; s++) {
+            dev::mbar_init(dev::smem_u32(&full_bar[s]), kIssuers);
+            dev::mbar_init(dev::smem_u32(&empty_bar[s]), kConsumerWarps);
+        }
+        abort_flag = 0;
+        issued_slot = 0;
+        dev::fence_barrier_init();
+    }
+    __syncthreads();
+    dev::pdl_trigger();
+
+    const int G = job.groups;
+    const int glo = (int)((int64_t)G * blockIdx.x / gridDim.x), ghi = (int)((int64_t)G * (blockIdx.x + 1) / gridDim.x);
+    const int nsteps = k >> 3;  // 8-element steps of a row
+
+    if (warp >= kConsumerWarps) {
+        // ------------------------------------------------------------ producers
+        int t = 0;
+        bool ok = true;
+        for (int g = glo; g < ghi && ok;) {
+            const int ng = min(kGroupsPerBlock, ghi - g);
+            const int bpg = boxes_per_group(ng);
+            const int sw = bpg * kBoxCols;
+            const int nslices = (k + sw - 1) / sw;
+            const int32_t row0 = (int32_t)(g * kGroupRows);
+            for (int sl = 0; sl < nslices; sl++, t++) {
+                const int slot = t % S;
+                const uint32_t ph = (uint32_t)(t / S) & 1u;
+                if (!dev::mbar_wait_warp(dev::smem_u32(&empty_bar[slot]), ph ^ 1u, abort_v, job.timeout_ns, job.err)) {
+                    ok = false;
+                    break;
+                }
+                const int kc0 = sl * sw;
+                const int nb = min(bpg, (k - kc0 + kBoxCols - 1) / kBoxCols);
+                if (lane < kIssuersPerWarp) {
+                    const int me = (warp - kConsumerWarps) * kIssuersPerWarp + lane;
+                    const uint32_t fb = dev::smem_u32(&full_bar[slot]);
+                    const uint32_t dst = ring_u + (uint32_t)slot * kStageBytes;
+                    const int nbox = ng * nb;  // <= 32: two per issuer at most
+                    const int mine = (me < nbox ? 1 : 0) + (me + kIssuers < nbox ? 1 : 0);
+                    dev::mbar_expect_tx(fb, (uint32_t)mine * kBoxBytes);
+                    for (int i = me; i < nbox; i += kIssuers) {
+                        const int q = i / nb, b = i % nb;
+                        tma_load_2d(dst + (uint32_t)(q * bpg + b) * kBoxBytes, &job.map, kc0 + b * kBoxCols,
+                                    row0 + q * kGroupRows, fb);
+                    }
+                }
+                if (warp == kConsumerWarps && lane == 0) issued_slot = t + 1;
+            }
+            g += ng;
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ consumers
+        dev::pdl_wait();  // X is the previous kernel's output; Y follows it too
+        {
+            const uint4 *xg = reinterpret_cast<const uint4 *>(job.X);
+            uint4 *xo = reinterpret_cast<uint4 *>(xs);
+            for (int i = threadIdx.x; i < (k >> 2); i += 32 * kConsumerWarps) xo[i] = __ldg(xg + i);  // 2k / 8 chunks
+        }
+        consumers_sync();
+
+        // TPR 4: lanes 4r..4r+3 serve row r of the warp's group, thread p lanes 2p, 2p+1.
+        // TPR 8: lanes 8r..8r+7 serve row (w & 1) * 4 + r of group w / 2, thread l lane l.
+        const int tq = lane % TPR;
+        const int tr = lane / TPR;
+        const int gw = TPR == 4 ? warp : warp >> 1;             // the warp's group in the sub-block
+        const int rho = TPR == 4 ? tr : ((warp & 1) << 2) | tr;  // row in the group
+        const int lb = TPR == 4 ? 4 * tq : 2 * tq;               // byte of the thread's first lane in a chunk
+        const uint16_t *x0 = xs + (TPR == 4 ? 2 * tq : tq);      // column 0, the thread's first lane
+        const uint16_t *x1 = x0 + k;                             // column 1
+        bool ok = true;
+        int t = 0;
+        for (int g = glo; g < ghi && ok;) {
+            const int ng = min(kGroupsPerBlock, ghi - g);
+            const int bpg = boxes_per_group(ng);
+            const int sw = bpg * kBoxCols;
+            const int nslices = (k + sw - 1) / sw;
+            const int row = (g + gw) * kGroupRows + rho;
+            const bool active = gw < ng;  // warp-uniform
+            float a0[2] = {0.0f, 0.0f}, a1[2] = {0.0f, 0.0f};  // [lane] of column 0 and column 1
+            for (int sl = 0; sl < nslices; sl++, t++) {
+                const int slot = t % S;
+                const uint32_t ph = (uint32_t)(t / S) & 1u;
+                if (!dev::mbar_wait_warp(dev::smem_u32(&full_bar[slot]), ph, abort_v, job.timeout_ns, job.err)) {
+                    ok = false;
+                    break;
+                }
+                const int kc0 = sl * sw;
+                const uint8_t *rbase = smem + xbytes + (size_t)slot * kStageBytes + (size_t)(gw * bpg) * kBoxBytes +
+                                       rho * 128 + lb;
+                if (active) {
+                    const int t0 = kc0 >> 3;                      // the slice's first step
+                    const int nst = min(8 * bpg, nsteps - t0);    // steps in this slice
+                    for (int b = 0; b * 8 < nst; b++) {
+                        const uint8_t *bx = rbase + b * kBoxBytes;
+                        const int n = min(8, nst - 8 * b);
+                        const int tb = t0 + 8 * b;
+                        if (n == 8) {
+#pragma unroll
+                            for (int c = 0; c < 8; c++) {
+                                if constexpr (TPR == 4) {
+                                    const uint32_t w = *reinterpret_cast<const uint32_t *>(bx + ((c ^ rho) << 4));
+                                    fma2(a0[0], a0[1], w, *reinterpret_cast<const uint32_t *>(x0 + 8 * (tb + c)));
+                                    fma2(a1[0], a1[1], w, *reinterpret_cast<const uint32_t *>(x1 + 8 * (tb + c)));
+                                } else {
+                                    const uint16_t w = *reinterpret_cast<const uint16_t *>(bx + ((c ^ rho) << 4));
+                                    fma1(a0[0], w, x0[8 * (tb + c)]);
+                                    fma1(a1[0], w, x1[8 * (tb + c)]);
+                                }
+                            }
+                        } else {
+                            for (int c = 0; c < n; c++) {
+                                if constexpr (TPR == 4) {
+                                    const uint32_t w = *reinterpret_cast<const uint32_t *>(bx + ((c ^ rho) << 4));
+                                    fma2(a0[0], a0[1], w, *reinterpret_cast<const uint32_t *>(x0 + 8 * (tb + c)));
+                                    fma2(a1[0], a1[1], w, *reinterpret_cast<const uint32_t *>(x1 + 8 * (tb + c)));
+                                } else {
+                                    const uint16_t w = *reinterpret_cast<const uint16_t *>(bx + ((c ^ rho) << 4));
+                                    fma1(a0[0], w, x0[8 * (tb + c)]);
+                                    fma1(a1[0], w, x1[8 * (tb + c)]);
+                                }
+                            }
+                        }
+                    }
+                }
+                if (sl == nslices - 1) {
+                    // ((l0+l4)+(l2+l6))+((l1+l5)+(l3+l7)) per column; the row's thread 0 stores
+                    // column 0 and its thread 1 column 1
+                    float y0, y1;
+                    if constexpr (TPR == 4) {
+                        // thread p: lanes 2p, 2p+1.  xor 2: (l0+l4, l1+l5) in p = 0, (l2+l6, l3+l7)
+                        // in p = 1; xor 1 then brings the other pair
+                        const float s00 = a0[0] + __shfl_xor_sync(kFull, a0[0], 2);
+                        const float s01 = a0[1] + __shfl_xor_sync(kFull, a0[1], 2);
+                        const float s10 = a1[0] + __shfl_xor_sync(kFull, a1[0], 2);
+                        const float s11 = a1[1] + __shfl_xor_sync(kFull, a1[1], 2);
+                        const float o00 = __shfl_xor_sync(kFull, s00, 1), o01 = __shfl_xor_sync(kFull, s01, 1);
+                        const float o10 = __shfl_xor_sync(kFull, s10, 1), o11 = __shfl_xor_sync(kFull, s11, 1);
+                        y0 = (s00 + o00) + (s01 + o01);
+                        y1 = (s10 + o10) + (s11 + o11);
+                    } else {
+                        // thread l: lane l.  xor 4: l + (l+4); xor 2: (l0+l4)+(l2+l6) in thread 0,
+                        // (l1+l5)+(l3+l7) in thread 1; xor 1: the sum in both
+                        float b0 = a0[0] + __shfl_xor_sync(kFull, a0[0], 4);
+                        float b1 = a1[0] + __shfl_xor_sync(kFull, a1[0], 4);
+                        b0 += __shfl_xor_sync(kFull, b0, 2);
+                        b1 += __shfl_xor_sync(kFull, b1, 2);
+                        y0 = b0 + __shfl_xor_sync(kFull, b0, 1);
+                        y1 = b1 + __shfl_xor_sync(kFull, b1, 1);
+                    }
+                    if (active && row < job.rows) {
+                        if (tq == 0) job.Y[row] = y0;
+                        if (tq == 1) job.Y[(size_t)job.rows + row] = y1;
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) dev::mbar_arrive(dev::smem_u32(&empty_bar[slot]));
+            }
+            g += ng;
+        }
+    }
+
+    // ---------------------------------------------------------------- teardown
+    __syncthreads();
+    if (*abort_v && threadIdx.x == 0) {
+        const int issued = issued_slot;
+        for (int s = 0; s < S && s < issued; s++) {
+            const int last = issued - 1 - ((issued - 1 - s) % S);
+            dev::mbar_drain(dev::smem_u32(&full_bar[s]), (uint32_t)(last / S) & 1u, job.timeout_ns);
+        }
+    }
+    __syncthreads();
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool encoder()
+{
+    std::call_once(g_encode_once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    return g_encode != nullptr;
+}
+
+constexpr int kMaxDevices = 64;
+std::once_flag g_attr_once[kMaxDevices][2];
+
+}  // namespace
+
+bool sgemm_two_applies(const uint16_t *X, int64_t ncols, int64_t k)
+{
+    return ncols == 2 && (reinterpret_cast<uintptr_t>(X) & 15) == 0 && k % 8 == 0 && k <= 0x7fffffffLL / 4;
+}
+
+int launch_sgemm_two(const uint16_t *W, int64_t rows, int64_t k, const uint16_t *X, float *Y, cudaStream_t s,
+                     const DeviceInfo &dev)
+{
+    if (rows % 4 != 0 || k % 8 != 0 || rows > 0x7fffffffLL - 8)
+        return fail(BM_ERR_INVALID_ARG, "sgemm (2 columns): rows %% 4 == 0 and k %% 8 == 0 required");
+    if (rows == 0) return BM_OK;
+    if (!encoder()) return fail(BM_ERR_CUDA, "sgemm (2 columns): cuTensorMapEncodeTiled unavailable");
+    TwoJob job{};
+    {
+        cuuint64_t dims[2] = {(cuuint64_t)k, (cuuint64_t)rows};
+        cuuint64_t strides[1] = {(cuuint64_t)k * 2};
+        cuuint32_t box[2] = {(cuuint32_t)kBoxCols, (cuuint32_t)kGroupRows};
+        cuuint32_t estr[2] = {1, 1};
+        if (g_encode(&job.map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<uint16_t *>(W), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return fail(BM_ERR_CUDA, "sgemm (2 columns): tensor map encoding failed");
+    }
+    job.X = X;
+    job.Y = Y;
+    job.rows = (int)rows;
+    job.groups = (int)((rows + kGroupRows - 1) / kGroupRows);
+    job.k = (int)k;
+    job.err = device_error_word();
+    if (!job.err) return fail(BM_ERR_CUDA, "sgemm (2 columns): device error word unavailable");
+    job.timeout_ns = kTimeoutNs;
+
+    // The one-column kernel's sizing: two CTAs per SM with rings as deep as their share
+    // needs (2..8 stages); one CTA per SM when the staged activation leaves no room for
+    // two stages at two CTAs per SM.
+    const int64_t G = job.groups;
+    const uint32_t xbytes = (uint32_t)((4 * k + 1023) / 1024 * 1024);
+    int64_t grid = std::min<int64_t>((int64_t)dev.sm_count * 2, G);
+    const int64_t groups_per_cta0 = (G + grid - 1) / grid;
+    const int64_t boxes_per_cta = groups_per_cta0 * ((k + kBoxCols - 1) / kBoxCols);
+    const int64_t stages_needed = (boxes_per_cta + kBoxesPerStage - 1) / kBoxesPerStage + 1;
+    const int64_t want = std::max<int64_t>(2, std::min<int64_t>(kMaxStages, stages_needed));
+    int64_t room = ((int64_t)dev.max_smem_optin / 2 - 2048 - 1024 - (int64_t)xbytes) / kStageBytes;
+    if (room < 2) {
+        grid = std::min<int64_t>(grid, dev.sm_count);
+        room = ((int64_t)dev.max_smem_optin - 2048 - 1024 - (int64_t)xbytes) / kStageBytes;
+        if (room < 2) return fail(BM_ERR_UNSUPPORTED_DEVICE, "sgemm (2 columns): too little shared memory");
+    }
+    job.stages = (int)std::min<int64_t>(want, room);
+    const size_t smem = xbytes + (size_t)job.stages * kStageBytes + 1024;
+    const bool tpr8 = (G + grid - 1) / grid <= groups_per_block<8>() / 2;  // one or two groups per CTA
+    auto kern = tpr8 ? k_sgemm_two<8> : k_sgemm_two<4>;
+
+    int dev_id = 0;
+    cudaGetDevice(&dev_id);
+    std::call_once(g_attr_once[dev_id & (kMaxDevices - 1)][tpr8 ? 1 : 0], [&] {
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, dev.max_smem_optin - 1024);
+    });
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_enabled() ? 1 : 0;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, job);
+    if (e != cudaSuccess) return fail(BM_ERR_CUDA, "sgemm (2 columns): launch failed: %s", cudaGetErrorString(e));
+    return BM_OK;
+}
+
+}  // namespace bm
