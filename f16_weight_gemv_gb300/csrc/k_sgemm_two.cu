@@ -19,17 +19,16 @@
 // griddepcontrol.wait.  Both activation columns (f16, 4k bytes) are staged once per
 // CTA after the wait.
 //
-// Consumers (eight warps), TPR threads per row:
-//   - TPR = 4: a warp holds one group (8 rows); thread p of a row holds lanes 2p and
-//     2p+1 of both columns' chains and reads, per 8-element step, the 4 bytes at
-//     element 8t + 2p of its row (the row's 16-byte chunk t % 8; the eight rows of a
-//     warp read eight distinct swizzled chunks, one conflict-free wavefront) and the
-//     matching 4 bytes of each column (broadcast);
-//   - TPR = 8 (CTAs of one or two groups, which the 4-thread layout would leave
-//     mostly idle): a warp holds 4 rows, two warps a group; thread l holds lane l of
-//     both columns and reads 2 bytes per step.
-// The fold: xor-shuffles over the row's threads in the order of the page's sum
-// (the partner holding lane l^4, then l^2 (lane pairs), then l^1).
+// Consumers (eight warps, one group each): thread p of a row holds lanes 2p and 2p+1
+// of both columns' chains and reads, per 8-element step, the 4 bytes at element
+// 8t + 2p of its row (the row's 16-byte chunk t % 8; the eight rows of a warp read
+// eight distinct swizzled chunks, one conflict-free wavefront) and the matching 4
+// bytes of each column (broadcast).  The fold: two xor-shuffles over the row's four
+// threads in the order of the page's sum (lane pairs l, l+4, then the other pairs).
+// Eight threads per row (one lane each, 2-byte reads, two warps per group) kept more
+// warps busy in CTAs of one or two groups but measured no faster there (Llama Q
+// 11.44 us with four threads per row, 11.61 with eight) and sixteen (one column per
+// thread) 30 % slower: 4-byte reads feeding two FMAs each are what this kernel needs.
 //
 // Every mbarrier wait is bounded; on a give-up the CTA records BM_ERR_TIMEOUT, drains
 // the copies it issued (bounded) and exits.
@@ -60,8 +59,7 @@ constexpr int kMaxStages = 8;
 constexpr unsigned long long kTimeoutNs = 2000000000ull;
 constexpr unsigned kFull = 0xffffffffu;
 
-template <int TPR>
-__host__ __device__ constexpr int groups_per_block() { return kConsumerWarps * (32 / TPR) / kGroupRows; }
+constexpr int kGroupsPerBlock = kConsumerWarps;  // sub-block: one group per consumer warp
 
 // floor(32 / ng) boxes per group for ng = 1..8, as a byte table.
 __host__ __device__ __forceinline__ int boxes_per_group(int ng)
@@ -93,12 +91,6 @@ __device__ __forceinline__ void fma2(float &a0, float &a1, uint32_t w, uint32_t 
         : "r"(w), "r"(x));
 }
 
-// a += w * x, rounded once to f32.
-__device__ __forceinline__ void fma1(float &a, uint16_t w, uint16_t x)
-{
-    asm("fma.rn.f32.f16 %0, %1, %2, %0;" : "+f"(a) : "h"(w), "h"(x));
-}
-
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int32_t c0, int32_t c1,
                                             uint32_t bar)
 {
@@ -111,10 +103,8 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
 
 __device__ __forceinline__ void consumers_sync() { asm volatile("bar.sync 1, %0;" ::"n"(32 * kConsumerWarps)); }
 
-template <int TPR>
 __global__ void __launch_bounds__(kThreads, 2) k_sgemm_two(const __grid_constant__ TwoJob job)
 {
-    constexpr int kGroupsPerBlock = groups_per_block<TPR>();
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[kMaxStages];
     __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
@@ -193,15 +183,12 @@ __global__ void __launch_bounds__(kThreads, 2) k_sgemm_two(const __grid_constant
         }
         consumers_sync();
 
-        // TPR 4: lanes 4r..4r+3 serve row r of the warp's group, thread p lanes 2p, 2p+1.
-        // TPR 8: lanes 8r..8r+7 serve row (w & 1) * 4 + r of group w / 2, thread l lane l.
-        const int tq = lane % TPR;
-        const int tr = lane / TPR;
-        const int gw = TPR == 4 ? warp : warp >> 1;             // the warp's group in the sub-block
-        const int rho = TPR == 4 ? tr : ((warp & 1) << 2) | tr;  // row in the group
-        const int lb = TPR == 4 ? 4 * tq : 2 * tq;               // byte of the thread's first lane in a chunk
-        const uint16_t *x0 = xs + (TPR == 4 ? 2 * tq : tq);      // column 0, the thread's first lane
-        const uint16_t *x1 = x0 + k;                             // column 1
+        // lanes 4r..4r+3 serve row r of the warp's group, thread p lanes 2p, 2p+1
+        const int tq = lane & 3;
+        const int rho = lane >> 2;                // row in the group
+        const int gw = warp;                      // the warp's group in the sub-block
+        const uint16_t *x0 = xs + 2 * tq;         // column 0 at the thread's first lane
+        const uint16_t *x1 = x0 + k;              // column 1
         bool ok = true;
         int t = 0;
         for (int g = glo; g < ghi && ok;) {
@@ -221,7 +208,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_sgemm_two(const __grid_constant
                 }
                 const int kc0 = sl * sw;
                 const uint8_t *rbase = smem + xbytes + (size_t)slot * kStageBytes + (size_t)(gw * bpg) * kBoxBytes +
-                                       rho * 128 + lb;
+                                       rho * 128 + 4 * tq;
                 if (active) {
                     const int t0 = kc0 >> 3;                      // the slice's first step
                     const int nst = min(8 * bpg, nsteps - t0);    // steps in this slice
@@ -229,59 +216,34 @@ __global__ void __launch_bounds__(kThreads, 2) k_sgemm_two(const __grid_constant
                         const uint8_t *bx = rbase + b * kBoxBytes;
                         const int n = min(8, nst - 8 * b);
                         const int tb = t0 + 8 * b;
+                        // one 8-element step: the thread's two lanes of the row against both columns
+                        auto step = [&](int c) {
+                            const uint32_t w = *reinterpret_cast<const uint32_t *>(bx + ((c ^ rho) << 4));
+                            const int xo = 8 * (tb + c);
+                            fma2(a0[0], a0[1], w, *reinterpret_cast<const uint32_t *>(x0 + xo));
+                            fma2(a1[0], a1[1], w, *reinterpret_cast<const uint32_t *>(x1 + xo));
+                        };
                         if (n == 8) {
 #pragma unroll
-                            for (int c = 0; c < 8; c++) {
-                                if constexpr (TPR == 4) {
-                                    const uint32_t w = *reinterpret_cast<const uint32_t *>(bx + ((c ^ rho) << 4));
-                                    fma2(a0[0], a0[1], w, *reinterpret_cast<const uint32_t *>(x0 + 8 * (tb + c)));
-                                    fma2(a1[0], a1[1], w, *reinterpret_cast<const uint32_t *>(x1 + 8 * (tb + c)));
-                                } else {
-                                    const uint16_t w = *reinterpret_cast<const uint16_t *>(bx + ((c ^ rho) << 4));
-                                    fma1(a0[0], w, x0[8 * (tb + c)]);
-                                    fma1(a1[0], w, x1[8 * (tb + c)]);
-                                }
-                            }
+                            for (int c = 0; c < 8; c++) step(c);
                         } else {
-                            for (int c = 0; c < n; c++) {
-                                if constexpr (TPR == 4) {
-                                    const uint32_t w = *reinterpret_cast<const uint32_t *>(bx + ((c ^ rho) << 4));
-                                    fma2(a0[0], a0[1], w, *reinterpret_cast<const uint32_t *>(x0 + 8 * (tb + c)));
-                                    fma2(a1[0], a1[1], w, *reinterpret_cast<const uint32_t *>(x1 + 8 * (tb + c)));
-                                } else {
-                                    const uint16_t w = *reinterpret_cast<const uint16_t *>(bx + ((c ^ rho) << 4));
-                                    fma1(a0[0], w, x0[8 * (tb + c)]);
-                                    fma1(a1[0], w, x1[8 * (tb + c)]);
-                                }
-                            }
+                            for (int c = 0; c < n; c++) step(c);
                         }
                     }
                 }
                 if (sl == nslices - 1) {
                     // ((l0+l4)+(l2+l6))+((l1+l5)+(l3+l7)) per column; the row's thread 0 stores
                     // column 0 and its thread 1 column 1
-                    float y0, y1;
-                    if constexpr (TPR == 4) {
-                        // thread p: lanes 2p, 2p+1.  xor 2: (l0+l4, l1+l5) in p = 0, (l2+l6, l3+l7)
-                        // in p = 1; xor 1 then brings the other pair
-                        const float s00 = a0[0] + __shfl_xor_sync(kFull, a0[0], 2);
-                        const float s01 = a0[1] + __shfl_xor_sync(kFull, a0[1], 2);
-                        const float s10 = a1[0] + __shfl_xor_sync(kFull, a1[0], 2);
-                        const float s11 = a1[1] + __shfl_xor_sync(kFull, a1[1], 2);
-                        const float o00 = __shfl_xor_sync(kFull, s00, 1), o01 = __shfl_xor_sync(kFull, s01, 1);
-                        const float o10 = __shfl_xor_sync(kFull, s10, 1), o11 = __shfl_xor_sync(kFull, s11, 1);
-                        y0 = (s00 + o00) + (s01 + o01);
-                        y1 = (s10 + o10) + (s11 + o11);
-                    } else {
-                        // thread l: lane l.  xor 4: l + (l+4); xor 2: (l0+l4)+(l2+l6) in thread 0,
-                        // (l1+l5)+(l3+l7) in thread 1; xor 1: the sum in both
-                        float b0 = a0[0] + __shfl_xor_sync(kFull, a0[0], 4);
-                        float b1 = a1[0] + __shfl_xor_sync(kFull, a1[0], 4);
-                        b0 += __shfl_xor_sync(kFull, b0, 2);
-                        b1 += __shfl_xor_sync(kFull, b1, 2);
-                        y0 = b0 + __shfl_xor_sync(kFull, b0, 1);
-                        y1 = b1 + __shfl_xor_sync(kFull, b1, 1);
-                    }
+                    // xor 2: (l0+l4, l1+l5) in thread 0, (l2+l6, l3+l7) in thread 1; xor 1 then
+                    // brings the other pair
+                    const float s00 = a0[0] + __shfl_xor_sync(kFull, a0[0], 2);
+                    const float s01 = a0[1] + __shfl_xor_sync(kFull, a0[1], 2);
+                    const float s10 = a1[0] + __shfl_xor_sync(kFull, a1[0], 2);
+                    const float s11 = a1[1] + __shfl_xor_sync(kFull, a1[1], 2);
+                    const float o00 = __shfl_xor_sync(kFull, s00, 1), o01 = __shfl_xor_sync(kFull, s01, 1);
+                    const float o10 = __shfl_xor_sync(kFull, s10, 1), o11 = __shfl_xor_sync(kFull, s11, 1);
+                    const float y0 = (s00 + o00) + (s01 + o01);
+                    const float y1 = (s10 + o10) + (s11 + o11);
                     if (active && row < job.rows) {
                         if (tq == 0) job.Y[row] = y0;
                         if (tq == 1) job.Y[(size_t)job.rows + row] = y1;
@@ -323,7 +285,7 @@ bool encoder()
 }
 
 constexpr int kMaxDevices = 64;
-std::once_flag g_attr_once[kMaxDevices][2];
+std::once_flag g_attr_once[kMaxDevices];
 
 }  // namespace
 
@@ -377,13 +339,11 @@ int launch_sgemm_two(const uint16_t *W, int64_t rows, int64_t k, const uint16_t 
     }
     job.stages = (int)std::min<int64_t>(want, room);
     const size_t smem = xbytes + (size_t)job.stages * kStageBytes + 1024;
-    const bool tpr8 = (G + grid - 1) / grid <= groups_per_block<8>() / 2;  // one or two groups per CTA
-    auto kern = tpr8 ? k_sgemm_two<8> : k_sgemm_two<4>;
 
     int dev_id = 0;
     cudaGetDevice(&dev_id);
-    std::call_once(g_attr_once[dev_id & (kMaxDevices - 1)][tpr8 ? 1 : 0], [&] {
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, dev.max_smem_optin - 1024);
+    std::call_once(g_attr_once[dev_id & (kMaxDevices - 1)], [&] {
+        cudaFuncSetAttribute(k_sgemm_two, cudaFuncAttributeMaxDynamicSharedMemorySize, dev.max_smem_optin - 1024);
     });
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3((unsigned)grid);
@@ -395,7 +355,7 @@ int launch_sgemm_two(const uint16_t *W, int64_t rows, int64_t k, const uint16_t 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl_enabled() ? 1 : 0;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, job);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, k_sgemm_two, job);
     if (e != cudaSuccess) return fail(BM_ERR_CUDA, "sgemm (2 columns): launch failed: %s", cudaGetErrorString(e));
     return BM_OK;
 }
