@@ -77,12 +77,12 @@ constexpr int kSgemmStreamMaxCols = 8;
 // element, bit for bit, on the CUDA cores, weights streamed through shared memory by TMA.
 int launch_sgemm_stream(const uint16_t *W, int64_t rows, int64_t k, const uint16_t *X, int64_t ncols, float *Y,
                         cudaStream_t s, const DeviceInfo &dev);
-// The two-column case of launch_sgemm_stream on the one-column kernel's streaming
-// (k_sgemm_two.cu): same bits; taken when sgemm_two_applies (two columns, X 16-byte
-// aligned).
-bool sgemm_two_applies(const uint16_t *X, int64_t ncols, int64_t k);
-int launch_sgemm_two(const uint16_t *W, int64_t rows, int64_t k, const uint16_t *X, float *Y, cudaStream_t s,
-                     const DeviceInfo &dev);
+// launch_sgemm_stream's products on the one-column kernel's streaming (k_sgemm_ring.cu):
+// same bits; taken when sgemm_ring_applies (X 16-byte aligned and small enough to stage
+// whole in shared memory).
+bool sgemm_ring_applies(const uint16_t *X, int64_t ncols, int64_t k, const DeviceInfo &dev);
+int launch_sgemm_ring(const uint16_t *W, int64_t rows, int64_t k, const uint16_t *X, int64_t ncols, float *Y,
+                      cudaStream_t s, const DeviceInfo &dev);
 // Tensor-core product for bm_takes_sgemm shapes (rows % 4 == 0, k % 8 == 0, ncols >= 2).
 int launch_gemm_tc(const uint16_t *W, int64_t rows, int64_t k, const uint16_t *X, int64_t ncols,
                    float *Y, cudaStream_t s, const DeviceInfo &dev);

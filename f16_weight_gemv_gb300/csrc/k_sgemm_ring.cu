@@ -1,5 +1,6 @@
-// k_sgemm_two.cu -- two-column products on tinyBLAS's path, bit for bit, streamed the
-// way the one-column kernel streams (k_gemv_stream.cu): rows % 4 == 0, k % 8 == 0.
+// k_sgemm_ring.cu -- products of 2..8 columns on tinyBLAS's path, bit for bit, streamed
+// the way the one-column kernel streams (k_gemv_stream.cu): rows % 4 == 0, k % 8 == 0,
+// the activation 16-byte aligned and small enough to stage whole in shared memory.
 //
 // Page "docs/modules/f16.md" (Design notes, "sgemm_dot"): every output
 // Y[c*rows + r] is eight f32 chains -- lane l adds W[r][8t+l] * X[c][8t+l] in
@@ -8,23 +9,25 @@
 // values, one rounding to f32), which is tinyBLAS's step since the product of two
 // f16 values is exact in f32.
 //
-// Two columns are the product of a two-token decode step, and like one column they
-// are bound by streaming W from HBM.  So this kernel keeps the one-column kernel's
-// machinery and changes only the arithmetic: the 8-row groups of W are split evenly
+// A few columns (the tokens of a small decode batch) are, like one column, bound by
+// streaming W from HBM.  So this kernel keeps the one-column kernel's machinery and
+// changes only the arithmetic: the 8-row groups of W are split evenly
 // between two CTAs per SM; a CTA walks its groups in sub-blocks and k-slices whose
 // stage holds up to 32 TMA boxes of 8 rows x 64 elements (128-byte swizzle: 16-byte
 // chunk c of row r at chunk c ^ (r % 8)), floor(32 / groups) boxes per group; sixteen
 // lanes of four producer warps issue a stage's boxes, each arriving on the stage's
 // barrier with its own byte count, the weight copies starting before
-// griddepcontrol.wait.  Both activation columns (f16, 4k bytes) are staged once per
-// CTA after the wait.
+// griddepcontrol.wait.  The NC activation columns (ncols rounded up to even; a
+// padding column is zero and never stored; f16, 2 NC k bytes) are staged once per CTA
+// after the wait.
 //
 // Consumers (eight warps, one group each): thread p of a row holds lanes 2p and 2p+1
-// of both columns' chains and reads, per 8-element step, the 4 bytes at element
+// of every column's chains and reads, per 8-element step, the 4 bytes at element
 // 8t + 2p of its row (the row's 16-byte chunk t % 8; the eight rows of a warp read
 // eight distinct swizzled chunks, one conflict-free wavefront) and the matching 4
-// bytes of each column (broadcast).  The fold: two xor-shuffles over the row's four
-// threads in the order of the page's sum (lane pairs l, l+4, then the other pairs).
+// bytes of each column (broadcast), then issues one FMA pair per column.  The fold:
+// two xor-shuffles over the row's four threads in the order of the page's sum (lane
+// pairs l, l+4, then the other pairs); thread c % 4 stores column c.
 // Eight threads per row (one lane each, 2-byte reads, two warps per group) kept more
 // warps busy in CTAs of one or two groups but measured no faster there (Llama Q
 // 11.44 us with four threads per row, 11.61 with eight) and sixteen (one column per
@@ -67,10 +70,11 @@ __host__ __device__ __forceinline__ int boxes_per_group(int ng)
     return (int)((0x04040506080A1020ull >> (8 * (ng - 1))) & 0xffu);
 }
 
-struct TwoJob {
+struct RingJob {
     CUtensorMap map;  // W as [rows][k] 16-bit elements, box 64 x 8, 128-byte swizzle
-    const uint16_t *X;  // [2][k] f16, 16-byte aligned
-    float *Y;           // [2][rows]
+    const uint16_t *X;  // [ncols][k] f16, 16-byte aligned
+    float *Y;           // [ncols][rows]
+    int ncols;
     int rows;
     int groups;  // ceil(rows / 8)
     int k;
@@ -103,7 +107,11 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
 
 __device__ __forceinline__ void consumers_sync() { asm volatile("bar.sync 1, %0;" ::"n"(32 * kConsumerWarps)); }
 
-__global__ void __launch_bounds__(kThreads, 2) k_sgemm_two(const __grid_constant__ TwoJob job)
+// Shared memory of the staged activation: NC columns of k f16, whole KB.
+__host__ __device__ constexpr uint32_t x_bytes(int nc, int64_t k) { return (uint32_t)((2 * nc * k + 1023) / 1024 * 1024); }
+
+template <int NC>
+__global__ void __launch_bounds__(kThreads, 2) k_sgemm_ring(const __grid_constant__ RingJob job)
 {
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[kMaxStages];
@@ -114,9 +122,9 @@ __global__ void __launch_bounds__(kThreads, 2) k_sgemm_two(const __grid_constant
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int k = job.k;
     const int S = job.stages;
-    const uint32_t xbytes = (uint32_t)((4 * k + 1023) / 1024 * 1024);  // both columns, f16
+    const uint32_t xbytes = x_bytes(NC, k);
     uint8_t *smem = smem_raw + ((1024u - (dev::smem_u32(smem_raw) & 1023u)) & 1023u);
-    uint16_t *xs = reinterpret_cast<uint16_t *>(smem);  // X[0][0..k), then X[1][0..k)
+    uint16_t *xs = reinterpret_cast<uint16_t *>(smem);  // X[c][0..k) at xs + c k
     const uint32_t ring_u = dev::smem_u32(smem) + xbytes;
     volatile int *abort_v = &abort_flag;
 
@@ -179,7 +187,9 @@ __global__ void __launch_bounds__(kThreads, 2) k_sgemm_two(const __grid_constant
         {
             const uint4 *xg = reinterpret_cast<const uint4 *>(job.X);
             uint4 *xo = reinterpret_cast<uint4 *>(xs);
-            for (int i = threadIdx.x; i < (k >> 2); i += 32 * kConsumerWarps) xo[i] = __ldg(xg + i);  // 2k / 8 chunks
+            const int nreal = job.ncols * (k >> 3), nall = NC * (k >> 3);  // 16-byte chunks
+            for (int i = threadIdx.x; i < nall; i += 32 * kConsumerWarps)
+                xo[i] = i < nreal ? __ldg(xg + i) : make_uint4(0u, 0u, 0u, 0u);
         }
         consumers_sync();
 
@@ -187,8 +197,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_sgemm_two(const __grid_constant
         const int tq = lane & 3;
         const int rho = lane >> 2;                // row in the group
         const int gw = warp;                      // the warp's group in the sub-block
-        const uint16_t *x0 = xs + 2 * tq;         // column 0 at the thread's first lane
-        const uint16_t *x1 = x0 + k;              // column 1
+        const uint16_t *x0 = xs + 2 * tq;         // column 0 at the thread's first lane; column c at + c k
         bool ok = true;
         int t = 0;
         for (int g = glo; g < ghi && ok;) {
@@ -198,7 +207,9 @@ __global__ void __launch_bounds__(kThreads, 2) k_sgemm_two(const __grid_constant
             const int nslices = (k + sw - 1) / sw;
             const int row = (g + gw) * kGroupRows + rho;
             const bool active = gw < ng;  // warp-uniform
-            float a0[2] = {0.0f, 0.0f}, a1[2] = {0.0f, 0.0f};  // [lane] of column 0 and column 1
+            float acc[NC][2];  // [column][lane]
+#pragma unroll
+            for (int c = 0; c < NC; c++) acc[c][0] = acc[c][1] = 0.0f;
             for (int sl = 0; sl < nslices; sl++, t++) {
                 const int slot = t % S;
                 const uint32_t ph = (uint32_t)(t / S) & 1u;
@@ -216,12 +227,13 @@ __global__ void __launch_bounds__(kThreads, 2) k_sgemm_two(const __grid_constant
                         const uint8_t *bx = rbase + b * kBoxBytes;
                         const int n = min(8, nst - 8 * b);
                         const int tb = t0 + 8 * b;
-                        // one 8-element step: the thread's two lanes of the row against both columns
+                        // one 8-element step: the thread's two lanes of the row against every column
                         auto step = [&](int c) {
                             const uint32_t w = *reinterpret_cast<const uint32_t *>(bx + ((c ^ rho) << 4));
-                            const int xo = 8 * (tb + c);
-                            fma2(a0[0], a0[1], w, *reinterpret_cast<const uint32_t *>(x0 + xo));
-                            fma2(a1[0], a1[1], w, *reinterpret_cast<const uint32_t *>(x1 + xo));
+                            const uint16_t *xc = x0 + 8 * (tb + c);
+#pragma unroll
+                            for (int q = 0; q < NC; q++)
+                                fma2(acc[q][0], acc[q][1], w, *reinterpret_cast<const uint32_t *>(xc + (size_t)q * k));
                         };
                         if (n == 8) {
 #pragma unroll
@@ -232,21 +244,16 @@ __global__ void __launch_bounds__(kThreads, 2) k_sgemm_two(const __grid_constant
                     }
                 }
                 if (sl == nslices - 1) {
-                    // ((l0+l4)+(l2+l6))+((l1+l5)+(l3+l7)) per column; the row's thread 0 stores
-                    // column 0 and its thread 1 column 1
-                    // xor 2: (l0+l4, l1+l5) in thread 0, (l2+l6, l3+l7) in thread 1; xor 1 then
-                    // brings the other pair
-                    const float s00 = a0[0] + __shfl_xor_sync(kFull, a0[0], 2);
-                    const float s01 = a0[1] + __shfl_xor_sync(kFull, a0[1], 2);
-                    const float s10 = a1[0] + __shfl_xor_sync(kFull, a1[0], 2);
-                    const float s11 = a1[1] + __shfl_xor_sync(kFull, a1[1], 2);
-                    const float o00 = __shfl_xor_sync(kFull, s00, 1), o01 = __shfl_xor_sync(kFull, s01, 1);
-                    const float o10 = __shfl_xor_sync(kFull, s10, 1), o11 = __shfl_xor_sync(kFull, s11, 1);
-                    const float y0 = (s00 + o00) + (s01 + o01);
-                    const float y1 = (s10 + o10) + (s11 + o11);
-                    if (active && row < job.rows) {
-                        if (tq == 0) job.Y[row] = y0;
-                        if (tq == 1) job.Y[(size_t)job.rows + row] = y1;
+                    // ((l0+l4)+(l2+l6))+((l1+l5)+(l3+l7)) per column: xor 2 gives (l0+l4, l1+l5) in thread 0, (l2+l6, l3+l7) in thread 1
+                    // (and the same sums in threads 2, 3); xor 1 then brings the other pair
+#pragma unroll
+                    for (int c = 0; c < NC; c++) {
+                        const float s0 = acc[c][0] + __shfl_xor_sync(kFull, acc[c][0], 2);
+                        const float s1 = acc[c][1] + __shfl_xor_sync(kFull, acc[c][1], 2);
+                        const float o0 = __shfl_xor_sync(kFull, s0, 1), o1 = __shfl_xor_sync(kFull, s1, 1);
+                        const float y = (s0 + o0) + (s1 + o1);
+                        if (active && row < job.rows && tq == (c & 3) && c < job.ncols)
+                            job.Y[(size_t)c * job.rows + row] = y;
                     }
                 }
                 __syncwarp();
@@ -285,65 +292,48 @@ bool encoder()
 }
 
 constexpr int kMaxDevices = 64;
-std::once_flag g_attr_once[kMaxDevices];
+std::once_flag g_attr_once[kMaxDevices][4];
 
 }  // namespace
 
-bool sgemm_two_applies(const uint16_t *X, int64_t ncols, int64_t k)
+bool sgemm_ring_applies(const uint16_t *X, int64_t ncols, int64_t k, const DeviceInfo &dev)
 {
-    return ncols == 2 && (reinterpret_cast<uintptr_t>(X) & 15) == 0 && k % 8 == 0 && k <= 0x7fffffffLL / 4;
+    if (ncols < 2 || ncols > kSgemmStreamMaxCols || k % 8 != 0 || (reinterpret_cast<uintptr_t>(X) & 15) != 0)
+        return false;
+    const int64_t nc = (ncols + 1) / 2 * 2;
+    // the staged activation and two stages must fit one CTA per SM
+    return (int64_t)x_bytes((int)nc, k) + 2 * (int64_t)kStageBytes + 2048 + 1024 <= (int64_t)dev.max_smem_optin;
 }
 
-int launch_sgemm_two(const uint16_t *W, int64_t rows, int64_t k, const uint16_t *X, float *Y, cudaStream_t s,
-                     const DeviceInfo &dev)
-{
-    if (rows % 4 != 0 || k % 8 != 0 || rows > 0x7fffffffLL - 8)
-        return fail(BM_ERR_INVALID_ARG, "sgemm (2 columns): rows %% 4 == 0 and k %% 8 == 0 required");
-    if (rows == 0) return BM_OK;
-    if (!encoder()) return fail(BM_ERR_CUDA, "sgemm (2 columns): cuTensorMapEncodeTiled unavailable");
-    TwoJob job{};
-    {
-        cuuint64_t dims[2] = {(cuuint64_t)k, (cuuint64_t)rows};
-        cuuint64_t strides[1] = {(cuuint64_t)k * 2};
-        cuuint32_t box[2] = {(cuuint32_t)kBoxCols, (cuuint32_t)kGroupRows};
-        cuuint32_t estr[2] = {1, 1};
-        if (g_encode(&job.map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<uint16_t *>(W), dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return fail(BM_ERR_CUDA, "sgemm (2 columns): tensor map encoding failed");
-    }
-    job.X = X;
-    job.Y = Y;
-    job.rows = (int)rows;
-    job.groups = (int)((rows + kGroupRows - 1) / kGroupRows);
-    job.k = (int)k;
-    job.err = device_error_word();
-    if (!job.err) return fail(BM_ERR_CUDA, "sgemm (2 columns): device error word unavailable");
-    job.timeout_ns = kTimeoutNs;
+namespace {
 
+template <int NC>
+int launch_nc(RingJob &job, cudaStream_t s, const DeviceInfo &dev)
+{
+    auto kern = k_sgemm_ring<NC>;
     // The one-column kernel's sizing: two CTAs per SM with rings as deep as their share
     // needs (2..8 stages); one CTA per SM when the staged activation leaves no room for
     // two stages at two CTAs per SM.
-    const int64_t G = job.groups;
-    const uint32_t xbytes = (uint32_t)((4 * k + 1023) / 1024 * 1024);
+    const int64_t G = job.groups, k = job.k;
+    const uint32_t xbytes = x_bytes(NC, k);
     int64_t grid = std::min<int64_t>((int64_t)dev.sm_count * 2, G);
-    const int64_t groups_per_cta0 = (G + grid - 1) / grid;
-    const int64_t boxes_per_cta = groups_per_cta0 * ((k + kBoxCols - 1) / kBoxCols);
+    const int64_t groups_per_cta = (G + grid - 1) / grid;
+    const int64_t boxes_per_cta = groups_per_cta * ((k + kBoxCols - 1) / kBoxCols);
     const int64_t stages_needed = (boxes_per_cta + kBoxesPerStage - 1) / kBoxesPerStage + 1;
     const int64_t want = std::max<int64_t>(2, std::min<int64_t>(kMaxStages, stages_needed));
     int64_t room = ((int64_t)dev.max_smem_optin / 2 - 2048 - 1024 - (int64_t)xbytes) / kStageBytes;
     if (room < 2) {
         grid = std::min<int64_t>(grid, dev.sm_count);
         room = ((int64_t)dev.max_smem_optin - 2048 - 1024 - (int64_t)xbytes) / kStageBytes;
-        if (room < 2) return fail(BM_ERR_UNSUPPORTED_DEVICE, "sgemm (2 columns): too little shared memory");
+        if (room < 2) return fail(BM_ERR_UNSUPPORTED_DEVICE, "sgemm ring: too little shared memory");
     }
     job.stages = (int)std::min<int64_t>(want, room);
     const size_t smem = xbytes + (size_t)job.stages * kStageBytes + 1024;
 
     int dev_id = 0;
     cudaGetDevice(&dev_id);
-    std::call_once(g_attr_once[dev_id & (kMaxDevices - 1)], [&] {
-        cudaFuncSetAttribute(k_sgemm_two, cudaFuncAttributeMaxDynamicSharedMemorySize, dev.max_smem_optin - 1024);
+    std::call_once(g_attr_once[dev_id & (kMaxDevices - 1)][NC / 2 - 1], [&] {
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, dev.max_smem_optin - 1024);
     });
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3((unsigned)grid);
@@ -355,9 +345,47 @@ int launch_sgemm_two(const uint16_t *W, int64_t rows, int64_t k, const uint16_t 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl_enabled() ? 1 : 0;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, k_sgemm_two, job);
-    if (e != cudaSuccess) return fail(BM_ERR_CUDA, "sgemm (2 columns): launch failed: %s", cudaGetErrorString(e));
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, job);
+    if (e != cudaSuccess) return fail(BM_ERR_CUDA, "sgemm ring: launch failed: %s", cudaGetErrorString(e));
     return BM_OK;
+}
+
+}  // namespace
+
+int launch_sgemm_ring(const uint16_t *W, int64_t rows, int64_t k, const uint16_t *X, int64_t ncols, float *Y,
+                      cudaStream_t s, const DeviceInfo &dev)
+{
+    if (rows % 4 != 0 || k % 8 != 0 || rows > 0x7fffffffLL - 8 || k > 0x7fffffffLL / 16 || ncols < 2 ||
+        ncols > kSgemmStreamMaxCols)
+        return fail(BM_ERR_INVALID_ARG, "sgemm ring: 2..8 columns, rows %% 4 == 0 and k %% 8 == 0 required");
+    if (rows == 0) return BM_OK;
+    if (!encoder()) return fail(BM_ERR_CUDA, "sgemm ring: cuTensorMapEncodeTiled unavailable");
+    RingJob job{};
+    {
+        cuuint64_t dims[2] = {(cuuint64_t)k, (cuuint64_t)rows};
+        cuuint64_t strides[1] = {(cuuint64_t)k * 2};
+        cuuint32_t box[2] = {(cuuint32_t)kBoxCols, (cuuint32_t)kGroupRows};
+        cuuint32_t estr[2] = {1, 1};
+        if (g_encode(&job.map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<uint16_t *>(W), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return fail(BM_ERR_CUDA, "sgemm ring: tensor map encoding failed");
+    }
+    job.X = X;
+    job.Y = Y;
+    job.ncols = (int)ncols;
+    job.rows = (int)rows;
+    job.groups = (int)((rows + kGroupRows - 1) / kGroupRows);
+    job.k = (int)k;
+    job.err = device_error_word();
+    if (!job.err) return fail(BM_ERR_CUDA, "sgemm ring: device error word unavailable");
+    job.timeout_ns = kTimeoutNs;
+    switch ((ncols + 1) / 2 * 2) {
+    case 2: return launch_nc<2>(job, s, dev);
+    case 4: return launch_nc<4>(job, s, dev);
+    case 6: return launch_nc<6>(job, s, dev);
+    default: return launch_nc<8>(job, s, dev);
+    }
 }
 
 }  // namespace bm

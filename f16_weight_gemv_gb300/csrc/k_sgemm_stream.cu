@@ -489,7 +489,7 @@ int launch_sgemm_stream(const uint16_t *W, int64_t rows, int64_t k, const uint16
         return fail(BM_ERR_INVALID_ARG, "sgemm stream: shape outside 2..8 columns, rows %% 4 == 0, k %% 8 == 0");
     if (rows == 0) return BM_OK;
     if (rows > 0x7fffffffLL || k > 0x7fffffffLL) return fail(BM_ERR_INVALID_ARG, "sgemm stream: size too large");
-    if (sgemm_two_applies(X, ncols, k)) return launch_sgemm_two(W, rows, k, X, Y, s, dev);
+    if (sgemm_ring_applies(X, ncols, k, dev)) return launch_sgemm_ring(W, rows, k, X, ncols, Y, s, dev);
     if (!encoder()) return fail(BM_ERR_CUDA, "sgemm stream: cuTensorMapEncodeTiled unavailable");
     const int ncp = (int)((ncols + 1) / 2 * 2);  // columns per thread, rounded up to even
     SgemmJob job{};
