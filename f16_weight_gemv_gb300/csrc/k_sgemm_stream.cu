@@ -1,5 +1,8 @@
 // k_sgemm_stream.cu -- products of 2..8 columns on tinyBLAS's path, bit for bit,
-// for the shapes bm_takes_sgemm accepts (rows % 4 == 0, k % 8 == 0).
+// for the shapes bm_takes_sgemm accepts (rows % 4 == 0, k % 8 == 0) whose activation
+// is too long to stage whole in shared memory (k_sgemm_ring.cu takes the others: it
+// streams like the one-column product and is faster); here the activation travels
+// with the weights, slice by slice.
 //
 // Page "docs/modules/f16.md" (Design notes, "sgemm_dot"): every output
 // Y[c*rows + r] is eight f32 chains -- lane l adds W[r][8t+l] * X[c][8t+l] in

@@ -1,5 +1,7 @@
-"""GPU parity of the CUDA-core tinyBLAS kernel (bm_takes_sgemm shapes of 2..8
-columns, with bm_set_exact_sgemm_cols(8)) against the oracle, bit for bit.
+"""GPU parity of the CUDA-core tinyBLAS kernels (bm_takes_sgemm shapes of 2..8
+columns, with bm_set_exact_sgemm_cols(8)) against the oracle, bit for bit: k_sgemm_ring
+where the activation fits in shared memory (most shapes here), k_sgemm_stream where it
+does not (1024 x 14336 at 7 columns, 8 x 65536 at 5).
 
 Each output of these products is tinyBLAS's sgemm_dot (page f16.md, "Design
 notes", "sgemm_dot"): eight lane chains in increasing t, folded
