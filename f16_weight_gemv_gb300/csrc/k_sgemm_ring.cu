@@ -95,6 +95,15 @@ __device__ __forceinline__ void fma2(float &a0, float &a1, uint32_t w, uint32_t 
         : "r"(w), "r"(x));
 }
 
+// 4 bytes of shared memory at a shared-window address.  (volatile: never moved across
+// the barrier waits, which are volatile too.)
+__device__ __forceinline__ uint32_t lds32(uint32_t addr)
+{
+    uint32_t v;
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int32_t c0, int32_t c1,
                                             uint32_t bar)
 {
@@ -124,7 +133,8 @@ __global__ void __launch_bounds__(kThreads, 2) k_sgemm_ring(const __grid_constan
     const int S = job.stages;
     const uint32_t xbytes = x_bytes(NC, k);
     uint8_t *smem = smem_raw + ((1024u - (dev::smem_u32(smem_raw) & 1023u)) & 1023u);
-    uint16_t *xs = reinterpret_cast<uint16_t *>(smem);  // X[c][0..k) at xs + c k
+    // the activation step-major: the 8 elements of step t of column c at 16 (t NC + c) bytes
+    uint16_t *xs = reinterpret_cast<uint16_t *>(smem);
     const uint32_t ring_u = dev::smem_u32(smem) + xbytes;
     volatile int *abort_v = &abort_flag;
 
@@ -187,9 +197,11 @@ __global__ void __launch_bounds__(kThreads, 2) k_sgemm_ring(const __grid_constan
         {
             const uint4 *xg = reinterpret_cast<const uint4 *>(job.X);
             uint4 *xo = reinterpret_cast<uint4 *>(xs);
-            const int nreal = job.ncols * (k >> 3), nall = NC * (k >> 3);  // 16-byte chunks
-            for (int i = threadIdx.x; i < nall; i += 32 * kConsumerWarps)
-                xo[i] = i < nreal ? __ldg(xg + i) : make_uint4(0u, 0u, 0u, 0u);
+            const int k8 = k >> 3;  // 16-byte chunks per column
+            for (int i = threadIdx.x; i < NC * k8; i += 32 * kConsumerWarps) {
+                const int ts = i / NC, c = i % NC;  // destination: step ts of column c
+                xo[i] = c < job.ncols ? __ldg(xg + (size_t)c * k8 + ts) : make_uint4(0u, 0u, 0u, 0u);
+            }
         }
         consumers_sync();
 
@@ -197,7 +209,11 @@ __global__ void __launch_bounds__(kThreads, 2) k_sgemm_ring(const __grid_constan
         const int tq = lane & 3;
         const int rho = lane >> 2;                // row in the group
         const int gw = warp;                      // the warp's group in the sub-block
-        const uint16_t *x0 = xs + 2 * tq;         // column 0 at the thread's first lane; column c at + c k
+        // Shared-window addresses.  The word of step c of a box (chunk c of the row, swizzled to
+        // chunk c ^ rho) is at w ^ (c << 4) for w = the row's 128-byte base | rho << 4 | 4 tq:
+        // the base's low 7 bits are zero, so the XOR swaps exactly the chunk bits.  Column q of
+        // step t is at x + 16 (t NC + q), an immediate offset once t is the box's first step.
+        const uint32_t xthr = dev::smem_u32(xs) + 4 * tq;
         bool ok = true;
         int t = 0;
         for (int g = glo; g < ghi && ok;) {
@@ -218,22 +234,22 @@ __global__ void __launch_bounds__(kThreads, 2) k_sgemm_ring(const __grid_constan
                     break;
                 }
                 const int kc0 = sl * sw;
-                const uint8_t *rbase = smem + xbytes + (size_t)slot * kStageBytes + (size_t)(gw * bpg) * kBoxBytes +
-                                       rho * 128 + 4 * tq;
+                const uint32_t wrow = dev::smem_u32(smem) + xbytes + (uint32_t)slot * kStageBytes +
+                                      (uint32_t)(gw * bpg) * kBoxBytes + (uint32_t)rho * 128;
+                const uint32_t wthr = wrow | ((uint32_t)rho << 4) | (uint32_t)(4 * tq);
                 if (active) {
                     const int t0 = kc0 >> 3;                      // the slice's first step
                     const int nst = min(8 * bpg, nsteps - t0);    // steps in this slice
                     for (int b = 0; b * 8 < nst; b++) {
-                        const uint8_t *bx = rbase + b * kBoxBytes;
+                        const uint32_t wb = wthr + (uint32_t)b * kBoxBytes;
+                        const uint32_t xb = xthr + (uint32_t)(t0 + 8 * b) * (NC * 16);
                         const int n = min(8, nst - 8 * b);
-                        const int tb = t0 + 8 * b;
                         // one 8-element step: the thread's two lanes of the row against every column
                         auto step = [&](int c) {
-                            const uint32_t w = *reinterpret_cast<const uint32_t *>(bx + ((c ^ rho) << 4));
-                            const uint16_t *xc = x0 + 8 * (tb + c);
+                            const uint32_t w = lds32(wb ^ ((uint32_t)c << 4));
 #pragma unroll
                             for (int q = 0; q < NC; q++)
-                                fma2(acc[q][0], acc[q][1], w, *reinterpret_cast<const uint32_t *>(xc + (size_t)q * k));
+                                fma2(acc[q][0], acc[q][1], w, lds32(xb + (uint32_t)(16 * (c * NC + q))));
                         };
                         if (n == 8) {
 #pragma unroll
