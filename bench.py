@@ -120,10 +120,10 @@ def algorithmic_bytes(rows, k, ncols=1):
 # measured on (sha256 prefix of k_gemv_stream.cu).  Shapes per launch do not depend on
 # the number of layers, so the full step's traffic is these, summed over its launches.
 NCU_TRAFFIC = {"kernel": "k_gemv_stream", "source": "f16_weight_gemv_gb300/csrc/k_gemv_stream.cu",
-               "sha256_16": "fd7df63e9dea0a28",
-               "bytes_per_call": {"4096x4096+1024x4096+1024x4096": 50417792, "4096x4096": 33637248,
-                                  "14336x4096+14336x4096": 235104128, "4096x14336": 117814528,
-                                  "128256x4096": 1051352064}}
+               "sha256_16": "ab91cb641fe613cf",
+               "bytes_per_call": {"4096x4096+1024x4096+1024x4096": 50420864, "4096x4096": 33638912,
+                                  "14336x4096+14336x4096": 235086592, "4096x14336": 117655552,
+                                  "128256x4096": 1051435264}}
 
 
 # DRAM traffic of the prefill layer's four k_gemm_tc launches (Q/K/V, O, gate/up, down; read +

@@ -328,25 +328,59 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv_stream(const __grid_consta
                     if (job.h_out && blockIdx.x == 0) reinterpret_cast<uint2 *>(job.h_out)[c] = p;
                 }
             }
-        } else if (job.x_is_f32) {
+        } else if (job.x_is_f32 && !job.g) {
+            // longer rows, no norm: this thread's loads in batches of eight, each batch in flight
+            // before its first conversion (a load, convert, store loop made one L2 round trip per
+            // 16 bytes: 14 in a row at k = 14336)
             const float4 *xf = reinterpret_cast<const float4 *>(job.x);
             uint2 *xo = reinterpret_cast<uint2 *>(xs);
-            float scale = 1.0f;
-            if (job.g) {  // longer rows: x read once for the sum, once more for the values
-                scale = norm::row_scale(static_cast<const float *>(job.x), k, job.rk, job.eps, true, threadIdx.x,
-                                        norm_sh, [] { consumers_sync(); });
-            }
-            for (int i = threadIdx.x; i < (k >> 2); i += 32 * kConsumerWarps) {
-                float4 v = __ldg(xf + i);
-                if (job.g) {
-                    const float4 w = __ldg(reinterpret_cast<const float4 *>(job.g) + i);
-                    v = make_float4(norm::apply(v.x, scale, w.x), norm::apply(v.y, scale, w.y),
-                                    norm::apply(v.z, scale, w.z), norm::apply(v.w, scale, w.w));
-                    if (job.n_out && blockIdx.x == 0) reinterpret_cast<float4 *>(job.n_out)[i] = v;
+            constexpr int kBatch = 8;
+            for (int i0 = threadIdx.x; i0 < n4; i0 += kBatch * kNormThreadsC) {
+                float4 v[kBatch];
+#pragma unroll
+                for (int u = 0; u < kBatch; u++) {
+                    const int i = i0 + u * kNormThreadsC;
+                    v[u] = i < n4 ? __ldg(xf + i) : make_float4(0.f, 0.f, 0.f, 0.f);
                 }
-                const uint2 p = make_uint2(pack_rn(v.x, v.y), pack_rn(v.z, v.w));
-                xo[i] = p;
-                if (job.h_out && blockIdx.x == 0) reinterpret_cast<uint2 *>(job.h_out)[i] = p;
+#pragma unroll
+                for (int u = 0; u < kBatch; u++) {
+                    const int i = i0 + u * kNormThreadsC;
+                    if (i < n4) {
+                        const uint2 p = make_uint2(pack_rn(v[u].x, v[u].y), pack_rn(v[u].z, v[u].w));
+                        xo[i] = p;
+                        if (job.h_out && blockIdx.x == 0) reinterpret_cast<uint2 *>(job.h_out)[i] = p;
+                    }
+                }
+            }
+        } else if (job.x_is_f32) {
+            // longer rows with the norm: x read once for the sum, once more for the values, the
+            // second pass in batches of four (x and g) in flight before their first use
+            const float4 *xf = reinterpret_cast<const float4 *>(job.x);
+            const float4 *gf = reinterpret_cast<const float4 *>(job.g);
+            uint2 *xo = reinterpret_cast<uint2 *>(xs);
+            const float scale = norm::row_scale(static_cast<const float *>(job.x), k, job.rk, job.eps, true,
+                                                threadIdx.x, norm_sh, [] { consumers_sync(); });
+            constexpr int kBatch = 4;
+            for (int i0 = threadIdx.x; i0 < n4; i0 += kBatch * kNormThreadsC) {
+                float4 v[kBatch], w[kBatch];
+#pragma unroll
+                for (int u = 0; u < kBatch; u++) {
+                    const int i = i0 + u * kNormThreadsC;
+                    v[u] = i < n4 ? __ldg(xf + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    w[u] = i < n4 ? __ldg(gf + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+#pragma unroll
+                for (int u = 0; u < kBatch; u++) {
+                    const int i = i0 + u * kNormThreadsC;
+                    if (i < n4) {
+                        const float4 o = make_float4(norm::apply(v[u].x, scale, w[u].x), norm::apply(v[u].y, scale, w[u].y),
+                                                     norm::apply(v[u].z, scale, w[u].z), norm::apply(v[u].w, scale, w[u].w));
+                        if (job.n_out && blockIdx.x == 0) reinterpret_cast<float4 *>(job.n_out)[i] = o;
+                        const uint2 p = make_uint2(pack_rn(o.x, o.y), pack_rn(o.z, o.w));
+                        xo[i] = p;
+                        if (job.h_out && blockIdx.x == 0) reinterpret_cast<uint2 *>(job.h_out)[i] = p;
+                    }
+                }
             }
         } else {
             const uint4 *xg = reinterpret_cast<const uint4 *>(job.x);
