@@ -226,8 +226,22 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv_bulk(const __grid_constant
         // ------------------------------------------------------------ consumers
         dev::pdl_wait();  // the activation is the previous kernel's output; outputs follow too
         const uint4 *xg = reinterpret_cast<const uint4 *>(job.x);
-        for (int64_t i = threadIdx.x; i < nchunk; i += 32 * kConsumerWarps)
-            xs4[i] = 8 * i + 8 <= k ? __ldg(xg + i) : ld_direct(job.x, 8 * i, k);
+        {
+            // in batches of eight loads, all in flight before the first store
+            constexpr int kBatch = 8, kT = 32 * kConsumerWarps;
+            for (int64_t i0 = threadIdx.x; i0 < nchunk; i0 += kBatch * kT) {
+                uint4 h[kBatch];
+#pragma unroll
+                for (int u = 0; u < kBatch; u++) {
+                    const int64_t i = i0 + u * kT;
+                    h[u] = i >= nchunk ? make_uint4(0u, 0u, 0u, 0u)
+                                       : 8 * i + 8 <= k ? __ldg(xg + i) : ld_direct(job.x, 8 * i, k);
+                }
+#pragma unroll
+                for (int u = 0; u < kBatch; u++)
+                    if (i0 + u * kT < nchunk) xs4[i0 + u * kT] = h[u];
+            }
+        }
         consumers_sync();
 
         const int j = lane & 3, tr = lane >> 2;  // accumulator j; row tr of the group

@@ -198,9 +198,19 @@ __global__ void __launch_bounds__(kThreads, 2) k_sgemm_ring(const __grid_constan
             const uint4 *xg = reinterpret_cast<const uint4 *>(job.X);
             uint4 *xo = reinterpret_cast<uint4 *>(xs);
             const int k8 = k >> 3;  // 16-byte chunks per column
-            for (int i = threadIdx.x; i < NC * k8; i += 32 * kConsumerWarps) {
-                const int ts = i / NC, c = i % NC;  // destination: step ts of column c
-                xo[i] = c < job.ncols ? __ldg(xg + (size_t)c * k8 + ts) : make_uint4(0u, 0u, 0u, 0u);
+            // in batches of eight loads, all in flight before the first store (one L2 round trip
+            // per batch instead of per chunk)
+            constexpr int kBatch = 8, kT = 32 * kConsumerWarps;
+            for (int i0 = threadIdx.x; i0 < NC * k8; i0 += kBatch * kT) {
+                uint4 h[kBatch];
+#pragma unroll
+                for (int u = 0; u < kBatch; u++) {
+                    const int i = i0 + u * kT, ts = i / NC, c = i % NC;  // destination: step ts of column c
+                    h[u] = i < NC * k8 && c < job.ncols ? __ldg(xg + (size_t)c * k8 + ts) : make_uint4(0u, 0u, 0u, 0u);
+                }
+#pragma unroll
+                for (int u = 0; u < kBatch; u++)
+                    if (i0 + u * kT < NC * k8) xo[i0 + u * kT] = h[u];
             }
         }
         consumers_sync();
