@@ -6,9 +6,11 @@
 // One CTA of kNormThreads threads per row (grid-stride over rows).  The steps
 // are those of bm_norm.cuh (the sum of squares exact in a 128-bit integer, the
 // mean by integer steps), shared with the fused front end of k_gemv_stream, so
-// the two give the same bits.  Each row is read three times (largest square,
-// exact sum, scaled values; the later reads hit L1/L2) and its outputs written
-// once.
+// the two give the same bits.  A row of up to 4096 values is read once into
+// registers for the sum; rows of 1025..4096 values also take their outputs from
+// there (with the norm weight's chunks loaded together), shorter ones read x once
+// more, longer ones three times (largest square, exact sum, scaled values; the
+// later reads hit L1/L2).  Outputs are written once.
 //
 // In place (out == x) is safe: every thread has finished reading the row for the
 // sum before the block barrier, and the second pass reads and writes each element
@@ -38,7 +40,11 @@ __device__ __forceinline__ uint16_t to_f16(float v)
 }
 
 // vec: x, g and out 16-byte aligned, h 8-byte aligned and k % 4 == 0, so that every
-// row keeps that alignment.
+// row keeps that alignment.  HOLD (rows of 1025..4096 values, several chunks a thread):
+// the outputs come from the chunks held for the sum, with the norm weight's chunks
+// loaded together, instead of a second pass of serial round trips; it takes more
+// registers, which rows of one chunk a thread would pay for in occupancy.
+template <bool HOLD>
 __global__ void __launch_bounds__(kNormThreads) k_rms_norm(const float *x, const float *__restrict__ g, int64_t nrows,
                                                            int64_t k, norm::Recip rk, float eps, float *out,
                                                            uint16_t *h, int vec)
@@ -50,7 +56,38 @@ __global__ void __launch_bounds__(kNormThreads) k_rms_norm(const float *x, const
     for (int64_t r = blockIdx.x; r < nrows; r += gridDim.x) {
         const float *xr = x + r * k;
         float scale;
-        if (vec && k <= 4 * 4 * kNormThreads) {  // the row's chunks held in registers: one read for the sum
+        if (HOLD) {
+            // the row's chunks held in registers: one read of x; after the reduction the norm
+            // weight's chunks, all four loads in flight together, and the outputs from the
+            // registers
+            const int64_t n4 = k >> 2;
+            float4 v[4], w[4];
+#pragma unroll
+            for (int i = 0; i < 4; i++) {
+                const int64_t c = t + i * kNormThreads;
+                v[i] = c < n4 ? reinterpret_cast<const float4 *>(xr)[c] : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            scale = norm::row_scale_held(v, (int)n4, rk, eps, t, sh, [] { __syncthreads(); });
+            __syncthreads();  // sh is refilled by the next row
+#pragma unroll
+            for (int i = 0; i < 4; i++) {
+                const int64_t c = t + i * kNormThreads;
+                w[i] = c < n4 ? __ldg(reinterpret_cast<const float4 *>(g) + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            float4 *o4 = out ? reinterpret_cast<float4 *>(out + r * k) : nullptr;
+            uint2 *h4 = h ? reinterpret_cast<uint2 *>(h + r * k) : nullptr;
+#pragma unroll
+            for (int i = 0; i < 4; i++) {
+                const int64_t c = t + i * kNormThreads;
+                if (c < n4) {
+                    const float4 o = make_float4(norm::apply(v[i].x, scale, w[i].x), norm::apply(v[i].y, scale, w[i].y),
+                                                 norm::apply(v[i].z, scale, w[i].z), norm::apply(v[i].w, scale, w[i].w));
+                    if (o4) o4[c] = o;
+                    if (h4) h4[c] = make_uint2(pack_rn(o.x, o.y), pack_rn(o.z, o.w));
+                }
+            }
+            continue;
+        } else if (vec && k <= 4 * 4 * kNormThreads) {  // the row's chunks held in registers for the sum
             const int64_t n4 = k >> 2;
             float4 v[4];
 #pragma unroll
@@ -106,7 +143,10 @@ int launch_rms_norm(const float *x, const float *g, int64_t nrows, int64_t k, fl
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl_enabled() ? 1 : 0;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, k_rms_norm, x, g, nrows, k, norm::reciprocal_of(k), eps, out, h, vec ? 1 : 0);
+    const bool hold = vec && k > 4 * kNormThreads && k <= 4 * 4 * kNormThreads;
+    cudaError_t e = hold ? cudaLaunchKernelEx(&cfg, k_rms_norm<true>, x, g, nrows, k, norm::reciprocal_of(k), eps, out, h, 1)
+                         : cudaLaunchKernelEx(&cfg, k_rms_norm<false>, x, g, nrows, k, norm::reciprocal_of(k), eps, out, h,
+                                              vec ? 1 : 0);
     if (e != cudaSuccess) return fail(BM_ERR_CUDA, "rms_norm: launch failed: %s", cudaGetErrorString(e));
     return BM_OK;
 }
