@@ -86,7 +86,9 @@ bool current_device(DeviceInfo *info, int *status)
             cudaDeviceGetAttribute(&di.minor, cudaDevAttrComputeCapabilityMinor, d) != cudaSuccess ||
             cudaDeviceGetAttribute(&di.sm_count, cudaDevAttrMultiProcessorCount, d) != cudaSuccess ||
             cudaDeviceGetAttribute(&di.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, d) !=
-                cudaSuccess)
+                cudaSuccess ||
+            cudaDeviceGetAttribute(&di.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, d) != cudaSuccess ||
+            cudaDeviceGetAttribute(&di.smem_reserved, cudaDevAttrReservedSharedMemoryPerBlock, d) != cudaSuccess)
             st = BM_ERR_CUDA;
         else if (di.major != 10 || di.minor != 3)
             st = BM_ERR_UNSUPPORTED_DEVICE;

@@ -13,6 +13,8 @@ struct DeviceInfo {
     int major = 0, minor = 0;
     int sm_count = 0;
     int max_smem_optin = 0;  // bytes of dynamic shared memory a block may opt into
+    int smem_per_sm = 0;     // bytes of shared memory of one SM
+    int smem_reserved = 0;   // bytes of it the system reserves for each resident block
 };
 
 // Fills *info for the current device; returns false (and sets the last error)

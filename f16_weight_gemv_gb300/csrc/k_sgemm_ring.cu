@@ -12,7 +12,7 @@
 // A few columns (the tokens of a small decode batch) are, like one column, bound by
 // streaming W from HBM.  So this kernel keeps the one-column kernel's machinery and
 // changes only the arithmetic: the 8-row groups of W are split evenly
-// between two CTAs per SM; a CTA walks its groups in sub-blocks and k-slices whose
+// between the CTAs (two per SM, one when that gives each SM four groups or fewer); a CTA walks its groups in sub-blocks and k-slices whose
 // stage holds up to 32 TMA boxes of 8 rows x 64 elements (128-byte swizzle: 16-byte
 // chunk c of row r at chunk c ^ (r % 8)), floor(32 / groups) boxes per group; sixteen
 // lanes of four producer warps issue a stage's boxes, each arriving on the stage's
@@ -119,23 +119,34 @@ __device__ __forceinline__ void consumers_sync() { asm volatile("bar.sync 1, %0;
 // Shared memory of the staged activation: NC columns of k f16, whole KB.
 __host__ __device__ constexpr uint32_t x_bytes(int nc, int64_t k) { return (uint32_t)((2 * nc * k + 1023) / 1024 * 1024); }
 
+// The barriers and flags behind the ring: full and empty barriers of kMaxStages stages,
+// the abort flag and the issued-stage count.
+constexpr uint32_t kTailBytes = 256;
+static_assert(2 * kMaxStages * 8 + 2 * 4 <= kTailBytes, "barrier area");
+
 template <int NC>
 __global__ void __launch_bounds__(kThreads, 2) k_sgemm_ring(const __grid_constant__ RingJob job)
 {
-    extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t full_bar[kMaxStages];
-    __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
-    __shared__ int abort_flag;
-    __shared__ int issued_slot;
-
+    // Dynamic shared memory only: with no static variables its base is the start of the
+    // block's window, 1024-byte aligned as the swizzled boxes need, so no bytes go to
+    // padding (at two CTAs per SM that is what makes room for a third stage at 2 x 4096
+    // activation elements).  Layout: the activation, the ring, the barriers and flags.
+    extern __shared__ __align__(1024) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int k = job.k;
     const int S = job.stages;
     const uint32_t xbytes = x_bytes(NC, k);
-    uint8_t *smem = smem_raw + ((1024u - (dev::smem_u32(smem_raw) & 1023u)) & 1023u);
+    if (dev::smem_u32(smem) & 1023u) {  // not the layout above: refuse without touching anything
+        if (threadIdx.x == 0) atomicExch(job.err, (unsigned)BM_ERR_UNSUPPORTED_DEVICE);
+        return;
+    }
     // the activation step-major: the 8 elements of step t of column c at 16 (t NC + c) bytes
     uint16_t *xs = reinterpret_cast<uint16_t *>(smem);
     const uint32_t ring_u = dev::smem_u32(smem) + xbytes;
+    uint64_t *const full_bar = reinterpret_cast<uint64_t *>(smem + xbytes + (size_t)S * kStageBytes);
+    uint64_t *const empty_bar = full_bar + kMaxStages;
+    int &abort_flag = *reinterpret_cast<int *>(empty_bar + kMaxStages);
+    int &issued_slot = (&abort_flag)[1];
     volatile int *abort_v = &abort_flag;
 
     if (threadIdx.x == 0) {
@@ -244,7 +255,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_sgemm_ring(const __grid_constan
                     break;
                 }
                 const int kc0 = sl * sw;
-                const uint32_t wrow = dev::smem_u32(smem) + xbytes + (uint32_t)slot * kStageBytes +
+                const uint32_t wrow = ring_u + (uint32_t)slot * kStageBytes +
                                       (uint32_t)(gw * bpg) * kBoxBytes + (uint32_t)rho * 128;
                 const uint32_t wthr = wrow | ((uint32_t)rho << 4) | (uint32_t)(4 * tq);
                 if (active) {
@@ -327,8 +338,8 @@ bool sgemm_ring_applies(const uint16_t *X, int64_t ncols, int64_t k, const Devic
     if (ncols < 2 || ncols > kSgemmStreamMaxCols || k % 8 != 0 || (reinterpret_cast<uintptr_t>(X) & 15) != 0)
         return false;
     const int64_t nc = (ncols + 1) / 2 * 2;
-    // the staged activation and two stages must fit one CTA per SM
-    return (int64_t)x_bytes((int)nc, k) + 2 * (int64_t)kStageBytes + 2048 + 1024 <= (int64_t)dev.max_smem_optin;
+    // the staged activation and two stages must fit one CTA per SM, with 3 KB to spare
+    return (int64_t)x_bytes((int)nc, k) + 2 * (int64_t)kStageBytes + 3072 <= (int64_t)dev.max_smem_optin;
 }
 
 namespace {
@@ -337,24 +348,38 @@ template <int NC>
 int launch_nc(RingJob &job, cudaStream_t s, const DeviceInfo &dev)
 {
     auto kern = k_sgemm_ring<NC>;
-    // The one-column kernel's sizing: two CTAs per SM with rings as deep as their share
-    // needs (2..8 stages); one CTA per SM when the staged activation leaves no room for
-    // two stages at two CTAs per SM.
-    const int64_t G = job.groups, k = job.k;
+    // Two CTAs per SM, each with a ring as deep as its share of the work needs (2..8
+    // stages), or one CTA per SM:
+    //  - when the rows give each SM four groups or fewer: at two CTAs per SM most CTAs
+    //    would hold one or two groups, so one or two consumer warps, each with a long
+    //    slice per stage (same-GPU A/B at 2 columns: Llama-3-8B Q 7 %, Qwen3-0.6B Q/K/V
+    //    30 %, SmolLM2 gate/up 40 % faster; 2048 x 4096 2 % slower);
+    //  - when the staged activation leaves no room for two stages at two CTAs per SM.
+    // At two CTAs per SM a CTA of four or more groups takes the stages its half of the
+    // SM holds (three at 2 x 4096 activation elements: gate 12 %, gate/up 6 %, the output
+    // product 5 % faster than two); one of fewer groups keeps two, since a third stage
+    // requested by every CTA at once only delays each CTA's first slice (Q/K/V 6144 x 4096
+    // 4 % slower with three).
+    const int64_t G = job.groups, k = job.k, sms = dev.sm_count;
     const uint32_t xbytes = x_bytes(NC, k);
-    int64_t grid = std::min<int64_t>((int64_t)dev.sm_count * 2, G);
+    int64_t grid = std::min<int64_t>(G <= 4 * sms ? sms : 2 * sms, G);
     const int64_t groups_per_cta = (G + grid - 1) / grid;
     const int64_t boxes_per_cta = groups_per_cta * ((k + kBoxCols - 1) / kBoxCols);
     const int64_t stages_needed = (boxes_per_cta + kBoxesPerStage - 1) / kBoxesPerStage + 1;
     const int64_t want = std::max<int64_t>(2, std::min<int64_t>(kMaxStages, stages_needed));
-    int64_t room = ((int64_t)dev.max_smem_optin / 2 - 2048 - 1024 - (int64_t)xbytes) / kStageBytes;
+    int64_t room = 0;
+    if (grid > sms) {
+        const int64_t share = ((int64_t)dev.smem_per_sm - 2 * (int64_t)dev.smem_reserved) / 2;  // one CTA's
+        room = (share - (int64_t)kTailBytes - (int64_t)xbytes) / kStageBytes;
+        if (groups_per_cta < 4) room = std::min<int64_t>(room, 2);
+    }
     if (room < 2) {
-        grid = std::min<int64_t>(grid, dev.sm_count);
-        room = ((int64_t)dev.max_smem_optin - 2048 - 1024 - (int64_t)xbytes) / kStageBytes;
+        grid = std::min<int64_t>(grid, sms);
+        room = ((int64_t)dev.max_smem_optin - 1024 - (int64_t)kTailBytes - (int64_t)xbytes) / kStageBytes;
         if (room < 2) return fail(BM_ERR_UNSUPPORTED_DEVICE, "sgemm ring: too little shared memory");
     }
     job.stages = (int)std::min<int64_t>(want, room);
-    const size_t smem = xbytes + (size_t)job.stages * kStageBytes + 1024;
+    const size_t smem = xbytes + (size_t)job.stages * kStageBytes + kTailBytes;
 
     int dev_id = 0;
     cudaGetDevice(&dev_id);
