@@ -353,7 +353,10 @@ int launch_nc(RingJob &job, cudaStream_t s, const DeviceInfo &dev)
     //  - when the rows give each SM four groups or fewer: at two CTAs per SM most CTAs
     //    would hold one or two groups, so one or two consumer warps, each with a long
     //    slice per stage (same-GPU A/B at 2 columns: Llama-3-8B Q 7 %, Qwen3-0.6B Q/K/V
-    //    30 %, SmolLM2 gate/up 40 % faster; 2048 x 4096 2 % slower);
+    //    30 %, SmolLM2 gate/up 40 % faster).  Its ring is capped at three stages: every
+    //    CTA requests its ring at once and the whole matrix is only a few rings, so a
+    //    deeper ring delays each CTA's first slice (Q 10.46 -> 9.82 us, 2048 x 4096
+    //    9.15 -> 8.36 with three stages instead of six; 4 columns unchanged);
     //  - when the staged activation leaves no room for two stages at two CTAs per SM.
     // At two CTAs per SM a CTA of four or more groups takes the stages its half of the
     // SM holds (three at 2 x 4096 activation elements: gate 12 %, gate/up 6 %, the output
@@ -378,6 +381,7 @@ int launch_nc(RingJob &job, cudaStream_t s, const DeviceInfo &dev)
         room = ((int64_t)dev.max_smem_optin - 1024 - (int64_t)kTailBytes - (int64_t)xbytes) / kStageBytes;
         if (room < 2) return fail(BM_ERR_UNSUPPORTED_DEVICE, "sgemm ring: too little shared memory");
     }
+    if (G <= 4 * sms) room = std::min<int64_t>(room, 3);
     job.stages = (int)std::min<int64_t>(want, room);
     const size_t smem = xbytes + (size_t)job.stages * kStageBytes + kTailBytes;
 
