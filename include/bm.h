@@ -337,8 +337,10 @@ int bm_set_pdl(int enable);
  * `ncols` is clamped to 0..8 (0 or 1: always the tensor cores).  The default, 2,
  * gives tinyBLAS's bits to two-column products, where on GB300 the exact kernel is
  * also the faster one (it streams the weights like the one-column product: Llama-3-8B
- * gate 22.6 us against 26.0 on the tensor cores, Q 11.5 against 12.8).  Larger values
- * buy tinyBLAS's bits at some speed.  Returns the previous setting.
+ * gate 20.9 us against 26.1 on the tensor cores, Q 9.9 against 12.8).  Larger values
+ * buy tinyBLAS's bits at some speed on the long products (gate at 3 columns 29.3 us
+ * against 26.1), at none on short ones (Q at 3 columns 12.6 against 12.9).  Returns the
+ * previous setting.
  */
 int bm_set_exact_sgemm_cols(int ncols);
 
