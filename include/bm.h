@@ -380,7 +380,9 @@ int bm_tc_plan(int64_t rows, int64_t k, int64_t ncols, int noalloc, int64_t *inf
 /* Waits for `stream`, then reads and clears this library's device error word
  * on the current device: BM_OK, BM_ERR_TIMEOUT (a kernel gave up a bounded
  * wait and wrote nothing trustworthy), BM_ERR_INVALID_ARG (bm_f16_get_rows met
- * an id out of range), or BM_ERR_CUDA (the wait failed). */
+ * an id out of range), BM_ERR_UNSUPPORTED_DEVICE (the bit-exact few-column kernel
+ * found its shared memory not 1024-byte aligned and wrote nothing; not seen on
+ * GB300), or BM_ERR_CUDA (the wait failed). */
 int bm_device_status(bm_stream_t stream);
 
 /* Self-test of the bounded device waits (no counterpart on the pages; it
