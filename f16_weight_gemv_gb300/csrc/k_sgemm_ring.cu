@@ -11,13 +11,13 @@
 //
 // A few columns (the tokens of a small decode batch) are, like one column, bound by
 // streaming W from HBM.  So this kernel keeps the one-column kernel's machinery and
-// changes only the arithmetic: the 8-row groups of W are split evenly
-// between the CTAs (two per SM, one when that gives each SM four groups or fewer); a CTA walks its groups in sub-blocks and k-slices whose
-// stage holds up to 32 TMA boxes of 8 rows x 64 elements (128-byte swizzle: 16-byte
-// chunk c of row r at chunk c ^ (r % 8)), floor(32 / groups) boxes per group; sixteen
-// lanes of four producer warps issue a stage's boxes, each arriving on the stage's
-// barrier with its own byte count, the weight copies starting before
-// griddepcontrol.wait.  The NC activation columns (ncols rounded up to even; a
+// changes only the arithmetic: the 8-row groups of W are split evenly between the
+// CTAs (two per SM, one when that gives each SM four groups or fewer); a CTA walks its
+// groups in sub-blocks and k-slices whose stage holds up to 32 TMA boxes of 8 rows x
+// 64 elements (128-byte swizzle: 16-byte chunk c of row r at chunk c ^ (r % 8)),
+// floor(32 / groups) boxes per group; sixteen lanes of four producer warps issue a
+// stage's boxes, each arriving on the stage's barrier with its own byte count, the
+// weight copies starting before griddepcontrol.wait.  The NC activation columns (ncols rounded up to even; a
 // padding column is zero and never stored; f16, 2 NC k bytes) are staged once per CTA
 // after the wait.
 //
