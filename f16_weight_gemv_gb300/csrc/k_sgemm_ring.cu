@@ -17,9 +17,9 @@
 // 64 elements (128-byte swizzle: 16-byte chunk c of row r at chunk c ^ (r % 8)),
 // floor(32 / groups) boxes per group; sixteen lanes of four producer warps issue a
 // stage's boxes, each arriving on the stage's barrier with its own byte count, the
-// weight copies starting before griddepcontrol.wait.  The NC activation columns (ncols rounded up to even; a
-// padding column is zero and never stored; f16, 2 NC k bytes) are staged once per CTA
-// after the wait.
+// weight copies starting before griddepcontrol.wait.  The NC activation columns (ncols
+// rounded up to even; a padding column is zero and never stored; f16, 2 NC k bytes) are
+// staged once per CTA after the wait.
 //
 // Consumers (eight warps, one group each): thread p of a row holds lanes 2p and 2p+1
 // of every column's chains and reads, per 8-element step, the 4 bytes at element
